@@ -1,0 +1,189 @@
+"""Float64 CPU oracle for Ring Attention -- TEST INFRASTRUCTURE ONLY.
+
+The arithmetic lives in ``ring_oracle.c`` (plain C, float64, optional OpenMP); this module compiles it
+with gcc on first use and wraps its functions with numpy arrays.  Only the test suite,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import this package.  The
+CUDA product path (``sequence_sharded_exact_gb300``) never imports it, and the two share no code.
+
+Every function follows the pages' definition of exact softmax attention cut into ring shards (see
+the header of ``ring_oracle.c`` for the passages and the readings taken where the pages are silent).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ring_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_ring_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+LAYOUTS = {"contiguous": 0, "zigzag": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile ring_oracle.c into _ring_oracle.so (gcc, -O2, no fast-math, no FMA contraction)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        Lg = ctypes.c_long
+        lib.oracle_natural_position.argtypes = [Lg, Lg, I, I]
+        lib.oracle_natural_position.restype = Lg
+        common = [P, P, P, I, I, I, Lg, I, I, I, I]
+        lib.oracle_attn_fwd_rows.argtypes = common + [Lg, P, P, P]
+        lib.oracle_attn_fwd.argtypes = common + [P, P]
+        lib.oracle_ring_fwd.argtypes = common + [P, P, P]
+        bcommon = [P, P, P, P, I, I, I, Lg, I, I, I, I]
+        lib.oracle_attn_bwd_dq_rows.argtypes = bcommon + [Lg, P, P]
+        lib.oracle_attn_bwd_dkv_rows.argtypes = bcommon + [Lg, P, P, P]
+        lib.oracle_attn_bwd.argtypes = bcommon + [P, P, P]
+        lib.oracle_shard_tiles.argtypes = [Lg, I, I, I, I, P]
+        lib.oracle_num_threads.argtypes = []
+        for f in ("oracle_attn_fwd_rows", "oracle_attn_fwd", "oracle_ring_fwd",
+                  "oracle_attn_bwd_dq_rows", "oracle_attn_bwd_dkv_rows", "oracle_attn_bwd",
+                  "oracle_shard_tiles", "oracle_num_threads"):
+            getattr(lib, f).restype = I
+        _lib = lib
+        return lib
+
+
+def _f32(a):
+    """Contiguous float32 numpy copy of a numpy array or torch tensor (bf16 upcasts exactly)."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu")
+        if str(a.dtype) != "torch.float32":
+            a = a.float()
+        a = a.contiguous().numpy()
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(st, what):
+    if st != 0:
+        raise ValueError(f"oracle: {what} failed with status {st}")
+
+
+def _layout(layout):
+    return LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def natural_position(r, L, n, layout):
+    """Natural sequence position of buffer row r."""
+    return int(_load().oracle_natural_position(int(r), int(L), int(n), _layout(layout)))
+
+
+def attn_fwd(q, k, v, n, causal, layout):
+    """Exact attention for every row.  q [B,H,L,d], k/v [B,Hkv,L,d] -> (out [B,H,L,d], lse [B,H,L])."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, H, L, d = q.shape
+    Hkv = k.shape[1]
+    out = np.empty((B, H, L, d), np.float64)
+    lse = np.empty((B, H, L), np.float64)
+    _check(_load().oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, L, d, int(n), int(causal),
+                                   _layout(layout), _ptr(out), _ptr(lse)), "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_rows(q, k, v, n, causal, layout, rows):
+    """Exact attention for selected rows; rows are flat indices (b*H + h)*L + r.
+    Returns (out [nrows,d], lse [nrows])."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, H, L, d = q.shape
+    Hkv = k.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, d), np.float64)
+    lse = np.empty((rows.size,), np.float64)
+    _check(_load().oracle_attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, L, d, int(n),
+                                        int(causal), _layout(layout), rows.size, _ptr(rows),
+                                        _ptr(out), _ptr(lse)), "attn_fwd_rows")
+    return out, lse
+
+
+def ring_fwd(q, k, v, n, causal, layout):
+    """The n-step ring walk with the page's online-softmax update.
+    Returns (out, lse, pairs[n,n]) where pairs[i,j] counts visible (query,key) pairs of step (i,j)."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, H, L, d = q.shape
+    Hkv = k.shape[1]
+    out = np.empty((B, H, L, d), np.float64)
+    lse = np.empty((B, H, L), np.float64)
+    pairs = np.zeros((n, n), np.int64)
+    _check(_load().oracle_ring_fwd(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, L, d, int(n), int(causal),
+                                   _layout(layout), _ptr(out), _ptr(lse), _ptr(pairs)), "ring_fwd")
+    return out, lse, pairs
+
+
+def attn_bwd(q, k, v, dout, n, causal, layout):
+    """Gradients of sum(out * dout) w.r.t. q, k, v for every row: (dq, dk, dv) float64."""
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, H, L, d = q.shape
+    Hkv = k.shape[1]
+    dq = np.empty((B, H, L, d), np.float64)
+    dk = np.empty((B, Hkv, L, d), np.float64)
+    dv = np.empty((B, Hkv, L, d), np.float64)
+    _check(_load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, H, Hkv, L, d, int(n),
+                                   int(causal), _layout(layout), _ptr(dq), _ptr(dk), _ptr(dv)),
+           "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_dq_rows(q, k, v, dout, n, causal, layout, rows):
+    """dQ for selected query rows (flat (b*H + h)*L + r) -> [nrows, d]."""
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, H, L, d = q.shape
+    Hkv = k.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    dq = np.empty((rows.size, d), np.float64)
+    _check(_load().oracle_attn_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, H, Hkv, L, d,
+                                           int(n), int(causal), _layout(layout), rows.size,
+                                           _ptr(rows), _ptr(dq)), "attn_bwd_dq_rows")
+    return dq
+
+
+def attn_bwd_dkv_rows(q, k, v, dout, n, causal, layout, keys):
+    """dK, dV for selected key rows (flat (b*Hkv + g)*L + t) -> ([nkeys, d], [nkeys, d])."""
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, H, L, d = q.shape
+    Hkv = k.shape[1]
+    keys = np.ascontiguousarray(keys, dtype=np.int64)
+    dk = np.empty((keys.size, d), np.float64)
+    dv = np.empty((keys.size, d), np.float64)
+    _check(_load().oracle_attn_bwd_dkv_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, H, Hkv, L, d,
+                                            int(n), int(causal), _layout(layout), keys.size,
+                                            _ptr(keys), _ptr(dk), _ptr(dv)), "attn_bwd_dkv_rows")
+    return dk, dv
+
+
+def shard_tiles(L, n, causal, layout, tile=128):
+    """Per query shard, the number of (query tile, key tile) pairs holding a visible pair."""
+    out = np.zeros((n,), np.int64)
+    _check(_load().oracle_shard_tiles(int(L), int(n), int(causal), _layout(layout), int(tile),
+                                      _ptr(out)), "shard_tiles")
+    return out
