@@ -1,0 +1,173 @@
+/*
+ * ringattn.h -- C ABI of libringattn.so: Ring Attention's blockwise exact attention on one GB300.
+ *
+ * What is computed (sources are web pages on Ring Attention, cited by title and section):
+ *   The sequence of length L is cut into n shards; shard i holds Q_i, K_i, V_i
+ *   (airsota "M4-051 Ring Attention and sequence parallelism", section 3).  At ring step
+ *   r = 0..n-1 shard i takes the K/V block of shard (i - r) mod n, computes the block attention
+ *   S = Q K^T / sqrt(d) and folds it into a running max / running sum / running output
+ *   (LLM-101-CN "distributed hands-on code", section 6.2, block_attention and forward; "Lecture 30:
+ *   TP/PP/SP/CP", section 3.2).  After n steps the output O / L equals full softmax attention.
+ *   Causal: a key is visible to a query iff its natural position is <= the query's; blocks that
+ *   are entirely masked are skipped (M4-051 sections 3 and 5).  Zigzag layout: the sequence is cut
+ *   into 2n chunks and shard i holds chunks i and 2n-1-i, which equalises causal work
+ *   (M4-051 section 4 item 2; Lecture 30 section 3.2, "Zigzag / Striped").
+ *   On one GPU the n shards are virtual: they are row ranges of the same buffers, and the ring
+ *   schedule is the order in which the kernels walk K/V tiles.  No data moves between shards.
+ *
+ * Conventions shared by every entry point:
+ *   - Layout of the sequence axis: every buffer stores it in the layout's order, i.e. as the
+ *     concatenation of the shards' local buffers (shard i occupies rows [i*L/n, (i+1)*L/n)).
+ *     With RA_LAYOUT_ZIGZAG, rows [i*S, i*S + C) of shard i are natural positions [i*C, (i+1)*C)
+ *     and rows [i*S + C, (i+1)*S) are natural positions [(2n-1-i)*C, (2n-i)*C), with S = L/n and
+ *     C = L/(2n).  Outputs come back in the same order as the inputs.
+ *   - Shapes (row-major, d contiguous): q, out, dout, dq: [B][H][L][d]; k, v, dk, dv:
+ *     [B][Hkv][L][d]; lse: [B][H][L] float32, natural logarithm of sum_t exp(s_t).
+ *     Query head h reads kv head h / (H / Hkv) (grouped-query attention).  Scale is 1/sqrt(d).
+ *   - dtype: RA_F32 (float) or RA_BF16 (bfloat16) for q, k, v, out, dout.  Accumulation is float32.
+ *   - Pointers are DEVICE pointers unless stated otherwise, allocated and owned by the caller,
+ *     16-byte aligned.  The library never allocates or frees device memory and keeps no pointer
+ *     after a call returns.
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).  Work is enqueued on
+ *     it; no call synchronises the host unless stated.
+ *   - Errors: arguments are checked before anything is enqueued; a rejected call returns
+ *     RA_ERR_INVALID_ARG or RA_ERR_UNSUPPORTED and enqueues nothing.  A failed launch returns
+ *     RA_ERR_CUDA.  ring_attn_last_error() gives a message for the calling thread's last failure.
+ *     Kernels never trap: every wait inside a kernel is bounded, and a wait that runs out sets a
+ *     device status word (read it with ring_attn_device_status) and the kernel returns.
+ *     Nothing throws across this interface.
+ */
+#ifndef RINGATTN_H
+#define RINGATTN_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define RA_API __attribute__((visibility("default")))
+#else
+#define RA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int ra_status;
+#define RA_OK 0
+#define RA_ERR_INVALID_ARG 1
+#define RA_ERR_UNSUPPORTED 2
+#define RA_ERR_CUDA 3
+#define RA_ERR_NO_DEVICE 4
+#define RA_ERR_TIMEOUT 5
+
+#define RA_LAYOUT_CONTIGUOUS 0
+#define RA_LAYOUT_ZIGZAG 1
+
+#define RA_F32 0
+#define RA_BF16 1
+
+/* Kernel paths reported by ring_attn_fwd_path / ring_attn_bwd_path. */
+#define RA_PATH_SIMT 1      /* CUDA-core kernels: any shape, f32 or bf16 */
+#define RA_PATH_TCGEN05 2   /* tensor-core kernels (TMA + tcgen05 + TMEM): bf16, d = 128,
+                               shard (contiguous) or chunk (zigzag) length a multiple of 256 */
+
+/* Device status bits (ring_attn_device_status). */
+#define RA_DEVICE_TIMEOUT 1u
+
+/*
+ * ring_attn_fwd -- the whole ring forward in one launch.
+ * For every shard i and ring step r = 0..n_shards-1, the rows of shard i attend to the K/V of
+ * shard (i - r) mod n_shards, with the running-max / running-sum rescale of LLM-101-CN section 6.2,
+ * fully masked causal blocks skipped (M4-051 section 3).  Writes out (dtype) and lse.
+ *   q, k, v   inputs as above (dtype);   out [B][H][L][d] (dtype);   lse [B][H][L] float32.
+ *   L % n_shards == 0; zigzag also needs L % (2 n_shards) == 0; H % Hkv == 0; d in {64, 128}.
+ */
+RA_API ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int B, int H, int Hkv, int L, int d, int n_shards, int causal, int layout,
+                        int dtype, void* stream);
+
+/*
+ * ring_attn_ring_step_fwd -- ring step `step` alone, for all shards at once: shard i attends to
+ * the K/V of shard (i - step) mod n_shards only (one block_attention of LLM-101-CN section 6.2).
+ *   o_part [B][H][L][d] float32 receives each row's attention output normalised by its own sum;
+ *   lse_part [B][H][L] float32 its log-sum-exp.  A row that sees no key in that block gets
+ *   o_part = 0 and lse_part = -infinity.  Fold the steps together with ring_attn_lse_merge.
+ */
+RA_API ra_status ring_attn_ring_step_fwd(const void* q, const void* k, const void* v, float* o_part,
+                                  float* lse_part, int B, int H, int Hkv, int L, int d,
+                                  int n_shards, int step, int causal, int layout, int dtype,
+                                  void* stream);
+
+/*
+ * ring_attn_lse_merge -- fold one partial result into a running one, in place:
+ *   lse = max(a, b) + log(1 + exp(-|a - b|)),  o = exp(a - lse) o_acc + exp(b - lse) o_part,
+ * with a = lse_acc, b = lse_part (the online-softmax merge across ring steps, LLM-101-CN 6.2,
+ * written for normalised partials).  A partial with lse = -infinity leaves the row unchanged.
+ *   o_acc, o_part: [rows][d] float32;  lse_acc, lse_part: [rows] float32;  rows >= 0, d >= 1.
+ */
+RA_API ra_status ring_attn_lse_merge(float* o_acc, float* lse_acc, const float* o_part,
+                              const float* lse_part, long long rows, int d, void* stream);
+
+/*
+ * ring_attn_fwd_stepwise -- the ring forward run step by step, as the multi-device algorithm
+ * does it: n_shards launches of the ring step followed by the LSE merge, then the conversion of
+ * the float32 accumulator into `out`.  Same arguments and results as ring_attn_fwd, plus
+ *   workspace: device memory of at least ring_attn_fwd_stepwise_workspace_size(...) bytes,
+ *   256-byte aligned, owned by the caller; its contents on entry do not matter.
+ */
+RA_API ra_status ring_attn_fwd_stepwise(const void* q, const void* k, const void* v, void* out,
+                                 float* lse, int B, int H, int Hkv, int L, int d, int n_shards,
+                                 int causal, int layout, int dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+RA_API size_t ring_attn_fwd_stepwise_workspace_size(int B, int H, int L, int d);
+
+/*
+ * ring_attn_bwd -- gradients of sum(out * dout) with respect to q, k and v, recomputing the
+ * attention weights P = exp(s - lse) from the saved lse (the pages give no backward; this is the
+ * derivative of the forward definition): D = rowsum(dout * out), dS = P (dout . v - D),
+ * dq = dS k / sqrt(d), dk = dS^T q / sqrt(d), dv = P^T dout, with dk and dv summed over the
+ * query heads that share a kv head.  Causal blocks that are entirely masked are skipped.
+ *   out, lse: the forward's results for the same inputs.  dout: [B][H][L][d] (dtype).
+ *   dq [B][H][L][d], dk and dv [B][Hkv][L][d] in grad_dtype (RA_F32 or RA_BF16).
+ *   workspace: device memory of at least ring_attn_bwd_workspace_size(...) bytes (256-byte
+ *   aligned; contents on entry do not matter), owned by the caller.
+ */
+RA_API ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        int grad_dtype, void* workspace, size_t workspace_bytes, int B, int H,
+                        int Hkv, int L, int d, int n_shards, int causal, int layout, int dtype,
+                        void* stream);
+RA_API size_t ring_attn_bwd_workspace_size(int B, int H, int Hkv, int L, int d, int grad_dtype);
+
+/*
+ * ring_attn_shard_tiles -- HOST ONLY, no CUDA call.  For each query shard, the number of
+ * (query tile, key tile) pairs of `tile` x `tile` buffer rows (tiles start at each shard's first
+ * row) that hold at least one visible (query, key) pair: the per-shard causal work that the
+ * contiguous layout leaves unbalanced (device i's work grows with i, M4-051 section 4 item 2) and
+ * the zigzag layout equalises.  tiles_per_shard: HOST array of n_shards entries.
+ */
+RA_API ra_status ring_attn_shard_tiles(int L, int n_shards, int causal, int layout, int tile,
+                                long long* tiles_per_shard);
+
+/* Which kernel path ring_attn_fwd / ring_attn_bwd take for these arguments (RA_PATH_*), written
+ * to *path (HOST pointer).  Same argument checks as the calls themselves; no CUDA call. */
+RA_API ra_status ring_attn_fwd_path(int B, int H, int Hkv, int L, int d, int n_shards, int causal,
+                             int layout, int dtype, int* path);
+RA_API ra_status ring_attn_bwd_path(int B, int H, int Hkv, int L, int d, int n_shards, int causal,
+                             int layout, int dtype, int* path);
+
+/* Reads the device status word of the current device into *status (HOST pointer; bits
+ * RA_DEVICE_*), then clears it.  Synchronises `stream`. */
+RA_API ra_status ring_attn_device_status(unsigned int* status, void* stream);
+
+/* Message for the calling thread's last non-OK status ("" if none).  Never NULL. */
+RA_API const char* ring_attn_last_error(void);
+
+/* ABI version (incremented on any incompatible change). */
+RA_API int ring_attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RINGATTN_H */

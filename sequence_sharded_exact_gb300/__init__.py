@@ -1,0 +1,20 @@
+"""GB300-native Ring Attention: blockwise exact attention over n virtual sequence shards.
+
+The compute path is the C-ABI library ``libringattn.so`` (hand-written sm_103a CUDA kernels); this
+package is a thin binding over it.  Importing the package does not load the library; the first
+call does, and fails loudly if the library has not been built (``python -c "import
+__graft_entry__ as g; g.build()"``).
+"""
+from .binding import (  # noqa: F401
+    RingAttnError,
+    bwd_workspace_size,
+    device_status,
+    fwd,
+    bwd,
+    fwd_path,
+    bwd_path,
+    library,
+    lse_merge,
+    ring_step_fwd,
+    shard_tiles,
+)

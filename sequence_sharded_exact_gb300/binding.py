@@ -1,0 +1,242 @@
+"""ctypes binding of libringattn.so (include/ringattn.h).  Argument marshalling only: every step of
+the computation runs in the library's CUDA kernels.  torch is used for device memory and streams.
+
+The library is loaded on first use from this package's directory; if it has not been built the
+call raises RingAttnError (there is no fallback of any kind).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libringattn.so")
+
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_NO_DEVICE, RA_ERR_TIMEOUT = range(6)
+LAYOUTS = {"contiguous": 0, "zigzag": 1}
+PATHS = {1: "simt", 2: "tcgen05"}
+RA_DEVICE_TIMEOUT = 1
+
+_lock = threading.Lock()
+_lib = None
+
+EXPORTS = (
+    "ring_attn_fwd", "ring_attn_ring_step_fwd", "ring_attn_lse_merge", "ring_attn_fwd_stepwise",
+    "ring_attn_fwd_stepwise_workspace_size", "ring_attn_bwd", "ring_attn_bwd_workspace_size",
+    "ring_attn_shard_tiles", "ring_attn_fwd_path", "ring_attn_bwd_path", "ring_attn_device_status",
+    "ring_attn_last_error", "ring_attn_abi_version",
+)
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"libringattn status {status}: {msg}")
+        self.status = status
+
+
+def library():
+    """The loaded ctypes library (raises RingAttnError if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RingAttnError(-1, f"{LIB_PATH} is missing: build it with "
+                                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, LL, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t
+        shape = [I] * 9  # B H Hkv L d n causal layout dtype  (order varies per call, set below)
+        del shape
+        lib.ring_attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P]
+        lib.ring_attn_ring_step_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
+        lib.ring_attn_lse_merge.argtypes = [P, P, P, P, LL, I, P]
+        lib.ring_attn_fwd_stepwise.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P]
+        lib.ring_attn_fwd_stepwise_workspace_size.argtypes = [I, I, I, I]
+        lib.ring_attn_fwd_stepwise_workspace_size.restype = SZ
+        lib.ring_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, P, SZ, I, I, I, I, I, I, I, I,
+                                      I, P]
+        lib.ring_attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
+        lib.ring_attn_bwd_workspace_size.restype = SZ
+        lib.ring_attn_shard_tiles.argtypes = [I, I, I, I, I, P]
+        lib.ring_attn_fwd_path.argtypes = [I, I, I, I, I, I, I, I, I, P]
+        lib.ring_attn_bwd_path.argtypes = [I, I, I, I, I, I, I, I, I, P]
+        lib.ring_attn_device_status.argtypes = [P, P]
+        lib.ring_attn_last_error.argtypes = []
+        lib.ring_attn_last_error.restype = ctypes.c_char_p
+        lib.ring_attn_abi_version.argtypes = []
+        for name in EXPORTS:
+            f = getattr(lib, name)
+            if f.restype is ctypes.c_int or name in ("ring_attn_fwd", "ring_attn_ring_step_fwd",
+                                                     "ring_attn_lse_merge", "ring_attn_fwd_stepwise",
+                                                     "ring_attn_bwd", "ring_attn_shard_tiles",
+                                                     "ring_attn_fwd_path", "ring_attn_bwd_path",
+                                                     "ring_attn_device_status",
+                                                     "ring_attn_abi_version"):
+                f.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(status):
+    if status != RA_OK:
+        msg = library().ring_attn_last_error().decode(errors="replace")
+        raise RingAttnError(status, msg)
+
+
+def _dtype_code(dt):
+    if dt == torch.float32:
+        return 0
+    if dt == torch.bfloat16:
+        return 1
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def _layout(layout):
+    return LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dims(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B,H,L,d] and k, v [B,Hkv,L,d]")
+    B, H, L, d = q.shape
+    Hkv = k.shape[1]
+    return int(B), int(H), int(Hkv), int(L), int(d)
+
+
+def _need(t, name, device):
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fwd_path(B, H, Hkv, L, d, n_shards, causal, layout, dtype):
+    out = ctypes.c_int(0)
+    _check(library().ring_attn_fwd_path(B, H, Hkv, L, d, n_shards, int(causal), _layout(layout),
+                                        _dtype_code(dtype), ctypes.byref(out)))
+    return PATHS[out.value]
+
+
+def bwd_path(B, H, Hkv, L, d, n_shards, causal, layout, dtype):
+    out = ctypes.c_int(0)
+    _check(library().ring_attn_bwd_path(B, H, Hkv, L, d, n_shards, int(causal), _layout(layout),
+                                        _dtype_code(dtype), ctypes.byref(out)))
+    return PATHS[out.value]
+
+
+def fwd(q, k, v, n_shards, causal=True, layout="zigzag", out=None, lse=None, stream=None):
+    """Ring Attention forward.  Returns (out [B,H,L,d] q.dtype, lse [B,H,L] float32)."""
+    B, H, Hkv, L, d = _dims(q, k)
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, nm, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    _need(out, "out", q.device)
+    _need(lse, "lse", q.device)
+    _check(library().ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, L, d,
+                                   int(n_shards), int(causal), _layout(layout), _dtype_code(q.dtype),
+                                   _stream(stream, q.device)))
+    return out, lse
+
+
+def ring_step_fwd(q, k, v, n_shards, step, causal=True, layout="zigzag", o_part=None,
+                  lse_part=None, stream=None):
+    """One ring step for all shards.  Returns (o_part float32 [B,H,L,d], lse_part [B,H,L])."""
+    B, H, Hkv, L, d = _dims(q, k)
+    if o_part is None:
+        o_part = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    _check(library().ring_attn_ring_step_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o_part),
+                                             _ptr(lse_part), B, H, Hkv, L, d, int(n_shards),
+                                             int(step), int(causal), _layout(layout),
+                                             _dtype_code(q.dtype), _stream(stream, q.device)))
+    return o_part, lse_part
+
+
+def lse_merge(o_acc, lse_acc, o_part, lse_part, stream=None):
+    """In-place merge of a partial (o_part, lse_part) into (o_acc, lse_acc); float32 tensors."""
+    d = int(o_acc.shape[-1])
+    rows = int(lse_acc.numel())
+    for t, nm in ((o_acc, "o_acc"), (lse_acc, "lse_acc"), (o_part, "o_part"), (lse_part, "lse_part")):
+        _need(t, nm, o_acc.device)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{nm} must be float32")
+    _check(library().ring_attn_lse_merge(_ptr(o_acc), _ptr(lse_acc), _ptr(o_part), _ptr(lse_part),
+                                         rows, d, _stream(stream, o_acc.device)))
+    return o_acc, lse_acc
+
+
+def fwd_stepwise(q, k, v, n_shards, causal=True, layout="zigzag", out=None, lse=None,
+                 workspace=None, stream=None):
+    """The ring forward run as n ring-step launches plus LSE merges (same results as fwd)."""
+    B, H, Hkv, L, d = _dims(q, k)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    need = library().ring_attn_fwd_stepwise_workspace_size(B, H, L, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(library().ring_attn_fwd_stepwise(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
+                                            Hkv, L, d, int(n_shards), int(causal),
+                                            _layout(layout), _dtype_code(q.dtype),
+                                            _ptr(workspace), workspace.numel(),
+                                            _stream(stream, q.device)))
+    return out, lse
+
+
+def bwd_workspace_size(B, H, Hkv, L, d, grad_dtype=torch.float32):
+    return int(library().ring_attn_bwd_workspace_size(B, H, Hkv, L, d, _dtype_code(grad_dtype)))
+
+
+def bwd(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigzag",
+        grad_dtype=torch.float32, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Ring Attention backward.  Returns (dq, dk, dv) in grad_dtype."""
+    B, H, Hkv, L, d = _dims(q, k)
+    if dq is None:
+        dq = torch.empty((B, H, L, d), dtype=grad_dtype, device=q.device)
+    if dk is None:
+        dk = torch.empty((B, Hkv, L, d), dtype=grad_dtype, device=q.device)
+    if dv is None:
+        dv = torch.empty((B, Hkv, L, d), dtype=grad_dtype, device=q.device)
+    need = bwd_workspace_size(B, H, Hkv, L, d, grad_dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(library().ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _dtype_code(grad_dtype),
+                                   _ptr(workspace), workspace.numel(), B, H, Hkv, L, d,
+                                   int(n_shards), int(causal), _layout(layout),
+                                   _dtype_code(q.dtype), _stream(stream, q.device)))
+    return dq, dk, dv
+
+
+def shard_tiles(L, n_shards, causal=True, layout="zigzag", tile=128):
+    """Host-only: per query shard, the (query tile, key tile) pairs with a visible pair."""
+    arr = (ctypes.c_longlong * n_shards)()
+    _check(library().ring_attn_shard_tiles(int(L), int(n_shards), int(causal), _layout(layout),
+                                           int(tile), arr))
+    return [int(x) for x in arr]
+
+
+def device_status(stream=None, device=None):
+    """Reads and clears the device status word (bit RA_DEVICE_TIMEOUT: a bounded wait ran out)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    st = ctypes.c_uint(0)
+    _check(library().ring_attn_device_status(ctypes.byref(st), _stream(stream, dev)))
+    return int(st.value)

@@ -1,0 +1,406 @@
+// api.cu -- the C ABI of libringattn (declared in include/ringattn.h): argument checks, path
+// selection, workspace carving, the device status word and the host-side shard scheduler queries.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "../../include/ringattn.h"
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+thread_local std::string g_last_error;
+
+ra_status fail(ra_status st, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+ra_status cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(RA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device status word: kernels set bits here when a bounded wait runs out.
+__device__ unsigned int g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+
+int current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+// Device address of the status word for the current device (looked up once per device).
+unsigned int* status_word(cudaError_t* err)
+{
+    int dev = current_device();
+    *err = cudaSuccess;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        *err = cudaGetSymbolAddress(&p, g_device_status);
+        if (*err != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+ra_status check_device()
+{
+    int n = 0;
+    cudaError_t e = cudaGetDeviceCount(&n);
+    if (e != cudaSuccess || n == 0) {
+        cudaGetLastError();
+        return fail(RA_ERR_NO_DEVICE, "no CUDA device available (%s)", cudaGetErrorName(e));
+    }
+    return RA_OK;
+}
+
+ra_status check_problem(const Problem& p)
+{
+    if (p.B < 1 || p.H < 1 || p.Hkv < 1 || p.L < 1 || p.n < 1)
+        return fail(RA_ERR_INVALID_ARG, "B, H, Hkv, L, n_shards must be >= 1 (got %d %d %d %d %d)",
+                    p.B, p.H, p.Hkv, p.L, p.n);
+    if (p.H % p.Hkv != 0)
+        return fail(RA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", p.H, p.Hkv);
+    if (p.L % p.n != 0)
+        return fail(RA_ERR_INVALID_ARG, "L (%d) must be a multiple of n_shards (%d)", p.L, p.n);
+    if (p.layout != RA_LAYOUT_CONTIGUOUS && p.layout != RA_LAYOUT_ZIGZAG)
+        return fail(RA_ERR_INVALID_ARG, "unknown layout %d", p.layout);
+    if (p.layout == RA_LAYOUT_ZIGZAG && p.L % (2 * p.n) != 0)
+        return fail(RA_ERR_INVALID_ARG, "zigzag layout needs L (%d) to be a multiple of 2*n_shards",
+                    p.L);
+    if (p.causal != 0 && p.causal != 1)
+        return fail(RA_ERR_INVALID_ARG, "causal must be 0 or 1 (got %d)", p.causal);
+    if (p.dtype != RA_F32 && p.dtype != RA_BF16)
+        return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", p.dtype);
+    if (p.d != 64 && p.d != 128)
+        return fail(RA_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", p.d);
+    if ((long long)p.B * p.H * p.L * p.d >= (1LL << 40))
+        return fail(RA_ERR_UNSUPPORTED, "problem too large");
+    return RA_OK;
+}
+
+ra_status check_ptrs(std::initializer_list<const void*> ptrs)
+{
+    int i = 0;
+    for (const void* x : ptrs) {
+        if (!x) return fail(RA_ERR_INVALID_ARG, "pointer argument %d is NULL", i);
+        if (!aligned16(x)) return fail(RA_ERR_INVALID_ARG, "pointer argument %d is not 16-byte aligned", i);
+        ++i;
+    }
+    return RA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+int device_sm_count()
+{
+    int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 148;
+    if (g_sm_count[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1) v = 148;
+        g_sm_count[dev] = v;
+    }
+    return g_sm_count[dev];
+}
+
+}  // namespace ra
+
+using namespace ra;
+
+extern "C" {
+
+int ring_attn_abi_version(void) { return 1; }
+
+const char* ring_attn_last_error(void) { return g_last_error.c_str(); }
+
+ra_status ring_attn_fwd_path(int B, int H, int Hkv, int L, int d, int n_shards, int causal,
+                             int layout, int dtype, int* path)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if (!path) return fail(RA_ERR_INVALID_ARG, "path is NULL");
+    *path = tc_fwd_supported(p) ? RA_PATH_TCGEN05 : RA_PATH_SIMT;
+    return RA_OK;
+}
+
+ra_status ring_attn_bwd_path(int B, int H, int Hkv, int L, int d, int n_shards, int causal,
+                             int layout, int dtype, int* path)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if (!path) return fail(RA_ERR_INVALID_ARG, "path is NULL");
+    *path = tc_bwd_supported(p) ? RA_PATH_TCGEN05 : RA_PATH_SIMT;
+    return RA_OK;
+}
+
+ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                        int H, int Hkv, int L, int d, int n_shards, int causal, int layout,
+                        int dtype, void* stream)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if ((st = check_ptrs({q, k, v, out, lse})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (tc_fwd_supported(p)) {
+        unsigned int* sw = status_word(&e);
+        if (!sw) return cuda_fail(e, "status word");
+        e = launch_fwd_tc(p, q, k, v, out, lse, kFwdFused, 0, sw, s);
+    } else {
+        e = launch_fwd_simt(p, q, k, v, out, lse, kFwdFused, 0, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_fwd launch");
+    return RA_OK;
+}
+
+ra_status ring_attn_ring_step_fwd(const void* q, const void* k, const void* v, float* o_part,
+                                  float* lse_part, int B, int H, int Hkv, int L, int d,
+                                  int n_shards, int step, int causal, int layout, int dtype,
+                                  void* stream)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if (step < 0 || step >= n_shards)
+        return fail(RA_ERR_INVALID_ARG, "step %d outside [0, n_shards)", step);
+    if ((st = check_ptrs({q, k, v, o_part, lse_part})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (tc_fwd_supported(p)) {
+        unsigned int* sw = status_word(&e);
+        if (!sw) return cuda_fail(e, "status word");
+        e = launch_fwd_tc(p, q, k, v, o_part, lse_part, kFwdRingStep, step, sw, s);
+    } else {
+        e = launch_fwd_simt(p, q, k, v, o_part, lse_part, kFwdRingStep, step, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_ring_step_fwd launch");
+    return RA_OK;
+}
+
+ra_status ring_attn_lse_merge(float* o_acc, float* lse_acc, const float* o_part,
+                              const float* lse_part, long long rows, int d, void* stream)
+{
+    if (rows < 0 || d < 1) return fail(RA_ERR_INVALID_ARG, "rows must be >= 0 and d >= 1");
+    if (rows == 0) return RA_OK;
+    ra_status st = check_ptrs({o_acc, lse_acc, o_part, lse_part});
+    if (st != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaError_t e = launch_lse_merge(o_acc, lse_acc, o_part, lse_part, rows, d,
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_lse_merge launch");
+    return RA_OK;
+}
+
+size_t ring_attn_fwd_stepwise_workspace_size(int B, int H, int L, int d)
+{
+    if (B < 1 || H < 1 || L < 1 || d < 1) return 0;
+    const size_t rows = (size_t)B * H * L;
+    return 2 * align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+ra_status ring_attn_fwd_stepwise(const void* q, const void* k, const void* v, void* out,
+                                 float* lse, int B, int H, int Hkv, int L, int d, int n_shards,
+                                 int causal, int layout, int dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if ((st = check_ptrs({q, k, v, out, lse, workspace})) != RA_OK) return st;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const size_t need = ring_attn_fwd_stepwise_workspace_size(B, H, L, d);
+    if (workspace_bytes < need)
+        return fail(RA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    if ((st = check_device()) != RA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long rows = p.q_rows();
+    char* ws = static_cast<char*>(workspace);
+    float* o_acc = reinterpret_cast<float*>(ws);
+    float* o_part = reinterpret_cast<float*>(ws + align256((size_t)rows * d * sizeof(float)));
+    float* lse_part = reinterpret_cast<float*>(ws + 2 * align256((size_t)rows * d * sizeof(float)));
+    const bool tc = tc_fwd_supported(p);
+    cudaError_t e = cudaSuccess;
+    unsigned int* sw = nullptr;
+    if (tc && !(sw = status_word(&e))) return cuda_fail(e, "status word");
+    for (int step = 0; step < n_shards && e == cudaSuccess; ++step) {
+        float* o_dst = step == 0 ? o_acc : o_part;
+        float* l_dst = step == 0 ? lse : lse_part;
+        e = tc ? launch_fwd_tc(p, q, k, v, o_dst, l_dst, kFwdRingStep, step, sw, s)
+               : launch_fwd_simt(p, q, k, v, o_dst, l_dst, kFwdRingStep, step, s);
+        if (e == cudaSuccess && step > 0) e = launch_lse_merge(o_acc, lse, o_part, lse_part, rows, d, s);
+    }
+    if (e == cudaSuccess) e = launch_convert(o_acc, out, dtype, rows * d, 1.0f, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_fwd_stepwise launch");
+    return RA_OK;
+}
+
+size_t ring_attn_bwd_workspace_size(int B, int H, int Hkv, int L, int d, int grad_dtype)
+{
+    (void)Hkv;
+    if (B < 1 || H < 1 || L < 1 || d < 1) return 0;
+    const size_t rows = (size_t)B * H * L;
+    size_t bytes = align256(rows * sizeof(float));                   // D
+    if (grad_dtype != RA_F32) bytes += align256(rows * d * sizeof(float));  // dQ accumulator
+    return bytes;
+}
+
+ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        int grad_dtype, void* workspace, size_t workspace_bytes, int B, int H,
+                        int Hkv, int L, int d, int n_shards, int causal, int layout, int dtype,
+                        void* stream)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if (grad_dtype != RA_F32 && grad_dtype != RA_BF16)
+        return fail(RA_ERR_INVALID_ARG, "unknown grad dtype %d", grad_dtype);
+    if ((st = check_ptrs({q, k, v, out, lse, dout, dq, dk, dv, workspace})) != RA_OK) return st;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const size_t need = ring_attn_bwd_workspace_size(B, H, Hkv, L, d, grad_dtype);
+    if (workspace_bytes < need)
+        return fail(RA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    if ((st = check_device()) != RA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long rows = p.q_rows();
+    char* ws = static_cast<char*>(workspace);
+    float* D = reinterpret_cast<float*>(ws);
+    cudaError_t e = launch_bwd_preprocess(out, dout, dtype, rows, d, D, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_bwd preprocess launch");
+    if (tc_bwd_supported(p)) {
+        unsigned int* sw = status_word(&e);
+        if (!sw) return cuda_fail(e, "status word");
+        float* dq_acc = grad_dtype == RA_F32
+                            ? static_cast<float*>(dq)
+                            : reinterpret_cast<float*>(ws + align256((size_t)rows * sizeof(float)));
+        e = launch_zero(dq_acc, rows * d, s);
+        if (e == cudaSuccess)
+            e = launch_bwd_tc(p, q, k, v, dout, D, lse, dq_acc, dk, dv, grad_dtype, sw, s);
+        if (e == cudaSuccess && grad_dtype != RA_F32)
+            e = launch_convert(dq_acc, dq, grad_dtype, rows * d, 1.0f, s);
+    } else {
+        e = launch_bwd_simt(p, q, k, v, dout, D, lse, dq, dk, dv, grad_dtype, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_bwd launch");
+    return RA_OK;
+}
+
+ra_status ring_attn_device_status(unsigned int* status, void* stream)
+{
+    if (!status) return fail(RA_ERR_INVALID_ARG, "status is NULL");
+    ra_status st = check_device();
+    if (st != RA_OK) return st;
+    cudaError_t e;
+    unsigned int* sw = status_word(&e);
+    if (!sw) return cuda_fail(e, "status word");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int host = 0;
+    e = cudaMemcpyAsync(&host, sw, sizeof(host), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(sw, 0, sizeof(unsigned int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_device_status");
+    *status = host;
+    return RA_OK;
+}
+
+// Host-side shard scheduler query.  Tiles are `tile` consecutive buffer rows from each shard's
+// first row; a (query tile, key tile) pair counts when the smallest natural key position of the
+// key tile does not exceed the largest natural query position of the query tile.  The per-tile
+// extremes come from the chunk geometry, and the count uses the sorted key minima.
+ra_status ring_attn_shard_tiles(int L, int n_shards, int causal, int layout, int tile,
+                                long long* tiles_per_shard)
+{
+    if (!tiles_per_shard) return fail(RA_ERR_INVALID_ARG, "tiles_per_shard is NULL");
+    if (tile < 1) return fail(RA_ERR_INVALID_ARG, "tile must be >= 1");
+    Problem p{1, 1, 1, L, 64, n_shards, causal, layout, RA_F32};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    const Geometry g = p.geo();
+    const long long tps = (g.S + tile - 1) / tile;
+    const long long nt = tps * g.n;
+    long long* kmin = new (std::nothrow) long long[nt];
+    long long* qmax = new (std::nothrow) long long[nt];
+    if (!kmin || !qmax) {
+        delete[] kmin;
+        delete[] qmax;
+        return fail(RA_ERR_INVALID_ARG, "out of host memory");
+    }
+    for (long long x = 0; x < nt; ++x) {
+        const int shard = (int)(x / tps);
+        const int r0 = shard * g.S + (int)(x % tps) * tile;
+        const int r1 = r0 + tile < (shard + 1) * g.S ? r0 + tile : (shard + 1) * g.S;
+        long long lo = (long long)1 << 62, hi = -1;
+        // the tile's rows split into runs of consecutive natural positions, one per chunk
+        for (int r = r0; r < r1;) {
+            const int c = r / g.Lc;
+            const int run_end = (c + 1) * g.Lc < r1 ? (c + 1) * g.Lc : r1;
+            const long long a = natural_position(g, r), b = natural_position(g, run_end - 1);
+            lo = a < lo ? a : lo;
+            hi = b > hi ? b : hi;
+            r = run_end;
+        }
+        kmin[x] = lo;
+        qmax[x] = hi;
+    }
+    // sort key minima (insertion into a counting array over natural positions)
+    long long* hist = new (std::nothrow) long long[(size_t)L + 1];
+    if (!hist) {
+        delete[] kmin;
+        delete[] qmax;
+        return fail(RA_ERR_INVALID_ARG, "out of host memory");
+    }
+    memset(hist, 0, sizeof(long long) * ((size_t)L + 1));
+    for (long long x = 0; x < nt; ++x) hist[kmin[x]] += 1;
+    for (int pos = 1; pos <= L; ++pos) hist[pos] += hist[pos - 1];  // hist[p] = #tiles with min <= p
+    for (int i = 0; i < g.n; ++i) {
+        long long cnt = 0;
+        for (long long a = 0; a < tps; ++a) {
+            const long long x = (long long)i * tps + a;
+            cnt += causal ? hist[qmax[x]] : nt;
+        }
+        tiles_per_shard[i] = cnt;
+    }
+    delete[] hist;
+    delete[] kmin;
+    delete[] qmax;
+    return RA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// ra_internal.h -- declarations shared by the translation units of libringattn (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ra_geometry.h"
+
+namespace ra {
+
+// Arguments of one attention problem, validated by the entry points.
+struct Problem {
+    int B, H, Hkv, L, d, n, causal, layout, dtype;
+    Geometry geo() const { return make_geometry(L, n, layout, causal); }
+    long long q_rows() const { return (long long)B * H * L; }
+    long long kv_rows() const { return (long long)B * Hkv * L; }
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Output mode of a forward kernel.
+enum FwdMode {
+    kFwdFused = 0,     // all ring steps, write out (dtype) + lse
+    kFwdRingStep = 1,  // one ring step, write float32 partial + lse (-inf when nothing visible)
+};
+
+// SIMT (CUDA-core) kernels: any shape, f32 or bf16 inputs.
+cudaError_t launch_fwd_simt(const Problem& p, const void* q, const void* k, const void* v,
+                            void* out, float* lse, int mode, int step, cudaStream_t s);
+cudaError_t launch_bwd_simt(const Problem& p, const void* q, const void* k, const void* v,
+                            const void* dout, const float* D, const float* lse, void* dq,
+                            void* dk, void* dv, int grad_dtype, cudaStream_t s);
+
+// Tensor-core kernels (TMA + tcgen05 + TMEM), bf16, d = 128, chunk length % 256 == 0.
+bool tc_fwd_supported(const Problem& p);
+cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v,
+                          void* out, float* lse, int mode, int step, unsigned int* status,
+                          cudaStream_t s);
+bool tc_bwd_supported(const Problem& p);
+cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
+                          const void* dout, const float* D, const float* lse, float* dq_acc,
+                          void* dk, void* dv, int grad_dtype, unsigned int* status,
+                          cudaStream_t s);
+
+// HBM-bound helper kernels.
+cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part,
+                             const float* lse_part, long long rows, int d, cudaStream_t s);
+cudaError_t launch_convert(const float* src, void* dst, int dst_dtype, long long count,
+                           float scale, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, int dtype, long long rows,
+                                  int d, float* D, cudaStream_t s);
+cudaError_t launch_zero(float* dst, long long count, cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace ra

@@ -1,0 +1,103 @@
+"""CPU-only checks of the C ABI: the library loads without a GPU, exports every declared entry
+point, rejects bad arguments before touching CUDA, and its host-side shard scheduler agrees with
+the oracle's brute-force tile counter."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import oracle
+from sequence_sharded_exact_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ringattn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ring_attn_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return binding.library()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("ring_attn_fwd", "ring_attn_bwd", "ring_attn_ring_step_fwd", "ring_attn_lse_merge",
+                 "ring_attn_shard_tiles", "ring_attn_last_error"):
+        assert want in names
+    assert set(names) == set(binding.EXPORTS), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.ring_attn_abi_version() == 1
+
+
+def _fwd(lib, **kw):
+    a = dict(q=16, k=16, v=16, out=16, lse=16, B=1, H=2, Hkv=1, L=1024, d=128, n=4, causal=1,
+             layout=1, dtype=1)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.ring_attn_fwd(P(a["q"]), P(a["k"]), P(a["v"]), P(a["out"]), P(a["lse"]), a["B"],
+                             a["H"], a["Hkv"], a["L"], a["d"], a["n"], a["causal"], a["layout"],
+                             a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), binding.RA_ERR_INVALID_ARG),
+    (dict(k=8), binding.RA_ERR_INVALID_ARG),           # not 16-byte aligned
+    (dict(H=3, Hkv=2), binding.RA_ERR_INVALID_ARG),    # H % Hkv
+    (dict(L=1000, n=3), binding.RA_ERR_INVALID_ARG),   # L % n
+    (dict(L=1026, n=6), binding.RA_ERR_INVALID_ARG),   # zigzag needs L % 2n
+    (dict(d=96), binding.RA_ERR_UNSUPPORTED),
+    (dict(layout=7), binding.RA_ERR_INVALID_ARG),
+    (dict(dtype=5), binding.RA_ERR_INVALID_ARG),
+    (dict(causal=2), binding.RA_ERR_INVALID_ARG),
+    (dict(B=0), binding.RA_ERR_INVALID_ARG),
+])
+def test_argument_errors_before_any_cuda_call(lib, kw, status):
+    assert _fwd(lib, **kw) == status
+    assert lib.ring_attn_last_error().decode()
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
+def test_no_device_answer(lib):
+    assert _fwd(lib) == binding.RA_ERR_NO_DEVICE
+
+
+def test_path_selection():
+    assert binding.fwd_path(1, 32, 8, 131072, 128, 8, True, "zigzag", torch.bfloat16) == "tcgen05"
+    assert binding.fwd_path(2, 8, 8, 8192, 128, 8, True, "contiguous", torch.bfloat16) == "tcgen05"
+    assert binding.fwd_path(1, 1, 1, 256, 64, 4, False, "contiguous", torch.float32) == "simt"
+    assert binding.fwd_path(1, 2, 2, 384, 128, 3, True, "zigzag", torch.bfloat16) == "simt"
+    assert binding.fwd_path(1, 2, 2, 512, 64, 2, True, "zigzag", torch.bfloat16) == "simt"
+
+
+@pytest.mark.parametrize("L,n,T", [(8192, 8, 128), (32768, 8, 128), (1000, 5, 64), (384, 3, 128),
+                                   (4096, 16, 128), (96, 4, 7)])
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_shard_tiles_match_oracle(L, n, T, layout, causal):
+    if layout == "zigzag" and L % (2 * n):
+        pytest.skip("zigzag needs L % 2n == 0")
+    got = binding.shard_tiles(L, n, causal, layout, T)
+    assert got == oracle.shard_tiles(L, n, causal, layout, T).tolist()
+
+
+def test_shard_tiles_workloads():
+    assert binding.shard_tiles(8192, 8, True, "contiguous") == [36 + 64 * i for i in range(8)]
+    assert binding.shard_tiles(131072, 8, True, "zigzag") == [65600] * 8
+    assert binding.shard_tiles(65536, 16, True, "zigzag") == [8208] * 16
+
+
+def test_workspace_sizes(lib):
+    assert binding.bwd_workspace_size(1, 32, 8, 65536, 128, torch.float32) >= 32 * 65536 * 4
+    assert binding.bwd_workspace_size(1, 32, 8, 65536, 128, torch.bfloat16) >= 32 * 65536 * 129 * 4
+    assert lib.ring_attn_fwd_stepwise_workspace_size(1, 2, 1024, 128) >= 2 * 2 * 1024 * 128 * 4

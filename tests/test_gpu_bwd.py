@@ -1,0 +1,69 @@
+"""GPU parity of the backward path (through the C ABI) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_sharded_exact_gb300 as ra
+from sequence_sharded_exact_gb300 import synth
+from parity_util import assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    torch.cuda.set_device(0)
+    ra.device_status()
+    yield
+    assert ra.device_status() == 0, "a bounded wait ran out inside a kernel"
+
+
+def run_bwd(B, H, Hkv, L, d, n, causal, layout, dtype, grad_dtype, seed, expect_path=None):
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=dtype, seed=seed, with_dout=True)
+    if expect_path:
+        assert ra.bwd_path(B, H, Hkv, L, d, n, causal, layout, dtype) == expect_path
+    q, k, v, do = (x[t].to(DEV) for t in ("q", "k", "v", "dout"))
+    out, lse = ra.fwd(q, k, v, n, causal, layout)
+    dq, dk, dv = ra.bwd(q, k, v, out, lse, do, n, causal, layout, grad_dtype=grad_dtype)
+    torch.cuda.synchronize()
+    rq, rk, rv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], n, causal, layout)
+    # the backward reads the forward's rounded output; bf16 tolerances apply to bf16 inputs
+    for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        assert got.dtype == grad_dtype
+        assert_close(to_np(got), ref, dtype, name)
+
+
+BWD_CASES = [
+    # B, H, Hkv, L, d, n, causal, layout, dtype
+    (1, 1, 1, 256, 64, 4, False, "contiguous", torch.float32),
+    (1, 2, 1, 384, 64, 3, True, "zigzag", torch.float32),
+    (1, 4, 2, 512, 128, 2, True, "zigzag", torch.bfloat16),
+    (1, 2, 2, 1024, 128, 4, True, "contiguous", torch.bfloat16),
+    (2, 4, 1, 512, 128, 4, True, "zigzag", torch.bfloat16),
+    (1, 2, 1, 600, 128, 3, True, "contiguous", torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,d,n,causal,layout,dtype", BWD_CASES)
+@pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
+def test_bwd_matches_oracle(B, H, Hkv, L, d, n, causal, layout, dtype, grad_dtype):
+    if grad_dtype == torch.bfloat16 and dtype == torch.float32:
+        pytest.skip("bf16 gradients are only offered for bf16 inputs in this suite")
+    run_bwd(B, H, Hkv, L, d, n, causal, layout, dtype, grad_dtype, seed=L + n)
+
+
+def test_bwd_sum_identities_on_device():
+    """Sum over keys of dV equals the group's summed dO; the sum of dK over keys vanishes."""
+    B, H, Hkv, L, d, n = 1, 4, 2, 1024, 128, 4
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=torch.bfloat16, seed=12, with_dout=True)
+    q, k, v, do = (x[t].to(DEV) for t in ("q", "k", "v", "dout"))
+    out, lse = ra.fwd(q, k, v, n, True, "zigzag")
+    dq, dk, dv = ra.bwd(q, k, v, out, lse, do, n, True, "zigzag")
+    torch.cuda.synchronize()
+    G = H // Hkv
+    dsum = x["dout"].double().view(B, Hkv, G, L, d).sum(dim=(2, 3))
+    assert torch.allclose(dv.double().cpu().sum(dim=2), dsum, atol=0.05, rtol=1e-3)
+    assert dk.double().cpu().sum(dim=2).abs().max().item() < 0.05

@@ -1,0 +1,161 @@
+"""GPU parity of the forward path (through the C ABI) against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_sharded_exact_gb300 as ra
+from sequence_sharded_exact_gb300 import synth
+from parity_util import assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    torch.cuda.set_device(0)
+    ra.device_status()
+    yield
+    assert ra.device_status() == 0, "a bounded wait ran out inside a kernel"
+
+
+def inputs(B, H, Hkv, L, d, dtype, seed, spike=0.0, dout=False):
+    return synth.make_inputs(B, H, Hkv, L, d, dtype=dtype, seed=seed, spike_frac=spike,
+                             with_dout=dout, device="cpu")
+
+
+def run_fwd_full(B, H, Hkv, L, d, n, causal, layout, dtype, seed, spike=0.0, expect_path=None):
+    x = inputs(B, H, Hkv, L, d, dtype, seed, spike)
+    if expect_path:
+        assert ra.fwd_path(B, H, Hkv, L, d, n, causal, layout, dtype) == expect_path
+    q, k, v = (x[t].to(DEV) for t in ("q", "k", "v"))
+    out, lse = ra.fwd(q, k, v, n, causal, layout)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attn_fwd(x["q"], x["k"], x["v"], n, causal, layout)
+    assert_close(to_np(out), ref_o, dtype, "out")
+    assert_close(to_np(lse), ref_l, dtype, "lse")
+    return out, lse, x
+
+
+def test_tiny_f32_workload():
+    """The tiny fp32 workload: B1 H1 d64 L256 n4, non-causal, contiguous (max-abs 1e-4)."""
+    w = synth.WORKLOADS["tiny_f32"]
+    run_fwd_full(w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"], w["causal"], w["layout"],
+                 w["dtype"], w["seed"], expect_path="simt")
+
+
+TC_CASES = [
+    # B, H, Hkv, L, n, causal, layout
+    (1, 2, 2, 512, 1, True, "contiguous"),
+    (1, 2, 1, 1024, 2, True, "zigzag"),
+    (2, 4, 2, 2048, 4, True, "zigzag"),
+    (1, 4, 4, 1024, 4, False, "contiguous"),
+    (1, 8, 2, 2048, 2, False, "zigzag"),
+    (1, 4, 1, 4096, 8, True, "zigzag"),
+    (1, 2, 2, 768, 3, True, "contiguous"),   # odd number of 256-row blocks
+    (1, 3, 1, 1280, 1, True, "contiguous"),  # n = 1, odd blocks, GQA 3:1
+    (1, 4, 2, 2048, 8, True, "contiguous"),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,n,causal,layout", TC_CASES)
+def test_tcgen05_fwd_matches_oracle(B, H, Hkv, L, n, causal, layout):
+    run_fwd_full(B, H, Hkv, L, 128, n, causal, layout, torch.bfloat16, seed=L + n + H,
+                 expect_path="tcgen05")
+
+
+def test_tcgen05_fwd_large_keys():
+    """1% of key rows scaled x8: the running maximum jumps late in the walk."""
+    run_fwd_full(1, 4, 2, 2048, 128, 4, True, "zigzag", torch.bfloat16, seed=5, spike=0.01,
+                 expect_path="tcgen05")
+
+
+SIMT_CASES = [
+    # B, H, Hkv, L, d, n, causal, layout, dtype
+    (1, 2, 1, 1000, 128, 5, True, "contiguous", torch.bfloat16),   # ragged: S = 200
+    (1, 2, 2, 384, 128, 3, True, "zigzag", torch.bfloat16),        # chunks of 64
+    (1, 2, 2, 512, 64, 2, True, "zigzag", torch.bfloat16),         # head dim 64
+    (2, 4, 2, 640, 128, 5, True, "zigzag", torch.float32),
+    (1, 2, 1, 300, 64, 3, False, "contiguous", torch.float32),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,d,n,causal,layout,dtype", SIMT_CASES)
+def test_simt_fwd_matches_oracle(B, H, Hkv, L, d, n, causal, layout, dtype):
+    run_fwd_full(B, H, Hkv, L, d, n, causal, layout, dtype, seed=L + d, expect_path="simt")
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,d,n,layout,dtype", [
+    (1, 4, 2, 1024, 128, 4, "zigzag", torch.bfloat16),       # tensor-core ring steps
+    (1, 2, 2, 1024, 128, 2, "contiguous", torch.bfloat16),
+    (1, 2, 1, 600, 64, 3, "zigzag", torch.float32),          # SIMT ring steps
+])
+def test_stepwise_ring_matches_oracle_and_fused(B, H, Hkv, L, d, n, layout, dtype):
+    """n ring-step launches folded with the LSE merge equal full attention and the fused kernel."""
+    x = inputs(B, H, Hkv, L, d, dtype, seed=77)
+    q, k, v = (x[t].to(DEV) for t in ("q", "k", "v"))
+    out_s, lse_s = ra.fwd_stepwise(q, k, v, n, True, layout)
+    out_f, lse_f = ra.fwd(q, k, v, n, True, layout)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attn_fwd(x["q"], x["k"], x["v"], n, True, layout)
+    assert_close(to_np(out_s), ref_o, dtype, "stepwise out")
+    assert_close(to_np(lse_s), ref_l, dtype, "stepwise lse")
+    assert_close(to_np(out_s), to_np(out_f), dtype, "stepwise vs fused")
+
+
+@pytest.mark.parametrize("d,L,dtype", [(128, 1024, torch.bfloat16), (64, 400, torch.float32)])
+def test_ring_step_skips_future_shards(d, L, dtype):
+    """Contiguous causal: at step r the shards i < r face a later shard and see nothing
+    (o = 0, lse = -inf); every other shard gets its block's attention."""
+    n = 4
+    S = L // n
+    x = inputs(1, 2, 1, L, d, dtype, seed=3)
+    q, k, v = (x[t].to(DEV) for t in ("q", "k", "v"))
+    for step in range(n):
+        o, lse = ra.ring_step_fwd(q, k, v, n, step, True, "contiguous")
+        torch.cuda.synchronize()
+        lse_np = lse.cpu().numpy()
+        for i in range(n):
+            rows = slice(i * S, (i + 1) * S)
+            if i < step:
+                assert np.all(np.isneginf(lse_np[:, :, rows]))
+                assert torch.count_nonzero(o[:, :, rows]).item() == 0
+            else:
+                assert np.all(np.isfinite(lse_np[:, :, rows]))
+
+
+def test_constant_v_gives_constant_output():
+    x = inputs(1, 4, 2, 1024, 128, torch.bfloat16, seed=9)
+    c = torch.randn(128, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    v = c.expand(1, 2, 1024, 128).contiguous().to(DEV)
+    out, _ = ra.fwd(x["q"].to(DEV), x["k"].to(DEV), v, 4, True, "zigzag")
+    torch.cuda.synchronize()
+    err = (out.float().cpu() - c.float()).abs().max().item()
+    assert err <= 2e-2 * max(1.0, c.float().abs().max().item())
+
+
+def test_lse_merge_kernel():
+    """Merging two partials of a row set equals the log-sum-exp combination of their weights."""
+    rows, d = 1000, 128
+    g = torch.Generator().manual_seed(4)
+    oa, ob = torch.randn(rows, d, generator=g), torch.randn(rows, d, generator=g)
+    la, lb = torch.randn(rows, generator=g) * 5, torch.randn(rows, generator=g) * 5
+    lb[::7] = float("-inf")   # empty partials leave the row unchanged
+    la[::11] = float("-inf")  # empty accumulators take the partial
+    la[::77] = float("-inf")
+    o_acc, l_acc = oa.clone().to(DEV), la.clone().to(DEV)
+    ra.lse_merge(o_acc, l_acc, ob.to(DEV), lb.to(DEV))
+    torch.cuda.synchronize()
+    a64, b64 = la.double(), lb.double()
+    lse = torch.logaddexp(a64, b64)
+    wa = torch.where(torch.isneginf(a64), 0.0, torch.exp(a64 - lse))
+    wb = torch.where(torch.isneginf(b64), 0.0, torch.exp(b64 - lse))
+    oa64 = torch.where(torch.isneginf(a64)[:, None], 0.0, oa.double())
+    ref_o = wa[:, None] * oa64 + wb[:, None] * ob.double()
+    got_o = o_acc.cpu().double()
+    both_empty = torch.isneginf(a64) & torch.isneginf(b64)
+    ref_o[both_empty] = got_o[both_empty]
+    assert torch.allclose(l_acc.cpu().double(), lse, atol=1e-5, rtol=0, equal_nan=False)
+    assert (got_o - ref_o).abs().max().item() < 1e-5
