@@ -1,0 +1,423 @@
+"""Benchmark of the Ring Attention hot path on GB300 (prints ONE JSON line on rank 0).
+
+Default workload: the long-context forward -- B=1, H=32 query heads, Hkv=8, d=128, L=131072 cut
+into n=8 shards of 16384, causal, zigzag layout, bf16, 1% of key rows x8 -- i.e. the
+configuration the throughput target is stated on.  One step = one ring-attention forward over the
+whole sequence (one launch of the fused tensor-core kernel).  Secondary measurements in the same
+line: the training workload (L=65536, n=16, forward + backward), the step-by-step ring (ring-step
+kernel + LSE merge per step) on the long-context workload, and the merge kernel's bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}] [--no-extra]
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same workload.
+For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of the workload (the
+sharded multi-device ring is not exercised on one-GPU machines); value = all ranks' work / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "zigzag_gqa_128k"
+TRAIN_WORKLOAD = "zigzag_gqa_64k_train"
+METRIC = "ring-attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
+
+
+def fwd_flops(B, H, L, d, causal):
+    """Algorithmic forward flops: 4 B H L^2 d (QK^T and PV), halved when causal."""
+    f = 4.0 * B * H * L * L * d
+    return f / 2 if causal else f
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p["bf16_tflops"], p["bf16_tflops_sustained"], p["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_launches(fn, steps, warmup, stream):
+    """Warm up, then time `steps` calls with CUDA events on `stream`; returns per-call ms list."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def sample_rows(B, H, L, count, seed):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(B * H * L, size=count, replace=False))
+
+
+def oracle_calibrate(x, w, target_s, seed=7):
+    """Number of random query rows the float64 oracle handles in about target_s seconds."""
+    import oracle
+
+    B, H, L, n = w["B"], w["H"], w["L"], w["n"]
+    arrs = tuple(x[t].float().cpu().numpy() for t in ("q", "k", "v"))
+    count, limit = 32, B * H * L // 4
+    while True:
+        rows = sample_rows(B, H, L, count, seed)
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(*arrs, n, w["causal"], w["layout"], rows)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 8 or count >= limit:
+            break
+        count = int(min(limit, count * 2))
+    return arrs, max(16, min(limit, int(count * target_s / max(dt, 1e-3))))
+
+
+def oracle_sample(arrs, w, count, seed):
+    """Times the float64 oracle on `count` random query rows of the workload.
+    Returns (TFLOP/s, seconds, rows, cores, algorithmic flops of those rows)."""
+    import oracle
+
+    B, H, L, d, n = w["B"], w["H"], w["L"], w["d"], w["n"]
+    rows = sample_rows(B, H, L, count, seed)
+    t0 = time.perf_counter()
+    oracle.attn_fwd_rows(*arrs, n, w["causal"], w["layout"], rows)
+    dt = time.perf_counter() - t0
+    flops = sum(row_flops(int(r), B, H, L, d, n, w["causal"], w["layout"]) for r in rows)
+    return flops / dt / 1e12, dt, len(rows), oracle.num_threads(), flops
+
+
+def row_flops(idx, B, H, L, d, n, causal, layout):
+    """Algorithmic flops of one query row: 4 d per visible key."""
+    import oracle
+
+    if not causal:
+        return 4.0 * d * L
+    p = oracle.natural_position(idx % L, L, n, layout)
+    return 4.0 * d * (p + 1)
+
+
+def run_reference(args, w):
+    """--impl reference: the float64 CPU oracle, timed on bounded samples of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from sequence_sharded_exact_gb300 import synth
+
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    x = synth.make_inputs(w["B"], w["H"], w["Hkv"], w["L"], w["d"], dtype=w["dtype"],
+                          seed=w["seed"], spike_frac=w["spike_frac"], device="cpu", gen_device=gen)
+    per_step = max(2.0, 90.0 / max(1, args.steps + args.warmup))
+    arrs, count = oracle_calibrate(x, w, per_step)
+    del x
+    secs, rows_total, cores, flops_total = 0.0, 0, 1, 0.0
+    for s in range(args.warmup + args.steps):
+        _, dt, rows, cores, flops = oracle_sample(arrs, w, count, seed=100 + s)
+        if s >= args.warmup:
+            secs += dt
+            rows_total += rows
+            flops_total += flops
+    value = flops_total / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / max(1, args.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{count} random query rows of the workload per step, "
+                                   f"{args.steps} timed steps (float64 two-pass attention rows)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w):
+    return {"workload": f"ring attention fwd, B{w['B']} H{w['H']} Hkv{w['Hkv']} d{w['d']} "
+                        f"L{w['L']} n{w['n']} {'causal' if w['causal'] else 'full'} {w['layout']}",
+            "B": w["B"], "H": w["H"], "Hkv": w["Hkv"], "L": w["L"], "d": w["d"], "n_shards": w["n"],
+            "causal": w["causal"], "layout": w["layout"], "tile": 128,
+            "key_rows_x8": w["spike_frac"],
+            "l2": f"inputs ({(w['H'] + 2 * w['Hkv']) * w['B'] * w['L'] * w['d'] * 2 / 1e9:.2f} GB) "
+                  "larger than L2; no flush"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--oracle-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="synthetic workload name (default: the long-context forward)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from sequence_sharded_exact_gb300 import synth
+
+    w = dict(synth.WORKLOADS[args.workload])
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import sequence_sharded_exact_gb300 as ra
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist = dist_mod
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+
+    B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=w["dtype"], seed=w["seed"] + rank,
+                          spike_frac=w["spike_frac"], device=dev, gen_device=dev)
+    q, k, v = x["q"], x["k"], x["v"]
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    path = ra.fwd_path(B, H, Hkv, L, d, n, w["causal"], w["layout"], w["dtype"])
+    flops = fwd_flops(B, H, L, d, w["causal"])
+
+    def step():
+        ra.fwd(q, k, v, n, w["causal"], w["layout"], out=out, lse=lse, stream=stream)
+
+    # timed region: barrier + synchronize on both sides, CUDA events on the launch stream
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        ev0.record(stream)
+        for a, b in per:
+            a.record(stream)
+            step()
+            b.record(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    total_ms = ev0.elapsed_time(ev1)
+    launch_ms = [a.elapsed_time(b) for a, b in per]
+    status = ra.device_status()
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
+
+    peak_b, peak_s, hbm, peak_kind = peaks()
+    kernel_ms = statistics.mean(launch_ms)
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: q,k,v ~ N(0,1) bf16, 1% of key rows x8, seeded",
+        "config": config_dict(w),
+        "fraction_of_peak": value / world / peak_b,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_b, "unit": "TFLOP/s",
+                     "frac": achieved / peak_b, "traffic": None,
+                     "peak_kind": f"{peak_kind} bf16 burst (MEASURED_PEAKS bf16_tflops)",
+                     "frac_of_sustained": achieved / peak_s,
+                     "kernel": "fwd_tc_kernel", "algorithmic_flops_per_launch": flops},
+        "gpu_launches": args.steps,
+        "path": path,
+        "device_status": status,
+    }
+
+    # end to end: pinned host buffers -> device, the C-ABI call, result -> host, every step
+    if rank == 0 or dist:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        e2e_steps = max(2, args.steps // 2)
+        e2e_ms = sum(time_launches(e2e_step, e2e_steps, 1, stream)) / e2e_steps
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+        line["e2e"] = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e2e_ms}
+        del hq, hk, hv, hout, hlse
+
+    line["clocks"] = clk.summary()
+
+    if rank == 0 and not args.no_extra:
+        line["extra"] = secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args)
+    if rank == 0:
+        arrs, count = oracle_calibrate(x, w, args.oracle_seconds)
+        tf, secs, rows, cores, oflops = oracle_sample(arrs, w, count, seed=11)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{rows} random query rows of the workload "
+                                          f"({oflops / 1e9:.1f} GFLOP, {secs:.1f} s, float64)"}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
+    """Training workload (fwd + bwd), stepwise ring with LSE merge, and the merge bandwidth."""
+    from sequence_sharded_exact_gb300 import synth
+
+    res = {}
+    B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
+    steps = max(2, min(args.steps, 5))
+    # stepwise ring: n ring-step launches + n-1 merges + conversion
+    ws = torch.empty(ra.library().ring_attn_fwd_stepwise_workspace_size(B, H, L, d),
+                     dtype=torch.uint8, device=dev)
+    out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
+    ms = time_launches(lambda: ra.fwd_stepwise(x["q"], x["k"], x["v"], n, w["causal"], w["layout"],
+                                               out=out2, lse=lse2, workspace=ws, stream=stream),
+                       steps, 1, stream)
+    flops = fwd_flops(B, H, L, d, w["causal"])
+    res["stepwise_fwd"] = {"tflops": flops / (statistics.mean(ms) / 1e3) / 1e12,
+                           "ms": statistics.mean(ms), "launches": 2 * n}
+    # LSE merge kernel alone: bytes = rows * (3 d + 3) * 4 (read o_acc, o_part, write o_acc, lse)
+    rows = B * H * L
+    o_acc = ws[: rows * d * 4].view(torch.float32).view(rows, d)
+    part = torch.randn(rows, d, device=dev)
+    la = torch.randn(rows, device=dev)
+    lb = torch.randn(rows, device=dev)
+    ms = time_launches(lambda: ra.lse_merge(o_acc, la, part, lb, stream=stream), 10, 3, stream)
+    gbytes = rows * (3 * d + 3) * 4 / 1e9
+    res["lse_merge"] = {"GB/s": gbytes / (statistics.mean(ms) / 1e3), "peak_GB/s": hbm,
+                        "frac": gbytes / (statistics.mean(ms) / 1e3) / hbm, "ms": statistics.mean(ms)}
+    del ws, out2, lse2, part, la, lb, o_acc
+    # training workload: forward + backward
+    t = synth.WORKLOADS[TRAIN_WORKLOAD]
+    xt = synth.make_workload(TRAIN_WORKLOAD, device=dev, gen_device=dev)
+    Bt, Ht, Hkt, Lt, dt_, nt = t["B"], t["H"], t["Hkv"], t["L"], t["d"], t["n"]
+    ot, lt = ra.fwd(xt["q"], xt["k"], xt["v"], nt, t["causal"], t["layout"])
+    dq = torch.empty(xt["q"].shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(xt["k"].shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(xt["v"].shape, dtype=torch.float32, device=dev)
+    wsb = torch.empty(max(256, ra.bwd_workspace_size(Bt, Ht, Hkt, Lt, dt_, torch.float32)),
+                      dtype=torch.uint8, device=dev)
+
+    def train_step():
+        ra.fwd(xt["q"], xt["k"], xt["v"], nt, t["causal"], t["layout"], out=ot, lse=lt, stream=stream)
+        ra.bwd(xt["q"], xt["k"], xt["v"], ot, lt, xt["dout"], nt, t["causal"], t["layout"],
+               dq=dq, dk=dk, dv=dv, workspace=wsb, stream=stream)
+
+    bwd_steps = 2 if ra.bwd_path(Bt, Ht, Hkt, Lt, dt_, nt, t["causal"], t["layout"],
+                                 t["dtype"]) == "tcgen05" else 0
+    ff = fwd_flops(Bt, Ht, Lt, dt_, t["causal"])
+    if bwd_steps:
+        ms = time_launches(train_step, bwd_steps, 1, stream)
+        res["train_fwd_bwd"] = {"workload": f"B{Bt} H{Ht} Hkv{Hkt} d{dt_} L{Lt} n{nt} causal zigzag",
+                                "tflops": 3.5 * ff / (statistics.mean(ms) / 1e3) / 1e12,
+                                "ms": statistics.mean(ms),
+                                "flops": "fwd 4BHL^2d/2 + bwd 2.5x fwd"}
+    else:
+        res["train_fwd_bwd"] = {"skipped": "backward runs on the CUDA-core path for this shape"}
+    fms = time_launches(lambda: ra.fwd(xt["q"], xt["k"], xt["v"], nt, t["causal"], t["layout"],
+                                       out=ot, lse=lt, stream=stream), 3, 1, stream)
+    res["train_fwd_only"] = {"tflops": ff / (statistics.mean(fms) / 1e3) / 1e12,
+                             "ms": statistics.mean(fms)}
+    res["device_status"] = ra.device_status()
+    return res
+
+
+if __name__ == "__main__":
+    main()

@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     bwd_workspace_size,
     device_status,
     fwd,
+    fwd_stepwise,
     bwd,
     fwd_path,
     bwd_path,

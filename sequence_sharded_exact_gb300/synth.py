@@ -34,29 +34,36 @@ WORKLOADS = {
 
 
 def make_inputs(B, H, Hkv, L, d, dtype=torch.bfloat16, seed=0, spike_frac=0.0, spike_scale=8.0,
-                with_dout=False, device="cpu"):
+                with_dout=False, device="cpu", gen_device="cpu"):
     """Return a dict with q, k, v (and dout) on `device`, already rounded to `dtype`.
 
-    The draw happens on the CPU generator so that the values do not depend on the device."""
-    g = torch.Generator(device="cpu")
+    The draw happens on the generator of `gen_device` ("cpu" by default, so that the values do
+    not depend on where they are used; "cuda" draws the large workloads quickly, from the device's
+    own generator stream)."""
+    g = torch.Generator(device=gen_device)
     g.manual_seed(int(seed))
-    q = torch.randn((B, H, L, d), generator=g, dtype=torch.float32)
-    k = torch.randn((B, Hkv, L, d), generator=g, dtype=torch.float32)
-    v = torch.randn((B, Hkv, L, d), generator=g, dtype=torch.float32)
-    dout = torch.randn((B, H, L, d), generator=g, dtype=torch.float32) if with_dout else None
+    f32 = dict(generator=g, dtype=torch.float32, device=gen_device)
+    q = torch.randn((B, H, L, d), **f32)
+    k = torch.randn((B, Hkv, L, d), **f32)
+    v = torch.randn((B, Hkv, L, d), **f32)
+    dout = torch.randn((B, H, L, d), **f32) if with_dout else None
     if spike_frac > 0.0:
         count = int(round(spike_frac * L))
         for bh in range(B * Hkv):
-            rows = torch.randperm(L, generator=g)[:count]
+            rows = torch.randperm(L, generator=g, device=gen_device)[:count]
             k.view(B * Hkv, L, d)[bh, rows] *= spike_scale
     out = {"q": q, "k": k, "v": v}
     if dout is not None:
         out["dout"] = dout
-    return {name: t.to(dtype).to(device) for name, t in out.items()}
+    res = {}
+    for name in list(out):
+        res[name] = out.pop(name).to(dtype).to(device)
+    return res
 
 
-def make_workload(name, device="cpu", with_dout=None):
+def make_workload(name, device="cpu", with_dout=None, gen_device="cpu"):
     w = WORKLOADS[name]
     wd = w["backward"] if with_dout is None else with_dout
     return make_inputs(w["B"], w["H"], w["Hkv"], w["L"], w["d"], dtype=w["dtype"], seed=w["seed"],
-                       spike_frac=w["spike_frac"], with_dout=wd, device=device)
+                       spike_frac=w["spike_frac"], with_dout=wd, device=device,
+                       gen_device=gen_device)

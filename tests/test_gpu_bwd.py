@@ -33,7 +33,7 @@ def run_bwd(B, H, Hkv, L, d, n, causal, layout, dtype, grad_dtype, seed, expect_
     # the backward reads the forward's rounded output; bf16 tolerances apply to bf16 inputs
     for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
         assert got.dtype == grad_dtype
-        assert_close(to_np(got), ref, dtype, name)
+        assert_close(to_np(got), ref, dtype, name, stored_bf16=grad_dtype == torch.bfloat16)
 
 
 BWD_CASES = [
