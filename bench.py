@@ -42,6 +42,20 @@ def fwd_flops(B, H, L, d, causal):
     return f / 2 if causal else f
 
 
+def max_over_ranks(value, dist_mod=None, device="cpu"):
+    """The largest of every rank's value (identity without a process group)."""
+    if dist_mod is None:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_step, steps, max_total_ms):
+    """All ranks' algorithmic work over the slowest rank's time, in TFLOP/s."""
+    return world * flops_per_step * steps / (max_total_ms / 1e3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -290,12 +304,9 @@ def main():
     total_ms = ev0.elapsed_time(ev1)
     launch_ms = [a.elapsed_time(b) for a, b in per]
     status = ra.device_status()
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
+    value = whole_job_tflops(world, flops, args.steps, total_ms)
 
     peak_b, peak_s, hbm, peak_kind = peaks()
     kernel_ms = statistics.mean(launch_ms)

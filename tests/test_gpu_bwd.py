@@ -36,6 +36,25 @@ def run_bwd(B, H, Hkv, L, d, n, causal, layout, dtype, grad_dtype, seed, expect_
         assert_close(to_np(got), ref, dtype, name, stored_bf16=grad_dtype == torch.bfloat16)
 
 
+TC_BWD_CASES = [
+    # B, H, Hkv, L, n, causal, layout  (bf16, d = 128: tensor-core backward)
+    (1, 1, 1, 256, 1, True, "contiguous"),
+    (1, 2, 2, 512, 2, False, "contiguous"),
+    (1, 4, 1, 1024, 4, True, "zigzag"),
+    (2, 4, 2, 1024, 2, True, "zigzag"),
+    (1, 2, 1, 1536, 3, True, "contiguous"),
+    (1, 8, 2, 2048, 8, True, "zigzag"),
+    (1, 4, 4, 1024, 4, False, "zigzag"),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,n,causal,layout", TC_BWD_CASES)
+@pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
+def test_tcgen05_bwd_matches_oracle(B, H, Hkv, L, n, causal, layout, grad_dtype):
+    run_bwd(B, H, Hkv, L, 128, n, causal, layout, torch.bfloat16, grad_dtype, seed=L * 3 + n,
+            expect_path="tcgen05")
+
+
 BWD_CASES = [
     # B, H, Hkv, L, d, n, causal, layout, dtype
     (1, 1, 1, 256, 64, 4, False, "contiguous", torch.float32),

@@ -70,3 +70,41 @@ def test_full_size_stepwise_matches_fused():
     ma, rl = errors(to_np(o2), to_np(o1))
     assert ma <= BF16_MAX_ABS and rl <= BF16_REL_L2
     assert (l1 - l2).abs().max().item() < 1e-3
+
+
+def test_full_size_training_backward():
+    """The training workload (L=65536, n=16, zigzag, causal, GQA 4:1): dQ on sampled rows and
+    dK/dV on the last keys of the sequence (whose visible queries are few enough for the oracle),
+    plus identities that hold at any size: sum over keys of dV equals the group's summed dO, and
+    the sum over keys of dK vanishes."""
+    name = "zigzag_gqa_64k_train"
+    w = synth.WORKLOADS[name]
+    B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
+    x = synth.make_workload(name, device=DEV, gen_device=DEV, with_dout=True)
+    assert ra.bwd_path(B, H, Hkv, L, d, n, w["causal"], w["layout"], w["dtype"]) == "tcgen05"
+    out, lse = ra.fwd(x["q"], x["k"], x["v"], n, w["causal"], w["layout"])
+    dq, dk, dv = ra.bwd(x["q"], x["k"], x["v"], out, lse, x["dout"], n, w["causal"], w["layout"])
+    torch.cuda.synchronize()
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all().item()
+    G = H // Hkv
+    dsum = x["dout"].double().view(B, Hkv, G, L, d).sum(dim=(2, 3))
+    assert (dv.double().sum(dim=2) - dsum).abs().max().item() < 0.5
+    assert dk.double().sum(dim=2).abs().max().item() < 0.5
+    host = {t: x[t].cpu() for t in ("q", "k", "v", "dout")}
+    rows = sampled_rows(w, 96, seed=5)
+    ref_dq = oracle.attn_bwd_dq_rows(host["q"], host["k"], host["v"], host["dout"], n,
+                                     w["causal"], w["layout"], rows)
+    got_dq = to_np(dq.view(-1, d)[torch.from_numpy(rows).to(DEV)])
+    ma, rl = errors(got_dq, ref_dq)
+    assert ma <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"dq {ma:.3e} {rl:.3e}"
+    # keys at the last natural positions, in both kv heads at the ends of the head range
+    last = [oracle.natural_position(r, L, n, w["layout"]) for r in range(L)]
+    order = np.argsort(last)[-24:]
+    keys = np.array([((B - 1) * Hkv + g) * L + int(t) for g in (0, Hkv - 1) for t in order])
+    ref_dk, ref_dv = oracle.attn_bwd_dkv_rows(host["q"], host["k"], host["v"], host["dout"], n,
+                                              w["causal"], w["layout"], keys)
+    idx = torch.from_numpy(keys).to(DEV)
+    for got, ref, what in ((dk.view(-1, d)[idx], ref_dk, "dk"), (dv.view(-1, d)[idx], ref_dv, "dv")):
+        ma, rl = errors(to_np(got), ref)
+        assert ma <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"{what} {ma:.3e} {rl:.3e}"
