@@ -140,6 +140,29 @@ RA_API ra_status ring_attn_bwd(const void* q, const void* k, const void* v, cons
 RA_API size_t ring_attn_bwd_workspace_size(int B, int H, int Hkv, int L, int d, int grad_dtype);
 
 /*
+ * ring_attn_bwd_static_scratch -- the backward of ring_attn_bwd for callers that cannot allocate
+ * device memory (a host framework that owns all device memory as one pre-sized pool and passes
+ * only input and output buffers, or a loop that may not call the allocator).  The paper has no
+ * counterpart: this is an interface convenience, not part of the method.
+ * Same arguments and results as ring_attn_bwd without the workspace: the scratch comes from a
+ * file-scope device array of ring_attn_bwd_static_scratch_capacity() bytes (64 MiB) that every
+ * GPU loading this library holds until the process exits.  Allocates nothing.
+ *   - A problem whose ring_attn_bwd_workspace_size exceeds the capacity is rejected with
+ *     RA_ERR_INVALID_ARG before anything is enqueued (fp32 gradients need 4 bytes per query row,
+ *     bf16 gradients 4 * (d + 1)).
+ *   - The first call on a device looks the array's device address up (cudaGetSymbolAddress) with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the array and leaves its contents behind; each call rewrites
+ *     or zeroes what it reads.  Calls whose GPU work overlaps (other streams or threads) race.
+ */
+RA_API ra_status ring_attn_bwd_static_scratch(const void* q, const void* k, const void* v,
+                                              const void* out, const float* lse, const void* dout,
+                                              void* dq, void* dk, void* dv, int grad_dtype, int B,
+                                              int H, int Hkv, int L, int d, int n_shards,
+                                              int causal, int layout, int dtype, void* stream);
+RA_API size_t ring_attn_bwd_static_scratch_capacity(void);
+
+/*
  * ring_attn_shard_tiles -- HOST ONLY, no CUDA call.  For each query shard, the number of
  * (query tile, key tile) pairs of `tile` x `tile` buffer rows (tiles start at each shard's first
  * row) that hold at least one visible (query, key) pair: the per-shard causal work that the

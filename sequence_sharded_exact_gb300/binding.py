@@ -27,7 +27,8 @@ EXPORTS = (
     "ring_attn_fwd", "ring_attn_ring_step_fwd", "ring_attn_lse_merge", "ring_attn_fwd_stepwise",
     "ring_attn_fwd_stepwise_workspace_size", "ring_attn_bwd", "ring_attn_bwd_workspace_size",
     "ring_attn_shard_tiles", "ring_attn_fwd_path", "ring_attn_bwd_path", "ring_attn_device_status",
-    "ring_attn_last_error", "ring_attn_abi_version",
+    "ring_attn_last_error", "ring_attn_abi_version", "ring_attn_bwd_static_scratch",
+    "ring_attn_bwd_static_scratch_capacity",
 )
 
 
@@ -67,6 +68,11 @@ def library():
         lib.ring_attn_last_error.argtypes = []
         lib.ring_attn_last_error.restype = ctypes.c_char_p
         lib.ring_attn_abi_version.argtypes = []
+        lib.ring_attn_bwd_static_scratch.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I,
+                                                     I, I, I, P]
+        lib.ring_attn_bwd_static_scratch.restype = ctypes.c_int
+        lib.ring_attn_bwd_static_scratch_capacity.argtypes = []
+        lib.ring_attn_bwd_static_scratch_capacity.restype = SZ
         for name in EXPORTS:
             f = getattr(lib, name)
             if f.restype is ctypes.c_int or name in ("ring_attn_fwd", "ring_attn_ring_step_fwd",
@@ -224,6 +230,28 @@ def bwd(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigzag",
                                    int(n_shards), int(causal), _layout(layout),
                                    _dtype_code(q.dtype), _stream(stream, q.device)))
     return dq, dk, dv
+
+
+def bwd_static_scratch(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigzag",
+                       grad_dtype=torch.float32, dq=None, dk=None, dv=None, stream=None):
+    """ring_attn_bwd_static_scratch: the backward with the library's static scratch (no workspace
+    argument; the C call allocates nothing).  Returns (dq, dk, dv) in grad_dtype."""
+    B, H, Hkv, L, d = _dims(q, k)
+    if dq is None:
+        dq = torch.empty((B, H, L, d), dtype=grad_dtype, device=q.device)
+    if dk is None:
+        dk = torch.empty((B, Hkv, L, d), dtype=grad_dtype, device=q.device)
+    if dv is None:
+        dv = torch.empty((B, Hkv, L, d), dtype=grad_dtype, device=q.device)
+    _check(library().ring_attn_bwd_static_scratch(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+        _dtype_code(grad_dtype), B, H, Hkv, L, d, int(n_shards), int(causal), _layout(layout),
+        _dtype_code(q.dtype), _stream(stream, q.device)))
+    return dq, dk, dv
+
+
+def bwd_static_scratch_capacity():
+    return int(library().ring_attn_bwd_static_scratch_capacity())
 
 
 def shard_tiles(L, n_shards, causal=True, layout="zigzag", tile=128):

@@ -121,6 +121,12 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
+int set_last_error(int status, const char* msg)
+{
+    g_last_error = msg ? msg : "";
+    return status;
+}
+
 int device_sm_count()
 {
     int dev = current_device();

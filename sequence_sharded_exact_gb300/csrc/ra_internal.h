@@ -56,4 +56,7 @@ cudaError_t launch_zero(float* dst, long long count, cudaStream_t s);
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Records `msg` as the calling thread's last error (ring_attn_last_error) and returns `status`.
+int set_last_error(int status, const char* msg);
+
 }  // namespace ra
