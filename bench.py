@@ -211,7 +211,7 @@ def run_reference(args, w):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / max(1, args.steps) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w),
+        "config": config_dict(w, args.step),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{count} random query rows of the workload per step, "
                                    f"{args.steps} timed steps (float64 two-pass attention rows)"},
@@ -221,8 +221,8 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def config_dict(w):
-    return {"workload": f"ring attention fwd, B{w['B']} H{w['H']} Hkv{w['Hkv']} d{w['d']} "
+def config_dict(w, step="fwd"):
+    return {"workload": f"ring attention {'fwd+bwd' if step == 'train' else 'fwd'}, B{w['B']} H{w['H']} Hkv{w['Hkv']} d{w['d']} "
                         f"L{w['L']} n{w['n']} {'causal' if w['causal'] else 'full'} {w['layout']}",
             "B": w["B"], "H": w["H"], "Hkv": w["Hkv"], "L": w["L"], "d": w["d"], "n_shards": w["n"],
             "causal": w["causal"], "layout": w["layout"], "tile": 128,
@@ -239,13 +239,18 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--oracle-seconds", type=float, default=15.0)
-    ap.add_argument("--workload", default=WORKLOAD,
-                    help="synthetic workload name (default: the long-context forward)")
+    ap.add_argument("--workload", default=None,
+                    help="synthetic workload name (default: the long-context forward for --step "
+                         "fwd, the 64K training workload for --step train)")
+    ap.add_argument("--step", default="fwd", choices=["fwd", "train"],
+                    help="fwd: one ring-attention forward per step; train: forward + backward")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
     from sequence_sharded_exact_gb300 import synth
 
+    if args.workload is None:
+        args.workload = WORKLOAD if args.step == "fwd" else TRAIN_WORKLOAD
     w = dict(synth.WORKLOADS[args.workload])
     if args.impl == "reference":
         run_reference(args, w)
@@ -269,16 +274,35 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
+    train = args.step == "train"
     x = synth.make_inputs(B, H, Hkv, L, d, dtype=w["dtype"], seed=w["seed"] + rank,
-                          spike_frac=w["spike_frac"], device=dev, gen_device=dev)
+                          spike_frac=w["spike_frac"], with_dout=train, device=dev, gen_device=dev)
     q, k, v = x["q"], x["k"], x["v"]
     out = torch.empty_like(q)
     lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
     path = ra.fwd_path(B, H, Hkv, L, d, n, w["causal"], w["layout"], w["dtype"])
-    flops = fwd_flops(B, H, L, d, w["causal"])
+    ff = fwd_flops(B, H, L, d, w["causal"])
+    flops = 3.5 * ff if train else ff
+    dq = dk = dv = wsb = None
+    if train:
+        path += "+" + ra.bwd_path(B, H, Hkv, L, d, n, w["causal"], w["layout"], w["dtype"])
+        dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+        wsb = torch.empty(max(256, ra.bwd_workspace_size(B, H, Hkv, L, d, torch.float32)),
+                          dtype=torch.uint8, device=dev)
+
+    def fwd_call():
+        ra.fwd(q, k, v, n, w["causal"], w["layout"], out=out, lse=lse, stream=stream)
+
+    def bwd_call():
+        ra.bwd(q, k, v, out, lse, x["dout"], n, w["causal"], w["layout"], dq=dq, dk=dk, dv=dv,
+               workspace=wsb, stream=stream)
 
     def step():
-        ra.fwd(q, k, v, n, w["causal"], w["layout"], out=out, lse=lse, stream=stream)
+        fwd_call()
+        if train:
+            bwd_call()
 
     # timed region: barrier + synchronize on both sides, CUDA events on the launch stream
     for _ in range(args.warmup):
@@ -289,71 +313,85 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+        per = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
         ev0.record(stream)
-        for a, b in per:
+        for a, b, c in per:
             a.record(stream)
-            step()
+            fwd_call()
             b.record(stream)
+            if train:
+                bwd_call()
+            c.record(stream)
         ev1.record(stream)
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     total_ms = ev0.elapsed_time(ev1)
-    launch_ms = [a.elapsed_time(b) for a, b in per]
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in per]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in per] if train else []
     status = ra.device_status()
     total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
     value = whole_job_tflops(world, flops, args.steps, total_ms)
 
     peak_b, peak_s, hbm, peak_kind = peaks()
-    kernel_ms = statistics.mean(launch_ms)
-    achieved = flops / (kernel_ms / 1e3) / 1e12
+    if train:
+        kname, kflops, kms = "bwd_tc_kernel", 2.5 * ff, statistics.mean(bwd_ms)
+        note = "ring_attn_bwd call (preprocess + zero + bwd_tc_kernel), CUDA events"
+    else:
+        kname, kflops, kms = "fwd_tc_kernel", ff, statistics.mean(fwd_ms)
+        note = "one fwd_tc_kernel launch, CUDA events"
+    achieved = kflops / (kms / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic: q,k,v ~ N(0,1) bf16, 1% of key rows x8, seeded",
-        "config": config_dict(w),
+        "data": "synthetic: q,k,v ~ N(0,1) bf16" + (", 1% of key rows x8" if w["spike_frac"] else "")
+                + (", dO ~ N(0,1)" if train else "") + ", seeded",
+        "config": config_dict(w, args.step),
         "fraction_of_peak": value / world / peak_b,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_b, "unit": "TFLOP/s",
                      "frac": achieved / peak_b, "traffic": None,
                      "peak_kind": f"{peak_kind} bf16 burst (MEASURED_PEAKS bf16_tflops)",
                      "frac_of_sustained": achieved / peak_s,
-                     "kernel": "fwd_tc_kernel", "algorithmic_flops_per_launch": flops},
-        "gpu_launches": args.steps,
+                     "kernel": kname, "timed": note, "algorithmic_flops_per_launch": kflops},
+        "gpu_launches": args.steps * (4 if train else 1),
         "path": path,
         "device_status": status,
     }
+    if train:
+        line["fwd_ms"] = statistics.mean(fwd_ms)
+        line["bwd_ms"] = statistics.mean(bwd_ms)
 
-    # end to end: pinned host buffers -> device, the C-ABI call, result -> host, every step
+    # end to end: pinned host buffers -> device, the C-ABI calls, results -> host, every step
     if rank == 0 or dist:
-        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        ins = [q, k, v] + ([x["dout"]] if train else [])
+        outs = [dq, dk, dv] if train else [out, lse]
+        h_in = [t.cpu().pin_memory() for t in ins]
+        h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
 
         def e2e_step():
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
+            for dst, src in zip(ins, h_in):
+                dst.copy_(src, non_blocking=True)
             step()
-            hout.copy_(out, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
+            for dst, src in zip(h_out, outs):
+                dst.copy_(src, non_blocking=True)
 
         e2e_steps = max(2, args.steps // 2)
         e2e_ms = sum(time_launches(e2e_step, e2e_steps, 1, stream)) / e2e_steps
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-        d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+        h2d = sum(t.numel() * t.element_size() for t in h_in)
+        d2h = sum(t.numel() * t.element_size() for t in h_out)
         line["e2e"] = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                       "what": ("forward + backward" if train else "forward")
+                               + " through the C ABI with pinned host buffers in and out",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e2e_ms}
-        del hq, hk, hv, hout, hlse
+        del h_in, h_out
 
     line["clocks"] = clk.summary()
 
-    if rank == 0 and not args.no_extra:
+    if rank == 0 and not args.no_extra and not train:
         line["extra"] = secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args)
     if rank == 0:
         arrs, count = oracle_calibrate(x, w, args.oracle_seconds)

@@ -183,6 +183,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
     }
 }
 
+// dst[0..3] += (a, b, c, d) as float32, without a return value.
+__device__ __forceinline__ void red_add_v4(float* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(__uint_as_float(a)),
+                 "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+                 : "memory");
+}
+
 // 128-byte-swizzled address of 16-byte chunk `ch` of row `r` in a region of 128-byte rows.
 __device__ __forceinline__ uint32_t sw128(uint32_t region, int r, int ch)
 {
@@ -212,62 +220,85 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                 const bool diag = a.geo.causal && qnat == u.pk;
                 const long long qbase = ((long long)u.b * a.H + u.g * a.G + hh) * a.geo.L + qrow;
                 if (!mbar_wait(bar(BAR_ST_FULL), gt & 1, ctl)) return;
-                if (!mbar_wait(bar(BAR_DPT_FULL), gt & 1, ctl)) return;
                 tc_fence_after_sync();
                 __syncwarp();
-                uint32_t pk_all[32];
+                // phase A: P^T = 2^(S^T c - lse2) for query columns [64w, 64w+64), kept in registers
+                // for phase B and written to TMEM as bf16 for dV += P^T dO.
+                float p[64];
+                {
+                    uint32_t s0[32], s1[32];
+                    tmem_ld_32x32b_x32(tmem + lane_off + kColST + (uint32_t)w * 64, s0);
+                    tmem_ld_32x32b_x32(tmem + lane_off + kColST + (uint32_t)w * 64 + 32, s1);
+                    const float4* l4 = reinterpret_cast<const float4*>(a.lse + qbase + w * 64);
+                    float4 lv[16];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int q0 = w * 64 + c * 32;  // first query column of this chunk
-                    uint32_t s[32], dp[32];
-                    tmem_ld_32x32b_x32(tmem + lane_off + kColST + q0, s);
-                    tmem_ld_32x32b_x32(tmem + lane_off + kColDPT + q0, dp);
-                    tmem_ld_wait(s);
-                    tmem_ld_wait(dp);
-                    const float4* l4 = reinterpret_cast<const float4*>(a.lse + qbase + q0);
-                    const float4* d4 = reinterpret_cast<const float4*>(a.Dv + qbase + q0);
-                    uint32_t dsp[16];
+                    for (int e4 = 0; e4 < 16; ++e4) lv[e4] = __ldg(l4 + e4);
+                    tmem_ld_wait(s0);
+                    tmem_ld_wait(s1);
+                    uint32_t pk[32];
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 lv = __ldg(l4 + e4);
-                        const float4 dv = __ldg(d4 + e4);
-                        const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
-                        const float dq[4] = {dv.x, dv.y, dv.z, dv.w};
-                        float p[4], ds[4];
+                    for (int e4 = 0; e4 < 16; ++e4) {
+                        const float lq[4] = {lv[e4].x, lv[e4].y, lv[e4].z, lv[e4].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int col = e4 * 4 + e;
-                            float pv = ex2_approx(fmaf(__uint_as_float(s[col]), a.scale_log2, -lq[e] * kLog2e));
-                            if (diag && (q0 + col) < r) pv = 0.f;
-                            p[e] = pv;
-                            ds[e] = pv * (__uint_as_float(dp[col]) - dq[e]) * a.scale;
+                            const uint32_t sv = col < 32 ? s0[col] : s1[col - 32];
+                            float pv = ex2_approx(fmaf(__uint_as_float(sv), a.scale_log2, -lq[e] * kLog2e));
+                            if (diag && (w * 64 + col) < r) pv = 0.f;
+                            p[col] = pv;
                         }
-                        pk_all[c * 16 + e4 * 2] = pack_bf16x2(p[0], p[1]);
-                        pk_all[c * 16 + e4 * 2 + 1] = pack_bf16x2(p[2], p[3]);
-                        dsp[e4 * 2] = pack_bf16x2(ds[0], ds[1]);
-                        dsp[e4 * 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+                        pk[e4 * 2] = pack_bf16x2(p[e4 * 4], p[e4 * 4 + 1]);
+                        pk[e4 * 2 + 1] = pack_bf16x2(p[e4 * 4 + 2], p[e4 * 4 + 3]);
                     }
-                    // dS^T row r, query columns q0 .. q0+31: 4 chunks of 16 bytes in half w
+                    // P^T of query columns [64w, 64w+64) -> TMEM columns [64w, 64w+32)
+                    tmem_st_32x32b_x32(tmem + lane_off + kColST + (uint32_t)w * 64, pk);
+                    tmem_st_wait();
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_P_READY));
+                // phase B: dS^T = P^T (dP^T - D) / sqrt(d) -> 128-byte-swizzled shared memory
+                if (!mbar_wait(bar(BAR_DPT_FULL), gt & 1, ctl)) return;
+                tc_fence_after_sync();
+                __syncwarp();
+                {
                     const uint32_t region = sbase + kSmemDS + (uint32_t)w * kHalfBytes;
+                    const float4* d4 = reinterpret_cast<const float4*>(a.Dv + qbase + w * 64);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int ch = (c * 32 + j * 8) >> 3;  // chunk within the 128-byte row
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128(region, r, ch)),
-                                     "r"(dsp[4 * j]), "r"(dsp[4 * j + 1]), "r"(dsp[4 * j + 2]), "r"(dsp[4 * j + 3])
-                                     : "memory");
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t dp[32];
+                        tmem_ld_32x32b_x32(tmem + lane_off + kColDPT + (uint32_t)(w * 64 + c * 32), dp);
+                        float4 dv4[8];
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) dv4[e4] = __ldg(d4 + c * 8 + e4);
+                        tmem_ld_wait(dp);
+                        uint32_t dsp[16];
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float dq[4] = {dv4[e4].x, dv4[e4].y, dv4[e4].z, dv4[e4].w};
+                            float ds[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int col = e4 * 4 + e;
+                                ds[e] = p[c * 32 + col] * (__uint_as_float(dp[col]) - dq[e]) * a.scale;
+                            }
+                            dsp[e4 * 2] = pack_bf16x2(ds[0], ds[1]);
+                            dsp[e4 * 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int ch = (c * 32 + j * 8) >> 3;  // 16-byte chunk within the 128-byte row
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128(region, r, ch)),
+                                         "r"(dsp[4 * j]), "r"(dsp[4 * j + 1]), "r"(dsp[4 * j + 2]), "r"(dsp[4 * j + 3])
+                                         : "memory");
+                        }
                     }
                 }
-                // P^T of query columns [64w, 64w+64) -> TMEM columns [64w, 64w+32)
-                tmem_st_32x32b_x32(tmem + lane_off + kColST + (uint32_t)w * 64, pk_all);
-                tmem_st_wait();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar(BAR_P_READY));
-                    mbar_arrive(bar(BAR_DS_READY));
-                }
-                // dQ_t (thread = query row) into the float32 accumulator
+                if (lane == 0) mbar_arrive(bar(BAR_DS_READY));
+                // dQ_t (thread = query row) added into the float32 accumulator
                 if (!mbar_wait(bar(BAR_DQ_FULL), gt & 1, ctl)) return;
                 tc_fence_after_sync();
                 __syncwarp();
@@ -279,9 +310,7 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                     tmem_ld_wait(x);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + e * 4),
-                                  make_float4(__uint_as_float(x[4 * e]), __uint_as_float(x[4 * e + 1]),
-                                              __uint_as_float(x[4 * e + 2]), __uint_as_float(x[4 * e + 3])));
+                        red_add_v4(dst + c * 32 + e * 4, x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
                 }
                 tc_fence_before_sync();
                 __syncwarp();
@@ -384,6 +413,18 @@ __device__ __forceinline__ void producer_role(const BwdArgs& a, uint32_t sbase, 
 // ------------------------------------------------------------------------------------------------
 // MMA issuer (one thread)
 // ------------------------------------------------------------------------------------------------
+// S^T = K Q^T into TMEM columns [0, 128) (both operands K-major).
+__device__ __forceinline__ void issue_st(uint32_t sbase, uint32_t tmem, uint32_t sq)
+{
+    constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (uint32_t)(kk >> 2) * kHalfBytes + (uint32_t)(kk & 3) * 32u;
+        mma_ss(tmem + kColST, sdesc_sw128(sbase + kSmemK + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), id_kk,
+               kk > 0);
+    }
+}
+
 __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint32_t tmem, const WaitCtl& ctl)
 {
     auto bar = [&](int i) { return sbase + kSmemBar + 8u * (uint32_t)i; };
@@ -403,16 +444,13 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
                 const uint32_t use = gt >> 1;
                 const uint32_t sq = sbase + kSmemQ + (uint32_t)stage * kStageBytes;
                 const uint32_t sd = sbase + kSmemDO + (uint32_t)stage * kStageBytes;
-                if (!mbar_wait(bar(BAR_QD_FULL + stage), use & 1, ctl)) goto drain;
-                tc_fence_after_sync();
-                // S^T = K Q^T
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kHalfBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tmem + kColST, sdesc_sw128(sbase + kSmemK + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024),
-                           id_kk, kk > 0);
+                if (t == 0) {
+                    // the first S^T of a unit; later ones are issued one step ahead (below)
+                    if (!mbar_wait(bar(BAR_QD_FULL + stage), use & 1, ctl)) goto drain;
+                    tc_fence_after_sync();
+                    issue_st(sbase, tmem, sq);
+                    tc_commit(bar(BAR_ST_FULL));
                 }
-                tc_commit(bar(BAR_ST_FULL));
                 // dP^T = V dO^T (its columns also hold the previous dQ: wait until that was read)
                 if (gt > 0 && !mbar_wait(bar(BAR_DQ_FREE), (gt - 1) & 1, ctl)) goto drain;
                 tc_fence_after_sync();
@@ -432,6 +470,14 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
                     const uint32_t acol = kColST + (kk < 4 ? (uint32_t)kk * 8u : 64u + (uint32_t)(kk - 4) * 8u);
                     mma_ts(tmem + kColDV, tmem + acol, sdesc_sw128(sd + (uint32_t)kk * 2048u, kHalfBytes, 1024), id_kn,
                            (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                // next S^T, into the columns P^T leaves once the dV product above has read it
+                if (t + 1 < u.ntiles) {
+                    const int nstage = (int)((gt + 1) & 1);
+                    if (!mbar_wait(bar(BAR_QD_FULL + nstage), ((gt + 1) >> 1) & 1, ctl)) goto drain;
+                    tc_fence_after_sync();
+                    issue_st(sbase, tmem, sbase + kSmemQ + (uint32_t)nstage * kStageBytes);
+                    tc_commit(bar(BAR_ST_FULL));
                 }
                 // dK += dS^T Q ; dQ_t = dS K
                 if (!mbar_wait(bar(BAR_DS_READY), gt & 1, ctl)) goto drain;
@@ -493,7 +539,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         math_role(a, sbase, tmem, ctl);
     } else if (warp == 8) {
         if ((threadIdx.x & 31) == 0) producer_role(a, sbase, &tmQ, &tmK, &tmV, &tmDO, ctl);
-    } else {
+    } else if (warp == 9) {
         if ((threadIdx.x & 31) == 0) mma_role(a, sbase, tmem, ctl);
     }
     tc_fence_before_sync();

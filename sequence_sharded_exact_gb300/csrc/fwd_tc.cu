@@ -15,7 +15,8 @@
 //     tiles that share every K/V tile); units come in mirrored pairs (natural block u and U-1-u)
 //     so that every CTA gets the same causal work; pairs are ordered kv head by kv head so that
 //     concurrently running CTAs read the same K/V from L2.
-//   * warp 8 (one thread) issues TMA loads: Q tiles, and K/V tiles through a 2-stage ring.
+//   * warp 8 (one thread) issues TMA loads: Q tiles, and K/V tiles through a 2-stage ring;
+//     warps 10-11 only complete the third warpgroup, whose registers go to the softmax warps.
 //   * warp 9 (one thread) issues tcgen05.mma: S_w = Q_w K^T into TMEM (w = 0, 1), then
 //     O_w += P_w V with P_w read from TMEM; the S MMA of the next tile is issued between the two
 //     P V products so that the tensor core works while the softmax warps do.
@@ -44,7 +45,7 @@ constexpr int kTile = 128;                        // rows of a Q tile (MMA M) an
 constexpr int kHd = 128;                          // head dim
 constexpr int kBlock = 2 * kTile;                 // query rows per work unit
 constexpr int kStages = 2;                        // K/V pipeline depth
-constexpr int kThreads = 320;                     // 10 warps
+constexpr int kThreads = 384;                     // 12 warps (warps 10-11 idle)
 constexpr uint32_t kHalfBytes = kTile * 64 * 2;   // 128 rows x 64 bf16 (one 128-byte-swizzle box)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;   // 128 x 128 bf16
 
@@ -217,33 +218,50 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                 tc_fence_after_sync();
                 __syncwarp();
                 uint32_t r[4][32];
+                // First half of the row, then the second half's loads overlap the first half's max.
+                tmem_ld_32x32b_x32(tS + 0, r[0]);
+                tmem_ld_32x32b_x32(tS + 32, r[1]);
+                tmem_ld_wait(r[0]);
+                tmem_ld_wait(r[1]);
+                tmem_ld_32x32b_x32(tS + 64, r[2]);
+                tmem_ld_32x32b_x32(tS + 96, r[3]);
+                float m8[8];
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tmem_ld_32x32b_x32(tS + c4 * 32, r[c4]);
+                for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+                if (mask != 0) {
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tmem_ld_wait(r[c4]);
-                float mx = -INFINITY;
-                if (mask == 0) {
+                    for (int c4 = 0; c4 < 2; ++c4)
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[c4][e]));
-                } else {
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const bool hide = mask == 2 || (c4 * 32 + e) > rw;
-                            const float x = hide ? -INFINITY : __uint_as_float(r[c4][e]);
-                            r[c4][e] = __float_as_uint(x);
-                            mx = fmaxf(mx, x);
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            if (mask == 2 || (c4 * 32 + e) > rw) r[c4][e] = __float_as_uint(-INFINITY);
                 }
+#pragma unroll
+                for (int c4 = 0; c4 < 2; ++c4)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(r[c4][e]));
+                tmem_ld_wait(r[2]);
+                tmem_ld_wait(r[3]);
+                if (mask != 0) {
+#pragma unroll
+                    for (int c4 = 2; c4 < 4; ++c4)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (mask == 2 || (c4 * 32 + e) > rw) r[c4][e] = __float_as_uint(-INFINITY);
+                }
+#pragma unroll
+                for (int c4 = 2; c4 < 4; ++c4)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(r[c4][e]));
+                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 const float m_tile = mx * sl2;
                 float m_new = m_run;
                 if (m_tile > m_run + 8.0f) m_new = m_tile;
                 const float alpha = (m_new == m_run) ? 1.0f : ex2_approx(m_run - m_new);
                 const float ref = m_new == -INFINITY ? 0.f : m_new;
-                float rsum = 0.f;
+                float s8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) s8[i] = 0.f;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[32];
@@ -254,12 +272,13 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                         for (int e = 0; e < 32; e += 2) {
                             const float p0 = ex2_approx(fmaf(__uint_as_float(r[c4][e]), sl2, -ref));
                             const float p1 = ex2_approx(fmaf(__uint_as_float(r[c4][e + 1]), sl2, -ref));
-                            rsum += p0 + p1;
+                            s8[(e >> 1) & 7] += p0 + p1;
                             pk[cc * 16 + e / 2] = pack_bf16x2(p0, p1);
                         }
                     }
                     tmem_st_32x32b_x32(tS + half * 32, pk);
                 }
+                const float rsum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
                 l_run = l_run * alpha + rsum;
                 tmem_st_wait();
                 const bool need = jj > 0 && alpha != 1.0f;
@@ -527,11 +546,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t tmem = *tmem_slot;
     const WaitCtl ctl{abort_flag, a.status, kWaitLimitNs};
 
+    // Register split: launched with 384 x 168 = 64512 registers; softmax warpgroups 2 x 128 x 192
+    // plus the TMA/MMA warpgroup 128 x 120 = 64512 (per SM sub-partition 192 + 192 + 120 = 504).
+    if (warp < 8)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+    else
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
+
     if (warp < 8) {
         softmax_role(a, sbase, tmem, ctl);
     } else if (warp == 8) {
         if ((threadIdx.x & 31) == 0) producer_role(a, sbase, &tmQ, &tmK, &tmV, ctl);
-    } else {
+    } else if (warp == 9) {
         if ((threadIdx.x & 31) == 0) mma_role(a, sbase, tmem, ctl);
     }
 

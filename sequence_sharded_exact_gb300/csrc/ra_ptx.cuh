@@ -90,7 +90,7 @@ struct WaitCtl {
     uint64_t limit_ns;
 };
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl)
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl)
 {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
