@@ -20,8 +20,8 @@
 //       and as an M-major operand for dQ).
 //   * warps 0-7 (two warpgroups, each owning half of the 128 columns): read S^T and dP^T
 //     (thread = key row), form P^T and dS^T, write P^T to TMEM and dS^T to shared memory; then read
-//     dQ_t from TMEM (thread = query row) and add it into the float32 dQ accumulator in HBM; at the
-//     end of a unit write dK and dV.
+//     dQ_t from TMEM (thread = query row), stage it in shared memory and add it into the float32 dQ
+//     accumulator in HBM with TMA bulk reductions; at the end of a unit write dK and dV.
 //   * TMEM columns: S^T/P^T [0,128), dP^T/dQ [128,256), dK [256,384), dV [384,512).
 //   * every wait is bounded; a wait that runs out sets the device status word and the CTA stops.
 #include <cuda.h>
@@ -183,12 +183,26 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
     }
 }
 
-// dst[0..3] += (a, b, c, d) as float32, without a return value.
-__device__ __forceinline__ void red_add_v4(float* dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+// TMA: global tile at {x, y, z} += the box in shared memory at `src` (float32 add, bulk group).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(__uint_as_float(a)),
-                 "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
-                 : "memory");
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];\n\t"
+        "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// Waits until the shared memory of every bulk copy this thread committed has been read.
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until every bulk copy this thread committed has completed.
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // 128-byte-swizzled address of 16-byte chunk `ch` of row `r` in a region of 128-byte rows.
@@ -200,7 +214,8 @@ __device__ __forceinline__ uint32_t sw128(uint32_t region, int r, int ch)
 // ------------------------------------------------------------------------------------------------
 // elementwise + dQ + epilogue warpgroups
 // ------------------------------------------------------------------------------------------------
-__device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint32_t tmem, const WaitCtl& ctl)
+__device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint32_t tmem, const CUtensorMap* tmDQ,
+                                          const WaitCtl& ctl)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int w = warp >> 2;                    // column half owned by this warpgroup
@@ -219,7 +234,7 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                 walk.next(hh, qrow, qnat);
                 const bool diag = a.geo.causal && qnat == u.pk;
                 const long long qbase = ((long long)u.b * a.H + u.g * a.G + hh) * a.geo.L + qrow;
-                if (!mbar_wait(bar(BAR_ST_FULL), gt & 1, ctl)) return;
+                if (!mbar_wait(bar(BAR_ST_FULL), gt & 1, ctl)) goto done;
                 tc_fence_after_sync();
                 __syncwarp();
                 // phase A: P^T = 2^(S^T c - lse2) for query columns [64w, 64w+64), kept in registers
@@ -258,7 +273,7 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(BAR_P_READY));
                 // phase B: dS^T = P^T (dP^T - D) / sqrt(d) -> 128-byte-swizzled shared memory
-                if (!mbar_wait(bar(BAR_DPT_FULL), gt & 1, ctl)) return;
+                if (!mbar_wait(bar(BAR_DPT_FULL), gt & 1, ctl)) goto done;
                 tc_fence_after_sync();
                 __syncwarp();
                 {
@@ -299,25 +314,43 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(BAR_DS_READY));
                 // dQ_t (thread = query row) added into the float32 accumulator
-                if (!mbar_wait(bar(BAR_DQ_FULL), gt & 1, ctl)) return;
+                if (!mbar_wait(bar(BAR_DQ_FULL), gt & 1, ctl)) goto done;
                 tc_fence_after_sync();
                 __syncwarp();
-                float* dst = a.dq_acc + (qbase + r) * kHd + w * 64;
+                // Stage 32 columns at a time in this warp's 4 KB slice of the dS^T buffer (the slice
+                // it writes itself; dS^T has been consumed once dQ is complete) and let TMA add it
+                // into the float32 accumulator as full 128-byte lines.
+                {
+                    const uint32_t stage_base = sbase + kSmemDS + (uint32_t)warp * 4096u;
+                    const int zq = u.b * a.H + u.g * a.G + hh;
+                    const int y = qrow + (warp & 3) * 32;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t x[32];
-                    tmem_ld_32x32b_x32(tmem + lane_off + kColDPT + (uint32_t)(w * 64 + c * 32), x);
-                    tmem_ld_wait(x);
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t x[32];
+                        tmem_ld_32x32b_x32(tmem + lane_off + kColDPT + (uint32_t)(w * 64 + c * 32), x);
+                        tmem_ld_wait(x);
+                        if (c == 1) {  // the first chunk's copy must have left shared memory
+                            if (lane == 0) bulk_wait_read_all();
+                            __syncwarp();
+                        }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        red_add_v4(dst + c * 32 + e * 4, x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+                        for (int j = 0; j < 8; ++j)
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128(stage_base, lane, j)),
+                                         "r"(x[4 * j]), "r"(x[4 * j + 1]), "r"(x[4 * j + 2]), "r"(x[4 * j + 3])
+                                         : "memory");
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0) tma_reduce_add_3d(tmDQ, stage_base, w * 64 + c * 32, y, zq);
+                    }
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
                 }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(BAR_DQ_FREE));
             }
             // epilogue: dK, dV of key row r, columns [64w, 64w+64)
-            if (!mbar_wait(bar(BAR_ACC_FULL), uc & 1, ctl)) return;
+            if (!mbar_wait(bar(BAR_ACC_FULL), uc & 1, ctl)) goto done;
             tc_fence_after_sync();
             __syncwarp();
             const long long krow = ((long long)u.b * a.Hkv + u.g) * a.geo.L + u.rk + r;
@@ -354,6 +387,10 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
             ++uc;
         }
     }
+done:
+    // every bulk reduction this warp issued has been applied before the CTA exits
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -510,7 +547,8 @@ drain:
 
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const BwdArgs a)
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+              const __grid_constant__ CUtensorMap tmDQ, const BwdArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -536,7 +574,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t tmem = *tmem_slot;
     const WaitCtl ctl{abort_flag, a.status, kWaitLimitNs};
     if (warp < 8) {
-        math_role(a, sbase, tmem, ctl);
+        math_role(a, sbase, tmem, &tmDQ, ctl);
     } else if (warp == 8) {
         if ((threadIdx.x & 31) == 0) producer_role(a, sbase, &tmQ, &tmK, &tmV, &tmDO, ctl);
     } else if (warp == 9) {
@@ -579,6 +617,21 @@ bool make_map(CUtensorMap* map, const void* base, int L, long long heads)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over the float32 dQ accumulator [heads][L][128]: box 32 columns x 32 rows x 1 head,
+// 128-byte swizzle (the layout the math warps stage it in).
+bool make_dq_map(CUtensorMap* map, float* base, int L, long long heads)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kHd, (cuuint64_t)L, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)kHd * 4, (cuuint64_t)L * kHd * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool tc_bwd_supported(const Problem& p)
@@ -591,9 +644,10 @@ cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const 
                           const float* D, const float* lse, float* dq_acc, void* dk, void* dv, int grad_dtype,
                           unsigned int* status, cudaStream_t s)
 {
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_map(&tq, q, p.L, (long long)p.B * p.H) || !make_map(&tk, k, p.L, (long long)p.B * p.Hkv) ||
-        !make_map(&tv, v, p.L, (long long)p.B * p.Hkv) || !make_map(&tdo, dout, p.L, (long long)p.B * p.H))
+        !make_map(&tv, v, p.L, (long long)p.B * p.Hkv) || !make_map(&tdo, dout, p.L, (long long)p.B * p.H) ||
+        !make_dq_map(&tdq, dq_acc, p.L, (long long)p.B * p.H))
         return cudaErrorInvalidValue;
     BwdArgs a;
     a.geo = p.geo();
@@ -625,7 +679,7 @@ cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const 
     }
     const long long sms = device_sm_count();
     const unsigned grid = (unsigned)(a.items < sms ? a.items : sms);
-    bwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, a);
+    bwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, a);
     return cudaGetLastError();
 }
 
