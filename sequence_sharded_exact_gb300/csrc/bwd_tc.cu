@@ -20,8 +20,10 @@
 //       and as an M-major operand for dQ).
 //   * warps 0-7 (two warpgroups, each owning half of the 128 columns): read S^T and dP^T
 //     (thread = key row), form P^T and dS^T, write P^T to TMEM and dS^T to shared memory; then read
-//     dQ_t from TMEM (thread = query row), stage it in shared memory and add it into the float32 dQ
-//     accumulator in HBM with TMA bulk reductions; at the end of a unit write dK and dV.
+//     dQ_t from TMEM (thread = query row) and stage it in shared memory; at the end of a unit write
+//     dK and dV.
+//   * warp 10: adds each staged dQ tile into the float32 accumulator in HBM with TMA bulk
+//     reductions and hands the staging buffer back to the producer.
 //   * TMEM columns: S^T/P^T [0,128), dP^T/dQ [128,256), dK [256,384), dV [384,512).
 //   * every wait is bounded; a wait that runs out sets the device status word and the CTA stops.
 #include <cuda.h>
@@ -37,7 +39,7 @@ namespace {
 
 constexpr int kTile = 128;
 constexpr int kHd = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // 12 warps: 0-7 math, 8 TMA loads, 9 MMA, 10 dQ reductions, 11 idle
 constexpr uint32_t kHalfBytes = kTile * 64 * 2;  // 16 KB
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 32 KB
 
@@ -62,7 +64,8 @@ enum : int {
     BAR_DQ_FREE,
     BAR_ACC_FULL,
     BAR_ACC_FREE,
-    BAR_DRAIN,
+    BAR_DQ_STAGED,            // 2 stages
+    BAR_DRAIN = BAR_DQ_STAGED + 2,
     BAR_COUNT
 };
 
@@ -187,11 +190,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z)
 {
     asm volatile(
-        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];\n\t"
-        "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(map)),
         "r"(src), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until the shared memory of every bulk copy this thread committed has been read.
 __device__ __forceinline__ void bulk_wait_read_all()
@@ -214,8 +219,7 @@ __device__ __forceinline__ uint32_t sw128(uint32_t region, int r, int ch)
 // ------------------------------------------------------------------------------------------------
 // elementwise + dQ + epilogue warpgroups
 // ------------------------------------------------------------------------------------------------
-__device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint32_t tmem, const CUtensorMap* tmDQ,
-                                          const WaitCtl& ctl)
+__device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint32_t tmem, const WaitCtl& ctl)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int w = warp >> 2;                    // column half owned by this warpgroup
@@ -229,11 +233,17 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
             if (!unit_of(a, item, member, u) || u.ntiles == 0) continue;
             QWalk walk;
             walk.begin(a, u);
+            float4 lv[16];  // lse of this step's query columns, loaded one step ahead
             for (int t = 0; t < u.ntiles; ++t, ++gt) {
                 int hh, qrow, qnat;
                 walk.next(hh, qrow, qnat);
                 const bool diag = a.geo.causal && qnat == u.pk;
                 const long long qbase = ((long long)u.b * a.H + u.g * a.G + hh) * a.geo.L + qrow;
+                if (t == 0) {
+                    const float4* l4 = reinterpret_cast<const float4*>(a.lse + qbase + w * 64);
+#pragma unroll
+                    for (int e4 = 0; e4 < 16; ++e4) lv[e4] = __ldg(l4 + e4);
+                }
                 if (!mbar_wait(bar(BAR_ST_FULL), gt & 1, ctl)) goto done;
                 tc_fence_after_sync();
                 __syncwarp();
@@ -244,10 +254,6 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                     uint32_t s0[32], s1[32];
                     tmem_ld_32x32b_x32(tmem + lane_off + kColST + (uint32_t)w * 64, s0);
                     tmem_ld_32x32b_x32(tmem + lane_off + kColST + (uint32_t)w * 64 + 32, s1);
-                    const float4* l4 = reinterpret_cast<const float4*>(a.lse + qbase + w * 64);
-                    float4 lv[16];
-#pragma unroll
-                    for (int e4 = 0; e4 < 16; ++e4) lv[e4] = __ldg(l4 + e4);
                     tmem_ld_wait(s0);
                     tmem_ld_wait(s1);
                     uint32_t pk[32];
@@ -269,6 +275,13 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                     tmem_st_32x32b_x32(tmem + lane_off + kColST + (uint32_t)w * 64, pk);
                     tmem_st_wait();
                 }
+                // D of these columns for phase B, in flight while dP^T is computed
+                float4 dv4[16];
+                {
+                    const float4* d4 = reinterpret_cast<const float4*>(a.Dv + qbase + w * 64);
+#pragma unroll
+                    for (int e4 = 0; e4 < 16; ++e4) dv4[e4] = __ldg(d4 + e4);
+                }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(BAR_P_READY));
@@ -278,19 +291,16 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                 __syncwarp();
                 {
                     const uint32_t region = sbase + kSmemDS + (uint32_t)w * kHalfBytes;
-                    const float4* d4 = reinterpret_cast<const float4*>(a.Dv + qbase + w * 64);
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         uint32_t dp[32];
                         tmem_ld_32x32b_x32(tmem + lane_off + kColDPT + (uint32_t)(w * 64 + c * 32), dp);
-                        float4 dv4[8];
-#pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) dv4[e4] = __ldg(d4 + c * 8 + e4);
                         tmem_ld_wait(dp);
                         uint32_t dsp[16];
 #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {
-                            const float dq[4] = {dv4[e4].x, dv4[e4].y, dv4[e4].z, dv4[e4].w};
+                            const float dq[4] = {dv4[c * 8 + e4].x, dv4[c * 8 + e4].y, dv4[c * 8 + e4].z,
+                                                 dv4[c * 8 + e4].w};
                             float ds[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
@@ -313,41 +323,48 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(BAR_DS_READY));
+                {  // next step's lse, in flight during the dQ readout (the last step reloads its own)
+                    long long qbase2 = qbase;
+                    if (t + 1 < u.ntiles) {
+                        QWalk peek = walk;
+                        int hh2, qrow2, qnat2;
+                        peek.next(hh2, qrow2, qnat2);
+                        qbase2 = ((long long)u.b * a.H + u.g * a.G + hh2) * a.geo.L + qrow2;
+                    }
+                    const float4* l4 = reinterpret_cast<const float4*>(a.lse + qbase2 + w * 64);
+#pragma unroll
+                    for (int e4 = 0; e4 < 16; ++e4) lv[e4] = __ldg(l4 + e4);
+                }
                 // dQ_t (thread = query row) added into the float32 accumulator
                 if (!mbar_wait(bar(BAR_DQ_FULL), gt & 1, ctl)) goto done;
                 tc_fence_after_sync();
                 __syncwarp();
-                // Stage 32 columns at a time in this warp's 4 KB slice of the dS^T buffer (the slice
-                // it writes itself; dS^T has been consumed once dQ is complete) and let TMA add it
-                // into the float32 accumulator as full 128-byte lines.
+                // Read dQ out of TMEM and release its columns at once; stage it in this warp's 8 KB
+                // slice of the step's (Q, dO) buffer, which no MMA reads any more.  The reducer warp
+                // adds it into the float32 accumulator with TMA and hands the buffer back.
                 {
-                    const uint32_t stage_base = sbase + kSmemDS + (uint32_t)warp * 4096u;
-                    const int zq = u.b * a.H + u.g * a.G + hh;
-                    const int y = qrow + (warp & 3) * 32;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t x[32];
-                        tmem_ld_32x32b_x32(tmem + lane_off + kColDPT + (uint32_t)(w * 64 + c * 32), x);
-                        tmem_ld_wait(x);
-                        if (c == 1) {  // the first chunk's copy must have left shared memory
-                            if (lane == 0) bulk_wait_read_all();
-                            __syncwarp();
-                        }
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128(stage_base, lane, j)),
-                                         "r"(x[4 * j]), "r"(x[4 * j + 1]), "r"(x[4 * j + 2]), "r"(x[4 * j + 3])
-                                         : "memory");
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        __syncwarp();
-                        if (lane == 0) tma_reduce_add_3d(tmDQ, stage_base, w * 64 + c * 32, y, zq);
-                    }
-                    if (lane == 0) bulk_wait_read_all();
+                    uint32_t x0[32], x1[32];
+                    tmem_ld_32x32b_x32(tmem + lane_off + kColDPT + (uint32_t)(w * 64), x0);
+                    tmem_ld_32x32b_x32(tmem + lane_off + kColDPT + (uint32_t)(w * 64 + 32), x1);
+                    tmem_ld_wait(x0);
+                    tmem_ld_wait(x1);
+                    tc_fence_before_sync();
                     __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(BAR_DQ_FREE));
+                    const uint32_t slice = sbase + kSmemQ + (uint32_t)(gt & 1) * kStageBytes + (uint32_t)warp * 8192u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128(slice, lane, j)),
+                                     "r"(x0[4 * j]), "r"(x0[4 * j + 1]), "r"(x0[4 * j + 2]), "r"(x0[4 * j + 3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128(slice + 4096u, lane, j)),
+                                     "r"(x1[4 * j]), "r"(x1[4 * j + 1]), "r"(x1[4 * j + 2]), "r"(x1[4 * j + 3])
+                                     : "memory");
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(BAR_DQ_STAGED + (int)(gt & 1)));
                 }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BAR_DQ_FREE));
             }
             // epilogue: dK, dV of key row r, columns [64w, 64w+64)
             if (!mbar_wait(bar(BAR_ACC_FULL), uc & 1, ctl)) goto done;
@@ -388,9 +405,47 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
         }
     }
 done:
-    // every bulk reduction this warp issued has been applied before the CTA exits
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
+    return;
+}
+
+// ------------------------------------------------------------------------------------------------
+// dQ reducer (one thread): adds each step's staged dQ tile into the float32 accumulator with TMA
+// bulk reductions, then returns the step's (Q, dO) buffer to the producer.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void reducer_role(const BwdArgs& a, uint32_t sbase, const CUtensorMap* tmDQ,
+                                             const WaitCtl& ctl)
+{
+    auto bar = [&](int i) { return sbase + kSmemBar + 8u * (uint32_t)i; };
+    tma_prefetch_desc(tmDQ);
+    uint32_t gt = 0;
+    for (long long item = blockIdx.x; item < a.items; item += gridDim.x) {
+        for (int member = 0; member < 2; ++member) {
+            KvUnit u;
+            if (!unit_of(a, item, member, u) || u.ntiles == 0) continue;
+            QWalk walk;
+            walk.begin(a, u);
+            for (int t = 0; t < u.ntiles; ++t, ++gt) {
+                int hh, qrow, qnat;
+                walk.next(hh, qrow, qnat);
+                const int stage = (int)(gt & 1);
+                if (!mbar_wait(bar(BAR_DQ_STAGED + stage), (gt >> 1) & 1, ctl)) goto done;
+                const int zq = u.b * a.H + u.g * a.G + hh;
+                const uint32_t buf = sbase + kSmemQ + (uint32_t)stage * kStageBytes;
+#pragma unroll 1
+                for (int wi = 0; wi < 8; ++wi) {
+                    const uint32_t slice = buf + (uint32_t)wi * 8192u;
+                    const int y = qrow + (wi & 3) * 32;
+                    tma_reduce_add_3d(tmDQ, slice, (wi >> 2) * 64, y, zq);
+                    tma_reduce_add_3d(tmDQ, slice + 4096u, (wi >> 2) * 64 + 32, y, zq);
+                }
+                bulk_commit();
+                bulk_wait_read_all();
+                mbar_arrive(bar(BAR_QD_EMPTY + stage));
+            }
+        }
+    }
+done:
+    bulk_wait_all();  // every reduction has been applied before the CTA exits
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -531,7 +586,6 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
                            sdesc_sw128(sbase + kSmemK + (uint32_t)kk * 2048u, kHalfBytes, 1024), id_mn, kk > 0);
                 }
                 tc_commit(bar(BAR_DQ_FULL));
-                tc_commit(bar(BAR_QD_EMPTY + stage));
             }
             tc_commit(bar(BAR_KV_EMPTY));
             tc_commit(bar(BAR_ACC_FULL));
@@ -558,7 +612,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemTmemSlot);
     if (threadIdx.x == 0) {
         for (int i = 0; i < BAR_COUNT; ++i) {
-            const bool by_warps = i == BAR_P_READY || i == BAR_DS_READY || i == BAR_DQ_FREE || i == BAR_ACC_FREE;
+            const bool by_warps = i == BAR_P_READY || i == BAR_DS_READY || i == BAR_DQ_FREE || i == BAR_ACC_FREE ||
+                                  i == BAR_DQ_STAGED || i == BAR_DQ_STAGED + 1;
             mbar_init(sbase + kSmemBar + 8u * (uint32_t)i, by_warps ? 8u : 1u);
         }
         *abort_flag = 0;
@@ -573,12 +628,20 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl ctl{abort_flag, a.status, kWaitLimitNs};
+    // Register split: launched with 384 x 168 = 64512 registers; math warpgroups 2 x 128 x 192 plus
+    // the TMA/MMA warpgroup 128 x 120 = 64512 (per SM sub-partition 192 + 192 + 120 = 504).
+    if (warp < 8)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+    else
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 120;" ::: "memory");
     if (warp < 8) {
-        math_role(a, sbase, tmem, &tmDQ, ctl);
+        math_role(a, sbase, tmem, ctl);
     } else if (warp == 8) {
         if ((threadIdx.x & 31) == 0) producer_role(a, sbase, &tmQ, &tmK, &tmV, &tmDO, ctl);
     } else if (warp == 9) {
         if ((threadIdx.x & 31) == 0) mma_role(a, sbase, tmem, ctl);
+    } else if (warp == 10) {
+        if ((threadIdx.x & 31) == 0) reducer_role(a, sbase, &tmDQ, ctl);
     }
     tc_fence_before_sync();
     __syncthreads();
