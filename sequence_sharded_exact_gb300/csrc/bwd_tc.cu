@@ -257,19 +257,24 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                     tmem_ld_wait(s0);
                     tmem_ld_wait(s1);
                     uint32_t pk[32];
+                    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+                    const float2 nl2e = make_float2(-kLog2e, -kLog2e);
 #pragma unroll
                     for (int e4 = 0; e4 < 16; ++e4) {
-                        const float lq[4] = {lv[e4].x, lv[e4].y, lv[e4].z, lv[e4].w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int col = e4 * 4 + e;
-                            const uint32_t sv = col < 32 ? s0[col] : s1[col - 32];
-                            float pv = ex2_approx(fmaf(__uint_as_float(sv), a.scale_log2, -lq[e] * kLog2e));
-                            if (diag && (w * 64 + col) < r) pv = 0.f;
-                            p[col] = pv;
+                        for (int h = 0; h < 2; ++h) {
+                            const int col = e4 * 4 + h * 2;
+                            const float2 lq = h == 0 ? make_float2(lv[e4].x, lv[e4].y) : make_float2(lv[e4].z, lv[e4].w);
+                            const uint32_t sa = col < 32 ? s0[col] : s1[col - 32];
+                            const uint32_t sb = col < 32 ? s0[col + 1] : s1[col - 31];
+                            const float2 xv = fma2(make_float2(__uint_as_float(sa), __uint_as_float(sb)), sc2, mul2(lq, nl2e));
+                            float p0 = ex2_approx(xv.x), p1 = ex2_approx(xv.y);
+                            if (diag && (w * 64 + col) < r) p0 = 0.f;
+                            if (diag && (w * 64 + col + 1) < r) p1 = 0.f;
+                            p[col] = p0;
+                            p[col + 1] = p1;
+                            pk[e4 * 2 + h] = pack_bf16x2(p0, p1);
                         }
-                        pk[e4 * 2] = pack_bf16x2(p[e4 * 4], p[e4 * 4 + 1]);
-                        pk[e4 * 2 + 1] = pack_bf16x2(p[e4 * 4 + 2], p[e4 * 4 + 3]);
                     }
                     // P^T of query columns [64w, 64w+64) -> TMEM columns [64w, 64w+32)
                     tmem_st_32x32b_x32(tmem + lane_off + kColST + (uint32_t)w * 64, pk);
@@ -297,18 +302,19 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                         tmem_ld_32x32b_x32(tmem + lane_off + kColDPT + (uint32_t)(w * 64 + c * 32), dp);
                         tmem_ld_wait(dp);
                         uint32_t dsp[16];
+                        const float2 sc = make_float2(a.scale, a.scale), neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {
-                            const float dq[4] = {dv4[c * 8 + e4].x, dv4[c * 8 + e4].y, dv4[c * 8 + e4].z,
-                                                 dv4[c * 8 + e4].w};
-                            float ds[4];
+                            const float4 dq = dv4[c * 8 + e4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int col = e4 * 4 + e;
-                                ds[e] = p[c * 32 + col] * (__uint_as_float(dp[col]) - dq[e]) * a.scale;
+                            for (int h = 0; h < 2; ++h) {
+                                const int col = e4 * 4 + h * 2;
+                                const float2 d2 = h == 0 ? make_float2(dq.x, dq.y) : make_float2(dq.z, dq.w);
+                                // dS = (dP - D) * P * scale
+                                const float2 t = fma2(d2, neg1, make_float2(__uint_as_float(dp[col]), __uint_as_float(dp[col + 1])));
+                                const float2 ds = mul2(t, mul2(make_float2(p[c * 32 + col], p[c * 32 + col + 1]), sc));
+                                dsp[e4 * 2 + h] = pack_bf16x2(ds.x, ds.y);
                             }
-                            dsp[e4 * 2] = pack_bf16x2(ds[0], ds[1]);
-                            dsp[e4 * 2 + 1] = pack_bf16x2(ds[2], ds[3]);
                         }
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {

@@ -238,7 +238,8 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
 #pragma unroll
                 for (int c4 = 0; c4 < 2; ++c4)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(r[c4][e]));
+                    for (int e = 0; e < 32; e += 2)
+                        m8[(e >> 1) & 7] = max3f(m8[(e >> 1) & 7], __uint_as_float(r[c4][e]), __uint_as_float(r[c4][e + 1]));
                 tmem_ld_wait(r[2]);
                 tmem_ld_wait(r[3]);
                 if (mask != 0) {
@@ -251,17 +252,18 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
 #pragma unroll
                 for (int c4 = 2; c4 < 4; ++c4)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(r[c4][e]));
-                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                    for (int e = 0; e < 32; e += 2)
+                        m8[(e >> 1) & 7] = max3f(m8[(e >> 1) & 7], __uint_as_float(r[c4][e]), __uint_as_float(r[c4][e + 1]));
+                const float mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                 const float m_tile = mx * sl2;
                 float m_new = m_run;
                 if (m_tile > m_run + 8.0f) m_new = m_tile;
                 const float alpha = (m_new == m_run) ? 1.0f : ex2_approx(m_run - m_new);
                 const float ref = m_new == -INFINITY ? 0.f : m_new;
-                float s8[8];
+                const float2 scale2 = make_float2(sl2, sl2), nref2 = make_float2(-ref, -ref);
+                float2 s4[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) s8[i] = 0.f;
+                for (int i = 0; i < 4; ++i) s4[i] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[32];
@@ -270,15 +272,17 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                         const int c4 = half * 2 + cc;
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            const float p0 = ex2_approx(fmaf(__uint_as_float(r[c4][e]), sl2, -ref));
-                            const float p1 = ex2_approx(fmaf(__uint_as_float(r[c4][e + 1]), sl2, -ref));
-                            s8[(e >> 1) & 7] += p0 + p1;
-                            pk[cc * 16 + e / 2] = pack_bf16x2(p0, p1);
+                            const float2 x2 = fma2(make_float2(__uint_as_float(r[c4][e]), __uint_as_float(r[c4][e + 1])),
+                                                   scale2, nref2);
+                            const float2 p2 = make_float2(ex2_approx(x2.x), ex2_approx(x2.y));
+                            s4[(e >> 1) & 3] = add2(s4[(e >> 1) & 3], p2);
+                            pk[cc * 16 + e / 2] = pack_bf16x2(p2.x, p2.y);
                         }
                     }
                     tmem_st_32x32b_x32(tS + half * 32, pk);
                 }
-                const float rsum = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+                const float2 s2 = add2(add2(s4[0], s4[1]), add2(s4[2], s4[3]));
+                const float rsum = s2.x + s2.y;
                 l_run = l_run * alpha + rsum;
                 tmem_st_wait();
                 const bool need = jj > 0 && alpha != 1.0f;
@@ -292,7 +296,12 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                         tmem_ld_32x32b_x32(tO + c4 * 32, o);
                         tmem_ld_wait(o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 v = mul2(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])),
+                                                  make_float2(alpha, alpha));
+                            o[e] = __float_as_uint(v.x);
+                            o[e + 1] = __float_as_uint(v.y);
+                        }
                         tmem_st_32x32b_x32(tO + c4 * 32, o);
                     }
                     tmem_st_wait();
