@@ -59,8 +59,9 @@ enum : int {
     BAR_Q_EMPTY = 1,
     BAR_K_FULL = 2,
     BAR_V_FULL = BAR_K_FULL + kStages,
-    BAR_KV_EMPTY = BAR_V_FULL + kStages,
-    BAR_S_FULL = BAR_KV_EMPTY + kStages,
+    BAR_K_EMPTY = BAR_V_FULL + kStages,   // K tile read by both S MMAs of its K/V tile
+    BAR_V_EMPTY = BAR_K_EMPTY + kStages,  // V tile read by both P V MMAs
+    BAR_S_FULL = BAR_V_EMPTY + kStages,
     BAR_P_FULL = BAR_S_FULL + 2,
     BAR_O_DONE = BAR_P_FULL + 2,
     BAR_DRAIN = BAR_O_DONE + 2,
@@ -386,12 +387,15 @@ __device__ __forceinline__ void producer_role(const FwdArgs& a, uint32_t sbase, 
                 walk.next(kv_row, kv_nat);
                 const int stage = (int)(kc % kStages);
                 const uint32_t use = kc / kStages;
-                if (use > 0 && !mbar_wait(bar(BAR_KV_EMPTY + stage), (use - 1) & 1, ctl)) { ok = false; break; }
+                // K and V stages are released separately: K once both S MMAs of its tile are done,
+                // about a K/V-tile period before V, so the next K loads that much earlier.
+                if (use > 0 && !mbar_wait(bar(BAR_K_EMPTY + stage), (use - 1) & 1, ctl)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(BAR_K_FULL + stage), kTileBytes);
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
                     tma_load_3d(sbase + kSmemK + (uint32_t)stage * kTileBytes + (uint32_t)half * kHalfBytes, tmK,
                                 bar(BAR_K_FULL + stage), half * 64, kv_row, zkv);
+                if (use > 0 && !mbar_wait(bar(BAR_V_EMPTY + stage), (use - 1) & 1, ctl)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(BAR_V_FULL + stage), kTileBytes);
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
@@ -472,6 +476,7 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
         tc_commit(bar(BAR_S_FULL + 0));
         issue_qk(sbase, tmem, 1, 0);
         tc_commit(bar(BAR_S_FULL + 1));
+        tc_commit(bar(BAR_K_EMPTY + 0));
         if (cur.u.ntiles == 1) tc_commit(bar(BAR_Q_EMPTY));
         while (true) {
             const int stage = (int)(kc % kStages);
@@ -507,10 +512,11 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
             tc_fence_after_sync();
             issue_pv(sbase, tmem, 1, stage, jj > 0);
             tc_commit(bar(BAR_O_DONE + 1));
-            tc_commit(bar(BAR_KV_EMPTY + stage));
+            tc_commit(bar(BAR_V_EMPTY + stage));
             if (!has_next) break;
             issue_qk(sbase, tmem, 1, nstage);
             tc_commit(bar(BAR_S_FULL + 1));
+            tc_commit(bar(BAR_K_EMPTY + nstage));
             if (jn == nxt.u.ntiles - 1) tc_commit(bar(BAR_Q_EMPTY));
             cur = nxt;
             jj = jn;
