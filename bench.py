@@ -35,6 +35,11 @@ WORKLOAD = "zigzag_gqa_128k"
 TRAIN_WORKLOAD = "zigzag_gqa_64k_train"
 METRIC = "ring-attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 
+# DRAM bytes (read + write) per launch of the dominant kernel, from ncu captures summarised in
+# profiles/ (the 32K capture scaled to 128K by rows: each Q/K/V/O byte moves once).  Update or drop
+# an entry whenever that kernel changes.
+TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4 * 648.4e6, ("zigzag_gqa_32k", "fwd"): 648.4e6}
+
 
 def fwd_flops(B, H, L, d, causal):
     """Algorithmic forward flops: 4 B H L^2 d (QK^T and PV), halved when causal."""
@@ -352,7 +357,8 @@ def main():
         "config": config_dict(w, args.step),
         "fraction_of_peak": value / world / peak_b,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_b, "unit": "TFLOP/s",
-                     "frac": achieved / peak_b, "traffic": None,
+                     "frac": achieved / peak_b,
+                     "traffic": TRAFFIC_BYTES.get((args.workload, args.step)),
                      "peak_kind": f"{peak_kind} bf16 burst (MEASURED_PEAKS bf16_tflops)",
                      "frac_of_sustained": achieved / peak_s,
                      "kernel": kname, "timed": note, "algorithmic_flops_per_launch": kflops},
