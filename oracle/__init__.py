@@ -23,7 +23,7 @@ _LIB_PATH = os.path.join(_HERE, "_ring_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-LAYOUTS = {"contiguous": 0, "zigzag": 1}
+LAYOUTS = {"contiguous": 0, "zigzag": 1, "striped": 2}
 
 
 def build(force: bool = False) -> str:

@@ -22,6 +22,8 @@
  * Readings where the pages are silent or garbled (each also listed in the design notes):
  *  - zigzag: the sequence is cut into 2n chunks of C = L/(2n); shard i holds chunk i followed by
  *    chunk 2n-1-i (the page's "segments i and n-1-i" cannot hold for n segments).
+ *  - striped ("Lecture 30" section 3.2: GPU 0 holds tokens 0, 4, 8, ...): shard i holds the natural
+ *    positions i, i + n, i + 2n, ... in increasing order.
  *  - every buffer (q, k, v, out, lse, dout, grads) stores the sequence axis in the layout's order,
  *    i.e. as the concatenation of the shards' local buffers; masking uses natural positions.
  *  - causal mask: key t is visible to query p iff pos(t) <= pos(p) (the query sees itself).
@@ -46,10 +48,15 @@
 #define ORACLE_BAD_ARGS 1
 #define ORACLE_NO_MEMORY 2
 
-/* Natural sequence position of buffer row r ([M4-051] section 4 item 2, zigzag reading above). */
+/* Natural sequence position of buffer row r ([M4-051] section 4 item 2 and [CP-30] section 3.2;
+ * zigzag and striped readings above).  layout 0 contiguous, 1 zigzag, 2 striped. */
 long oracle_natural_position(long r, long L, int n, int layout)
 {
     if (layout == 0) return r;
+    if (layout == 2) {
+        long S = L / n;
+        return (r % S) * n + r / S;
+    }
     long C = L / (2L * n);
     long shard = r / (2 * C);
     long off = r % (2 * C);
@@ -62,7 +69,7 @@ static int check_args(int B, int H, int Hkv, long L, int d, int n, int layout)
     if (B < 1 || H < 1 || Hkv < 1 || L < 1 || d < 1 || n < 1) return 0;
     if (H % Hkv != 0) return 0;
     if (L % n != 0) return 0;
-    if (layout != 0 && layout != 1) return 0;
+    if (layout != 0 && layout != 1 && layout != 2) return 0;
     if (layout == 1 && L % (2L * n) != 0) return 0;
     return 1;
 }
@@ -236,7 +243,7 @@ int oracle_ring_fwd(const float* q, const float* k, const float* v, int B, int H
 int oracle_shard_tiles(long L, int n, int causal, int layout, int T, long* tiles_per_shard)
 {
     if (L < 1 || n < 1 || T < 1 || L % n != 0) return ORACLE_BAD_ARGS;
-    if (layout != 0 && layout != 1) return ORACLE_BAD_ARGS;
+    if (layout != 0 && layout != 1 && layout != 2) return ORACLE_BAD_ARGS;
     if (layout == 1 && L % (2L * n) != 0) return ORACLE_BAD_ARGS;
     const long S = L / n;
     const long tps = (S + T - 1) / T; /* tiles per shard */

@@ -27,6 +27,8 @@ def buffer_to_natural(L, n, layout):
     chunk i followed by chunk 2n-1-i (airsota M4-051, section 4 item 2)."""
     if layout == "contiguous":
         return np.arange(L)
+    if layout == "striped":  # shard i: tokens i, i + n, i + 2n, ... (Lecture 30, section 3.2)
+        return np.concatenate([np.arange(i, L, n) for i in range(n)])
     C = L // (2 * n)
     parts = []
     for i in range(n):
@@ -70,6 +72,9 @@ SMALL_CASES = [
     (1, 2, 2, 32, 8, 8, False, "zigzag"),
     (2, 3, 3, 30, 5, 5, True, "contiguous"),
     (1, 4, 4, 32, 8, 16, True, "zigzag"),
+    (1, 2, 1, 24, 8, 4, True, "striped"),
+    (2, 4, 2, 30, 4, 5, True, "striped"),
+    (1, 2, 2, 32, 8, 8, False, "striped"),
 ]
 
 
@@ -85,13 +90,14 @@ def test_fwd_matches_library_attention(B, H, Hkv, L, d, n, causal, layout):
 
 
 @pytest.mark.parametrize("L,n,layout", [(16, 1, "contiguous"), (24, 3, "zigzag"), (64, 8, "zigzag"),
-                                        (40, 5, "contiguous"), (32, 16, "zigzag")])
+                                        (40, 5, "contiguous"), (32, 16, "zigzag"), (24, 4, "striped"),
+                                        (30, 5, "striped"), (16, 1, "striped")])
 def test_natural_position_is_a_permutation(L, n, layout):
     got = np.array([oracle.natural_position(r, L, n, layout) for r in range(L)])
     np.testing.assert_array_equal(got, buffer_to_natural(L, n, layout))
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ring_result_independent_of_n(layout, causal):
     """The n-step ring equals full attention and does not depend on n (M4-051 section 3)."""
@@ -124,6 +130,18 @@ def test_causal_contiguous_uses_only_earlier_blocks():
             assert pairs[i, j] == expect * B * H, (i, j)
 
 
+def test_causal_striped_pair_counts():
+    """Striped: block (i, j) holds S(S+1)/2 visible pairs when j <= i and S(S-1)/2 when j > i, so
+    every ring step does the same work on every shard."""
+    B, H, Hkv, L, d, n = 1, 1, 1, 40, 4, 5
+    S = L // n
+    q, k, v = rand((B, H, L, d), 34), rand((B, Hkv, L, d), 35), rand((B, Hkv, L, d), 36)
+    _, _, pairs = oracle.ring_fwd(q, k, v, n, True, "striped")
+    for i in range(n):
+        for j in range(n):
+            assert pairs[i, j] == (S * (S + 1) // 2 if j <= i else S * (S - 1) // 2), (i, j)
+
+
 def test_causal_zigzag_pair_counts_are_balanced():
     """Zigzag: every off-diagonal step does half a shard pair (2C^2); every shard the same total."""
     B, H, Hkv, L, d, n = 1, 1, 1, 64, 4, 4
@@ -149,6 +167,8 @@ def test_tile_counts_closed_forms(L, n, T):
     got = oracle.shard_tiles(L, n, True, "zigzag", T)
     np.testing.assert_array_equal(got, [(2 * n - 1) * c * c + c * (c + 1)] * n)
     np.testing.assert_array_equal(oracle.shard_tiles(L, n, False, "zigzag", T), [s * n * s] * n)
+    # striped: query tile a of shard i sees key tile b of every shard iff b <= a
+    np.testing.assert_array_equal(oracle.shard_tiles(L, n, True, "striped", T), [n * s * (s + 1) // 2] * n)
 
 
 def test_tile_counts_golden():
@@ -186,7 +206,7 @@ def test_constant_v_gives_constant_output():
             np.testing.assert_allclose(dk, 0, atol=1e-12)
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
 def test_closed_form_special_cases(layout):
     B, H, Hkv, L, d, n = 1, 2, 1, 32, 8, 4
     q, k, v = rand((B, H, L, d), 51), rand((B, Hkv, L, d), 52), rand((B, Hkv, L, d), 53)
@@ -274,7 +294,7 @@ def test_bwd_sum_identities_and_layout_independence():
         [(B, H, L, d), (B, Hkv, L, d), (B, Hkv, L, d), (B, H, L, d)], start=91))
     ref = None
     for n, layout in ((1, "contiguous"), (4, "contiguous"), (2, "zigzag"), (4, "zigzag"),
-                      (8, "zigzag")):
+                      (8, "zigzag"), (4, "striped"), (8, "striped")):
         perm = buffer_to_natural(L, n, layout)
         q, k, v, do = (a[:, :, perm] for a in (qn, kn, vn, don))
         dq, dk, dv = oracle.attn_bwd(q, k, v, do, n, True, layout)
