@@ -20,7 +20,9 @@
  *     concatenation of the shards' local buffers (shard i occupies rows [i*L/n, (i+1)*L/n)).
  *     With RA_LAYOUT_ZIGZAG, rows [i*S, i*S + C) of shard i are natural positions [i*C, (i+1)*C)
  *     and rows [i*S + C, (i+1)*S) are natural positions [(2n-1-i)*C, (2n-i)*C), with S = L/n and
- *     C = L/(2n).  Outputs come back in the same order as the inputs.
+ *     C = L/(2n).  With RA_LAYOUT_STRIPED, row i*S + t of shard i is natural position t*n + i
+ *     (shard i holds tokens i, i + n, i + 2n, ...: the round-robin split of "Lecture 30:
+ *     TP/PP/SP/CP", section 3.2).  Outputs come back in the same order as the inputs.
  *   - Shapes (row-major, d contiguous): q, out, dout, dq: [B][H][L][d]; k, v, dk, dv:
  *     [B][Hkv][L][d]; lse: [B][H][L] float32, natural logarithm of sum_t exp(s_t).
  *     Query head h reads kv head h / (H / Hkv) (grouped-query attention).  Scale is 1/sqrt(d).
@@ -62,6 +64,7 @@ typedef int ra_status;
 
 #define RA_LAYOUT_CONTIGUOUS 0
 #define RA_LAYOUT_ZIGZAG 1
+#define RA_LAYOUT_STRIPED 2
 
 #define RA_F32 0
 #define RA_BF16 1
@@ -69,7 +72,8 @@ typedef int ra_status;
 /* Kernel paths reported by ring_attn_fwd_path / ring_attn_bwd_path. */
 #define RA_PATH_SIMT 1      /* CUDA-core kernels: any shape, f32 or bf16 */
 #define RA_PATH_TCGEN05 2   /* tensor-core kernels (TMA + tcgen05 + TMEM): bf16, d = 128,
-                               shard (contiguous) or chunk (zigzag) length a multiple of 256 */
+                               shard (contiguous, striped) or chunk (zigzag) length a multiple of
+                               256 (forward) or 128 (backward) */
 
 /* Device status bits (ring_attn_device_status). */
 #define RA_DEVICE_TIMEOUT 1u

@@ -22,7 +22,7 @@
  * Readings where the pages are silent or garbled (each also listed in the design notes):
  *  - zigzag: the sequence is cut into 2n chunks of C = L/(2n); shard i holds chunk i followed by
  *    chunk 2n-1-i (the page's "segments i and n-1-i" cannot hold for n segments).
- *  - striped ("Lecture 30" section 3.2: GPU 0 holds tokens 0, 4, 8, ...): shard i holds the natural
+ *  - striped (the round-robin token split of "Lecture 30" section 3.2): shard i holds the natural
  *    positions i, i + n, i + 2n, ... in increasing order.
  *  - every buffer (q, k, v, out, lse, dout, grads) stores the sequence axis in the layout's order,
  *    i.e. as the concatenation of the shards' local buffers; masking uses natural positions.

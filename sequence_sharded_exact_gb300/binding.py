@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libringattn.so")
 
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_NO_DEVICE, RA_ERR_TIMEOUT = range(6)
-LAYOUTS = {"contiguous": 0, "zigzag": 1}
+LAYOUTS = {"contiguous": 0, "zigzag": 1, "striped": 2}
 PATHS = {1: "simt", 2: "tcgen05"}
 RA_DEVICE_TIMEOUT = 1
 

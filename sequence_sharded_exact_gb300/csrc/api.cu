@@ -90,7 +90,7 @@ ra_status check_problem(const Problem& p)
         return fail(RA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", p.H, p.Hkv);
     if (p.L % p.n != 0)
         return fail(RA_ERR_INVALID_ARG, "L (%d) must be a multiple of n_shards (%d)", p.L, p.n);
-    if (p.layout != RA_LAYOUT_CONTIGUOUS && p.layout != RA_LAYOUT_ZIGZAG)
+    if (p.layout != RA_LAYOUT_CONTIGUOUS && p.layout != RA_LAYOUT_ZIGZAG && p.layout != RA_LAYOUT_STRIPED)
         return fail(RA_ERR_INVALID_ARG, "unknown layout %d", p.layout);
     if (p.layout == RA_LAYOUT_ZIGZAG && p.L % (2 * p.n) != 0)
         return fail(RA_ERR_INVALID_ARG, "zigzag layout needs L (%d) to be a multiple of 2*n_shards",

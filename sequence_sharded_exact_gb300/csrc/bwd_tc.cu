@@ -81,7 +81,7 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;
 struct BwdArgs {
     Geometry geo;
     int B, H, Hkv, G;
-    int T;            // 128-row tiles per head
+    int T;            // 128-row tiles per head (striped: per shard)
     int pairs;        // mirrored tile pairs per kv head
     long long items;  // B * Hkv * pairs
     const float* lse;
@@ -103,24 +103,49 @@ struct KvUnit {
     int ntiles;  // query tiles over all heads of the group
 };
 
+// The query rows of chunk c of the shard the K/V tile meets at step st that can see it, widened
+// down to a tile boundary (striped: the first visible row may sit inside the diagonal tile).
+__device__ __forceinline__ KvRange q_tile_range(const Geometry& g, int shard, int st, int c, int pk)
+{
+    KvRange qr = q_range(g, shard, st, c, pk);
+    if (qr.count == 0) return qr;
+    int i = shard + st;
+    if (i >= g.n) i -= g.n;
+    const int cs = (i * g.cps + c) * g.Lc;  // first row of that chunk
+    const int off = (qr.row0 - cs) / kTile * kTile;
+    qr.row0 = cs + off;
+    qr.count = g.Lc - off;
+    return qr;
+}
+
 __device__ __forceinline__ int q_tiles_per_head(const BwdArgs& a, int shard, int pk)
 {
     int nt = 0;
     for (int st = 0; st < a.geo.n; ++st)
-        for (int c = 0; c < a.geo.cps; ++c) nt += q_range(a.geo, shard, st, c, pk).count / kTile;
+        for (int c = 0; c < a.geo.cps; ++c) nt += q_tile_range(a.geo, shard, st, c, pk).count / kTile;
     return nt;
 }
 
 __device__ __forceinline__ bool unit_of(const BwdArgs& a, long long item, int member, KvUnit& u)
 {
     const int pair = (int)(item % a.pairs);
-    const long long rest = item / a.pairs;
+    long long rest = item / a.pairs;
+    int shard = 0;
+    if (a.geo.layout == 2) {  // striped: tiles of consecutive rows inside one shard
+        shard = (int)(rest % a.geo.n);
+        rest /= a.geo.n;
+    }
     u.g = (int)(rest % a.Hkv);
     u.b = (int)(rest / a.Hkv);
     const int tile = member == 0 ? pair : a.T - 1 - pair;
     if (member == 1 && tile == pair) return false;
-    u.pk = tile * kTile;
-    u.rk = buffer_row(a.geo, u.pk);
+    if (a.geo.layout == 2) {
+        u.rk = shard * a.geo.S + tile * kTile;
+        u.pk = natural_position(a.geo, u.rk);
+    } else {
+        u.pk = tile * kTile;
+        u.rk = buffer_row(a.geo, u.pk);
+    }
     u.shard = u.rk / a.geo.S;
     u.per_head = q_tiles_per_head(a, u.shard, u.pk);
     u.ntiles = u.per_head * a.G;
@@ -136,7 +161,7 @@ struct QWalk {
     {
         while (true) {
             while (st < geo.n) {
-                qr = q_range(geo, shard, st, c, pk);
+                qr = q_tile_range(geo, shard, st, c, pk);
                 nt = qr.count / kTile;
                 if (nt > 0) return;
                 if (++c == geo.cps) {
@@ -237,7 +262,11 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
             for (int t = 0; t < u.ntiles; ++t, ++gt) {
                 int hh, qrow, qnat;
                 walk.next(hh, qrow, qnat);
-                const bool diag = a.geo.causal && qnat == u.pk;
+                // 0 all visible, 1 / 3 diagonal (key row r visible to query column q iff r <= q /
+                // r < q), 2 none; outside the striped layout only the diagonal tile is masked
+                const int mk = a.geo.layout == 2 ? tile_mask(a.geo, qrow, u.rk) : (a.geo.causal && qnat == u.pk ? 1 : 0);
+                // this key row's query columns 64w + c with c < lim are masked
+                const int lim = (mk == 0 ? 0 : (mk == 1 ? r : (mk == 3 ? r + 1 : 1 << 20))) - w * 64;
                 const long long qbase = ((long long)u.b * a.H + u.g * a.G + hh) * a.geo.L + qrow;
                 if (t == 0) {
                     const float4* l4 = reinterpret_cast<const float4*>(a.lse + qbase + w * 64);
@@ -269,8 +298,8 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                             const uint32_t sb = col < 32 ? s0[col + 1] : s1[col - 31];
                             const float2 xv = fma2(make_float2(__uint_as_float(sa), __uint_as_float(sb)), sc2, mul2(lq, nl2e));
                             float p0 = ex2_approx(xv.x), p1 = ex2_approx(xv.y);
-                            if (diag && (w * 64 + col) < r) p0 = 0.f;
-                            if (diag && (w * 64 + col + 1) < r) p1 = 0.f;
+                            if (col < lim) p0 = 0.f;
+                            if (col + 1 < lim) p1 = 0.f;
                             p[col] = p0;
                             p[col + 1] = p1;
                             pk[e4 * 2 + h] = pack_bf16x2(p0, p1);
@@ -724,9 +753,9 @@ cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const 
     a.H = p.H;
     a.Hkv = p.Hkv;
     a.G = p.H / p.Hkv;
-    a.T = p.L / kTile;
+    a.T = (p.layout == 2 ? p.L / p.n : p.L) / kTile;
     a.pairs = (a.T + 1) / 2;
-    a.items = (long long)p.B * p.Hkv * a.pairs;
+    a.items = (long long)p.B * p.Hkv * a.pairs * (p.layout == 2 ? p.n : 1);
     a.lse = lse;
     a.Dv = D;
     a.dq_acc = dq_acc;

@@ -82,9 +82,9 @@ struct FwdArgs {
     Geometry geo;
     int B, H, Hkv, G;
     int mode, step;
-    int U;           // 256-row blocks per head
-    int pairs;       // mirrored block pairs per head
-    long long items; // B * H * pairs
+    int U;           // 256-row blocks per head (striped: per shard)
+    int pairs;       // mirrored block pairs per head (striped: per shard)
+    long long items; // B * H * pairs (striped: B * H * n * pairs)
     void* out;
     float* lse;
     unsigned int* status;
@@ -95,6 +95,7 @@ struct Unit {
     int b, h, g;
     int r0;      // buffer row of the unit's first query row
     int p0;      // its natural position
+    int p_hi;    // largest natural position among its rows
     int shard;   // query shard
     int ntiles;  // K/V tiles walked
 };
@@ -109,7 +110,7 @@ struct KvWalk {
     {
         while (st < st_end) {
             kr = kv_range(geo, shard, st, c, p_hi);
-            nt = kr.count / kTile;
+            nt = (kr.count + kTile - 1) / kTile;  // a partial last tile is masked element-wise
             if (nt > 0) return;
             if (++c == geo.cps) {
                 c = 0;
@@ -122,7 +123,7 @@ struct KvWalk {
     {
         geo = a.geo;
         shard = u.shard;
-        p_hi = u.p0 + kBlock - 1;
+        p_hi = u.p_hi;
         st = a.mode == kFwdFused ? 0 : a.step;
         st_end = a.mode == kFwdFused ? a.geo.n : a.step + 1;
         c = 0;
@@ -148,6 +149,11 @@ __device__ __forceinline__ bool unit_of(const FwdArgs& a, long long item, int me
 {
     const int pair = (int)(item % a.pairs);
     long long rest = item / a.pairs;
+    int shard = 0;
+    if (a.geo.layout == 2) {  // striped: blocks of consecutive rows inside one shard
+        shard = (int)(rest % a.geo.n);
+        rest /= a.geo.n;
+    }
     const int hg = (int)(rest % a.G);
     rest /= a.G;
     u.g = (int)(rest % a.Hkv);
@@ -155,14 +161,20 @@ __device__ __forceinline__ bool unit_of(const FwdArgs& a, long long item, int me
     u.h = u.g * a.G + hg;
     const int blk = member == 0 ? pair : a.U - 1 - pair;
     if (member == 1 && blk == pair) return false;
-    u.p0 = blk * kBlock;
-    u.r0 = buffer_row(a.geo, u.p0);
+    if (a.geo.layout == 2) {
+        u.r0 = shard * a.geo.S + blk * kBlock;
+        u.p0 = natural_position(a.geo, u.r0);
+    } else {
+        u.p0 = blk * kBlock;
+        u.r0 = buffer_row(a.geo, u.p0);
+    }
+    u.p_hi = natural_position(a.geo, u.r0 + kBlock - 1);
     u.shard = u.r0 / a.geo.S;
     int nt = 0;
     const int s0 = a.mode == kFwdFused ? 0 : a.step;
     const int s1 = a.mode == kFwdFused ? a.geo.n : a.step + 1;
     for (int st = s0; st < s1; ++st)
-        for (int c = 0; c < a.geo.cps; ++c) nt += kv_range(a.geo, u.shard, st, c, u.p0 + kBlock - 1).count / kTile;
+        for (int c = 0; c < a.geo.cps; ++c) nt += (kv_range(a.geo, u.shard, st, c, u.p_hi).count + kTile - 1) / kTile;
     u.ntiles = nt;
     return true;
 }
@@ -207,14 +219,19 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                 a.lse[row_g] = -INFINITY;
                 continue;
             }
-            const int pq = u.p0 + w * kTile;  // natural position of this Q tile's first row
+            const int pq = u.p0 + w * kTile;  // natural position of this Q tile's first row (not striped)
             float m_run = -INFINITY, l_run = 0.f;
             KvWalk walk;
             walk.begin(a, u);
             for (int jj = 0; jj < u.ntiles; ++jj, ++tcount) {
                 int kv_row, kv_nat;
                 walk.next(kv_row, kv_nat);
-                const int mask = !a.geo.causal ? 0 : (kv_nat < pq ? 0 : (kv_nat == pq ? 1 : 2));
+                // 0 all visible, 1 / 3 diagonal (key c visible to row r iff c <= r / c < r), 2 none;
+                // the natural positions of tile starts decide it unless the layout is striped
+                const int mask = a.geo.layout == 2 ? tile_mask(a.geo, u.r0 + w * kTile, kv_row)
+                                 : (!a.geo.causal ? 0 : (kv_nat < pq ? 0 : (kv_nat == pq ? 1 : 2)));
+                // keys c > lim of this row are masked
+                const int lim = mask == 2 ? -1 : (mask == 3 ? rw - 1 : rw);
                 if (!mbar_wait(bar_s, tcount & 1, ctl)) return;
                 tc_fence_after_sync();
                 __syncwarp();
@@ -234,7 +251,7 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                     for (int c4 = 0; c4 < 2; ++c4)
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if (mask == 2 || (c4 * 32 + e) > rw) r[c4][e] = __float_as_uint(-INFINITY);
+                            if ((c4 * 32 + e) > lim) r[c4][e] = __float_as_uint(-INFINITY);
                 }
 #pragma unroll
                 for (int c4 = 0; c4 < 2; ++c4)
@@ -248,7 +265,7 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                     for (int c4 = 2; c4 < 4; ++c4)
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if (mask == 2 || (c4 * 32 + e) > rw) r[c4][e] = __float_as_uint(-INFINITY);
+                            if ((c4 * 32 + e) > lim) r[c4][e] = __float_as_uint(-INFINITY);
                 }
 #pragma unroll
                 for (int c4 = 2; c4 < 4; ++c4)
@@ -641,9 +658,9 @@ cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const 
     a.G = p.H / p.Hkv;
     a.mode = mode;
     a.step = step;
-    a.U = p.L / kBlock;
+    a.U = (p.layout == 2 ? p.L / p.n : p.L) / kBlock;
     a.pairs = (a.U + 1) / 2;
-    a.items = (long long)p.B * p.H * a.pairs;
+    a.items = (long long)p.B * p.H * a.pairs * (p.layout == 2 ? p.n : 1);
     a.out = out;
     a.lse = lse;
     a.status = status;

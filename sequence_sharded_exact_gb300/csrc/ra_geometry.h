@@ -7,7 +7,10 @@
 // positions:
 //   contiguous layout: 1 chunk per shard, natural range [i*S, (i+1)*S);
 //   zigzag layout:     2 chunks per shard of C = L/(2n) rows: natural chunk i, then natural chunk
-//                      2n-1-i (M4-051 section 4 item 2; "Lecture 30: TP/PP/SP/CP" section 3.2).
+//                      2n-1-i (M4-051 section 4 item 2; "Lecture 30: TP/PP/SP/CP" section 3.2);
+//   striped layout:    1 chunk per shard holding natural positions i, i + n, i + 2n, ... (the
+//                      round-robin token split of "Lecture 30" section 3.2): consecutive rows of a
+//                      chunk are `stride` = n positions apart (1 in the other layouts).
 // Ring schedule (LLM-101-CN "distributed hands-on code", section 6.2; Lecture 30 section 3.2): at
 // step r the rows of shard i use the K/V of shard (i - r) mod n.  Within a shard the chunks are
 // walked in buffer order and, causally, only keys whose natural position does not exceed the
@@ -26,11 +29,12 @@ namespace ra {
 struct Geometry {
     int L;       // sequence length
     int n;       // shards
-    int layout;  // 0 contiguous, 1 zigzag
+    int layout;  // 0 contiguous, 1 zigzag, 2 striped
     int causal;  // 0 / 1
     int S;       // rows per shard
     int Lc;      // rows per chunk
     int cps;     // chunks per shard (1 or 2)
+    int stride;  // natural-position step between consecutive rows of a chunk (n if striped, else 1)
 };
 
 RA_HD Geometry make_geometry(int L, int n, int layout, int causal)
@@ -43,12 +47,14 @@ RA_HD Geometry make_geometry(int L, int n, int layout, int causal)
     g.S = L / n;
     g.cps = layout == 1 ? 2 : 1;
     g.Lc = g.S / g.cps;
+    g.stride = layout == 2 ? n : 1;
     return g;
 }
 
 // Natural position of the first row of buffer chunk c.
 RA_HD int chunk_natural_start(const Geometry& g, int c)
 {
+    if (g.layout == 2) return c;
     if (g.cps == 1) return c * g.Lc;
     int shard = c >> 1;
     int nat_chunk = (c & 1) ? (2 * g.n - 1 - shard) : shard;
@@ -59,12 +65,13 @@ RA_HD int chunk_natural_start(const Geometry& g, int c)
 RA_HD int natural_position(const Geometry& g, int r)
 {
     int c = r / g.Lc;
-    return chunk_natural_start(g, c) + (r - c * g.Lc);
+    return chunk_natural_start(g, c) + (r - c * g.Lc) * g.stride;
 }
 
 // Buffer row holding natural position p.
 RA_HD int buffer_row(const Geometry& g, int p)
 {
+    if (g.layout == 2) return (p % g.n) * g.S + p / g.n;
     if (g.cps == 1) return p;
     int nc = p / g.Lc;
     int off = p - nc * g.Lc;
@@ -72,8 +79,8 @@ RA_HD int buffer_row(const Geometry& g, int p)
     return shard * g.S + (nc < g.n ? 0 : g.Lc) + off;
 }
 
-// One contiguous run of key rows of a ring step: buffer rows [row0, row0 + count) hold natural
-// positions [nat0, nat0 + count).
+// One run of key rows of a ring step: buffer rows [row0, row0 + count) hold natural positions
+// nat0, nat0 + stride, ..., in increasing order.
 struct KvRange {
     int row0;
     int nat0;
@@ -92,8 +99,8 @@ RA_HD KvRange kv_range(const Geometry& g, int i, int step, int c, int p_hi)
     kr.nat0 = chunk_natural_start(g, ck);
     int cnt = g.Lc;
     if (g.causal) {
-        cnt = p_hi + 1 - kr.nat0;
-        if (cnt < 0) cnt = 0;
+        // rows at positions <= p_hi
+        cnt = p_hi < kr.nat0 ? 0 : (g.stride == 1 ? p_hi - kr.nat0 : (p_hi - kr.nat0) / g.stride) + 1;
         if (cnt > g.Lc) cnt = g.Lc;
     }
     kr.count = cnt;
@@ -113,14 +120,33 @@ RA_HD KvRange q_range(const Geometry& g, int j, int step, int c, int p_lo)
     qr.nat0 = chunk_natural_start(g, cq);
     int first = 0;
     if (g.causal) {
-        first = p_lo - qr.nat0;
-        if (first < 0) first = 0;
+        // rows at positions >= p_lo
+        first = p_lo <= qr.nat0 ? 0
+                : (g.stride == 1 ? p_lo - qr.nat0 : (p_lo - qr.nat0 + g.stride - 1) / g.stride);
         if (first > g.Lc) first = g.Lc;
     }
     qr.row0 += first;
-    qr.nat0 += first;
+    qr.nat0 += first * g.stride;
     qr.count = g.Lc - first;
     return qr;
+}
+
+// Causal relation of a query tile and a key tile of `tile` rows each, both starting at multiples
+// of `tile` inside their chunks (chunk lengths multiples of `tile`), given by their first buffer
+// rows.  0: every key visible to every query; 1: diagonal, key c visible to query r iff c <= r;
+// 3: diagonal, iff c < r (striped, key shard after the query shard); 2: no key visible.
+RA_HD int tile_mask(const Geometry& g, int q_row0, int kv_row0)
+{
+    if (!g.causal) return 0;
+    if (g.layout == 2) {
+        const int i = q_row0 / g.S, u0 = q_row0 - i * g.S;
+        const int j = kv_row0 / g.S, t0 = kv_row0 - j * g.S;
+        if (t0 < u0) return 0;
+        if (t0 > u0) return 2;
+        return j <= i ? 1 : 3;
+    }
+    const int pq = natural_position(g, q_row0), pk = natural_position(g, kv_row0);
+    return pk < pq ? 0 : (pk == pq ? 1 : 2);
 }
 
 }  // namespace ra

@@ -16,8 +16,9 @@ from __future__ import annotations
 
 import torch
 
-# The five workloads of the benchmark and parity suite (sizes as quoted on the pages' examples:
-# 128K tokens over 8 shards of 16K, head dim 128, inner tile 128).
+# The workloads of the benchmark and parity suite (sizes as quoted on the pages' examples: 128K
+# tokens over 8 shards of 16K, head dim 128, inner tile 128).  The striped ones repeat the zigzag
+# sizes in the round-robin layout.
 WORKLOADS = {
     "tiny_f32": dict(B=1, H=1, Hkv=1, L=256, d=64, n=4, causal=False, layout="contiguous",
                      dtype=torch.float32, spike_frac=0.0, backward=False, seed=1001),
@@ -30,6 +31,11 @@ WORKLOADS = {
     "zigzag_gqa_64k_train": dict(B=1, H=32, Hkv=8, L=65536, d=128, n=16, causal=True,
                                  layout="zigzag", dtype=torch.bfloat16, spike_frac=0.0,
                                  backward=True, seed=1005),
+    "striped_gqa_128k": dict(B=1, H=32, Hkv=8, L=131072, d=128, n=8, causal=True, layout="striped",
+                             dtype=torch.bfloat16, spike_frac=0.01, backward=False, seed=1006),
+    "striped_gqa_64k_train": dict(B=1, H=32, Hkv=8, L=65536, d=128, n=16, causal=True,
+                                  layout="striped", dtype=torch.bfloat16, spike_frac=0.0,
+                                  backward=True, seed=1007),
 }
 
 

@@ -78,11 +78,16 @@ def test_path_selection():
     assert binding.fwd_path(1, 1, 1, 256, 64, 4, False, "contiguous", torch.float32) == "simt"
     assert binding.fwd_path(1, 2, 2, 384, 128, 3, True, "zigzag", torch.bfloat16) == "simt"
     assert binding.fwd_path(1, 2, 2, 512, 64, 2, True, "zigzag", torch.bfloat16) == "simt"
+    # striped: the tensor-core paths need shards of whole 256-row (forward) / 128-row (backward) tiles
+    assert binding.fwd_path(1, 32, 8, 131072, 128, 8, True, "striped", torch.bfloat16) == "tcgen05"
+    assert binding.fwd_path(1, 2, 2, 384, 128, 3, True, "striped", torch.bfloat16) == "simt"
+    assert binding.bwd_path(1, 2, 2, 384, 128, 3, True, "striped", torch.bfloat16) == "tcgen05"
+    assert binding.bwd_path(1, 2, 2, 600, 128, 3, True, "striped", torch.bfloat16) == "simt"
 
 
 @pytest.mark.parametrize("L,n,T", [(8192, 8, 128), (32768, 8, 128), (1000, 5, 64), (384, 3, 128),
                                    (4096, 16, 128), (96, 4, 7)])
-@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
 @pytest.mark.parametrize("causal", [True, False])
 def test_shard_tiles_match_oracle(L, n, T, layout, causal):
     if layout == "zigzag" and L % (2 * n):
@@ -95,6 +100,10 @@ def test_shard_tiles_workloads():
     assert binding.shard_tiles(8192, 8, True, "contiguous") == [36 + 64 * i for i in range(8)]
     assert binding.shard_tiles(131072, 8, True, "zigzag") == [65600] * 8
     assert binding.shard_tiles(65536, 16, True, "zigzag") == [8208] * 16
+    # striped, S = L / n rows per shard in s = S / 128 tiles: every pair of shards meets in a
+    # triangle of s (s + 1) / 2 tiles
+    assert binding.shard_tiles(131072, 8, True, "striped") == [8 * 128 * 129 // 2] * 8
+    assert binding.shard_tiles(65536, 16, True, "striped") == [16 * 32 * 33 // 2] * 16
 
 
 def test_workspace_sizes(lib):

@@ -45,6 +45,10 @@ TC_BWD_CASES = [
     (1, 2, 1, 1536, 3, True, "contiguous"),
     (1, 8, 2, 2048, 8, True, "zigzag"),
     (1, 4, 4, 1024, 4, False, "zigzag"),
+    (1, 4, 2, 1024, 4, True, "striped"),
+    (1, 2, 1, 1536, 3, True, "striped"),     # 4 tiles per shard: two mirrored pairs
+    (1, 2, 2, 384, 3, True, "striped"),      # one tile per shard
+    (2, 2, 2, 512, 2, False, "striped"),
 ]
 
 
@@ -63,6 +67,8 @@ BWD_CASES = [
     (1, 2, 2, 1024, 128, 4, True, "contiguous", torch.bfloat16),
     (2, 4, 1, 512, 128, 4, True, "zigzag", torch.bfloat16),
     (1, 2, 1, 600, 128, 3, True, "contiguous", torch.bfloat16),
+    (1, 2, 1, 384, 64, 3, True, "striped", torch.float32),
+    (1, 2, 2, 600, 128, 3, True, "striped", torch.bfloat16),
 ]
 
 

@@ -37,7 +37,7 @@ def sampled_rows(w, count, seed):
 
 
 @pytest.mark.parametrize("name", ["causal_contig_8k", "zigzag_gqa_32k", "zigzag_gqa_128k",
-                                  "zigzag_gqa_64k_train"])
+                                  "zigzag_gqa_64k_train", "striped_gqa_128k"])
 def test_full_size_forward_sampled_rows(name):
     w = synth.WORKLOADS[name]
     B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
@@ -72,12 +72,12 @@ def test_full_size_stepwise_matches_fused():
     assert (l1 - l2).abs().max().item() < 1e-3
 
 
-def test_full_size_training_backward():
-    """The training workload (L=65536, n=16, zigzag, causal, GQA 4:1): dQ on sampled rows and
+@pytest.mark.parametrize("name", ["zigzag_gqa_64k_train", "striped_gqa_64k_train"])
+def test_full_size_training_backward(name):
+    """The training workload (L=65536, n=16, causal, GQA 4:1): dQ on sampled rows and
     dK/dV on the last keys of the sequence (whose visible queries are few enough for the oracle),
     plus identities that hold at any size: sum over keys of dV equals the group's summed dO, and
     the sum over keys of dK vanishes."""
-    name = "zigzag_gqa_64k_train"
     w = synth.WORKLOADS[name]
     B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
     x = synth.make_workload(name, device=DEV, gen_device=DEV, with_dout=True)

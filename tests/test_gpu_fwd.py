@@ -57,6 +57,10 @@ TC_CASES = [
     (1, 2, 2, 768, 3, True, "contiguous"),   # odd number of 256-row blocks
     (1, 3, 1, 1280, 1, True, "contiguous"),  # n = 1, odd blocks, GQA 3:1
     (1, 4, 2, 2048, 8, True, "contiguous"),
+    (1, 4, 2, 2048, 4, True, "striped"),
+    (1, 2, 1, 1024, 2, False, "striped"),
+    (2, 2, 2, 3072, 3, True, "striped"),     # 4 blocks of 256 rows per shard
+    (1, 4, 1, 4096, 8, True, "striped"),     # 2 blocks per shard: one mirrored pair
 ]
 
 
@@ -79,6 +83,8 @@ SIMT_CASES = [
     (1, 2, 2, 512, 64, 2, True, "zigzag", torch.bfloat16),         # head dim 64
     (2, 4, 2, 640, 128, 5, True, "zigzag", torch.float32),
     (1, 2, 1, 300, 64, 3, False, "contiguous", torch.float32),
+    (1, 2, 2, 384, 128, 3, True, "striped", torch.bfloat16),       # S = 128: below a block
+    (1, 2, 1, 600, 64, 5, True, "striped", torch.float32),
 ]
 
 
@@ -91,6 +97,8 @@ def test_simt_fwd_matches_oracle(B, H, Hkv, L, d, n, causal, layout, dtype):
     (1, 4, 2, 1024, 128, 4, "zigzag", torch.bfloat16),       # tensor-core ring steps
     (1, 2, 2, 1024, 128, 2, "contiguous", torch.bfloat16),
     (1, 2, 1, 600, 64, 3, "zigzag", torch.float32),          # SIMT ring steps
+    (1, 4, 2, 2048, 128, 4, "striped", torch.bfloat16),
+    (1, 2, 1, 600, 64, 3, "striped", torch.float32),
 ])
 def test_stepwise_ring_matches_oracle_and_fused(B, H, Hkv, L, d, n, layout, dtype):
     """n ring-step launches folded with the LSE merge equal full attention and the fused kernel."""
@@ -159,3 +167,27 @@ def test_lse_merge_kernel():
     ref_o[both_empty] = got_o[both_empty]
     assert torch.allclose(l_acc.cpu().double(), lse, atol=1e-5, rtol=0, equal_nan=False)
     assert (got_o - ref_o).abs().max().item() < 1e-5
+
+
+@pytest.mark.parametrize("d,L,dtype", [(128, 2048, torch.bfloat16), (64, 600, torch.float32)])
+def test_striped_ring_step_first_rows(d, L, dtype):
+    """Striped causal: at step r > 0 the query shard i faces key shard j = i - r (mod n).  Where
+    j > i the shard's first query row (natural position i) sees none of shard j (o = 0,
+    lse = -inf); every other row sees at least shard j's first key."""
+    n = 4
+    S = L // n
+    x = inputs(1, 2, 1, L, d, dtype, seed=8)
+    q, k, v = (x[t].to(DEV) for t in ("q", "k", "v"))
+    for step in range(1, n):
+        o, lse = ra.ring_step_fwd(q, k, v, n, step, True, "striped")
+        torch.cuda.synchronize()
+        lse_np = lse.cpu().numpy()
+        for i in range(n):
+            j = (i - step) % n
+            rows = lse_np[:, :, i * S:(i + 1) * S]
+            assert np.all(np.isfinite(rows[:, :, 1:]))
+            if j > i:
+                assert np.all(np.isneginf(rows[:, :, 0]))
+                assert torch.count_nonzero(o[:, :, i * S]).item() == 0
+            else:
+                assert np.all(np.isfinite(rows[:, :, 0]))
