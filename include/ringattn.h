@@ -176,6 +176,30 @@ RA_API size_t ring_attn_bwd_static_scratch_capacity(void);
 RA_API ra_status ring_attn_shard_tiles(int L, int n_shards, int causal, int layout, int tile,
                                 long long* tiles_per_shard);
 
+/*
+ * ring_attn_fwd_tile_visits / ring_attn_bwd_tile_visits -- ring_attn_fwd / ring_attn_bwd that also
+ * count the work the tensor-core kernels do: for every tile pair a kernel computes, 1 is added to
+ * visits[i * n_shards + j], i the shard of the query rows and j the shard of the key rows
+ * (forward: a 256-row query block of one query head against a 128-row K/V tile; backward: a
+ * 128-row query tile of one query head against a 128-row K/V tile).  The causal skip of M4-051
+ * section 3 shows as visits[i][j] == 0 for every key shard whose positions all follow the query
+ * shard's, and a computed pair always holds at least one visible (query, key) pair.
+ *   visits: DEVICE array of n_shards * n_shards unsigned 64-bit counters, 16-byte aligned, added
+ *   to (the caller zeroes it).  Other arguments and results as in ring_attn_fwd / ring_attn_bwd.
+ *   RA_ERR_UNSUPPORTED when the problem does not take the tensor-core path (ring_attn_*_path).
+ */
+RA_API ra_status ring_attn_fwd_tile_visits(const void* q, const void* k, const void* v, void* out,
+                                           float* lse, int B, int H, int Hkv, int L, int d,
+                                           int n_shards, int causal, int layout, int dtype,
+                                           unsigned long long* visits, void* stream);
+RA_API ra_status ring_attn_bwd_tile_visits(const void* q, const void* k, const void* v,
+                                           const void* out, const float* lse, const void* dout,
+                                           void* dq, void* dk, void* dv, int grad_dtype,
+                                           void* workspace, size_t workspace_bytes, int B, int H,
+                                           int Hkv, int L, int d, int n_shards, int causal,
+                                           int layout, int dtype, unsigned long long* visits,
+                                           void* stream);
+
 /* Which kernel path ring_attn_fwd / ring_attn_bwd take for these arguments (RA_PATH_*), written
  * to *path (HOST pointer).  Same argument checks as the calls themselves; no CUDA call. */
 RA_API ra_status ring_attn_fwd_path(int B, int H, int Hkv, int L, int d, int n_shards, int causal,

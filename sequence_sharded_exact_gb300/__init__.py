@@ -11,7 +11,9 @@ from .binding import (  # noqa: F401
     device_status,
     fwd,
     fwd_stepwise,
+    fwd_tile_visits,
     bwd,
+    bwd_tile_visits,
     fwd_path,
     bwd_path,
     library,

@@ -28,7 +28,7 @@ EXPORTS = (
     "ring_attn_fwd_stepwise_workspace_size", "ring_attn_bwd", "ring_attn_bwd_workspace_size",
     "ring_attn_shard_tiles", "ring_attn_fwd_path", "ring_attn_bwd_path", "ring_attn_device_status",
     "ring_attn_last_error", "ring_attn_abi_version", "ring_attn_bwd_static_scratch",
-    "ring_attn_bwd_static_scratch_capacity",
+    "ring_attn_bwd_static_scratch_capacity", "ring_attn_fwd_tile_visits", "ring_attn_bwd_tile_visits",
 )
 
 
@@ -71,6 +71,11 @@ def library():
         lib.ring_attn_bwd_static_scratch.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I,
                                                      I, I, I, P]
         lib.ring_attn_bwd_static_scratch.restype = ctypes.c_int
+        lib.ring_attn_fwd_tile_visits.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P]
+        lib.ring_attn_fwd_tile_visits.restype = ctypes.c_int
+        lib.ring_attn_bwd_tile_visits.argtypes = [P, P, P, P, P, P, P, P, P, I, P, SZ, I, I, I, I, I,
+                                                  I, I, I, I, P, P]
+        lib.ring_attn_bwd_tile_visits.restype = ctypes.c_int
         lib.ring_attn_bwd_static_scratch_capacity.argtypes = []
         lib.ring_attn_bwd_static_scratch_capacity.restype = SZ
         for name in EXPORTS:
@@ -143,8 +148,24 @@ def bwd_path(B, H, Hkv, L, d, n_shards, causal, layout, dtype):
     return PATHS[out.value]
 
 
+def _visits(n_shards, device):
+    return torch.zeros((n_shards, n_shards), dtype=torch.int64, device=device)
+
+
 def fwd(q, k, v, n_shards, causal=True, layout="zigzag", out=None, lse=None, stream=None):
     """Ring Attention forward.  Returns (out [B,H,L,d] q.dtype, lse [B,H,L] float32)."""
+    return _fwd(q, k, v, n_shards, causal, layout, out, lse, None, stream)
+
+
+def fwd_tile_visits(q, k, v, n_shards, causal=True, layout="zigzag", stream=None):
+    """ring_attn_fwd_tile_visits: the forward plus the count of (256-row query block, 128-row K/V
+    tile) pairs computed per (query shard, key shard).  Returns (out, lse, visits [n, n] int64)."""
+    visits = _visits(n_shards, q.device)
+    out, lse = _fwd(q, k, v, n_shards, causal, layout, None, None, visits, stream)
+    return out, lse, visits
+
+
+def _fwd(q, k, v, n_shards, causal, layout, out, lse, visits, stream):
     B, H, Hkv, L, d = _dims(q, k)
     for t, nm in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, nm, q.device)
@@ -154,9 +175,12 @@ def fwd(q, k, v, n_shards, causal=True, layout="zigzag", out=None, lse=None, str
         lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
     _need(out, "out", q.device)
     _need(lse, "lse", q.device)
-    _check(library().ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, L, d,
-                                   int(n_shards), int(causal), _layout(layout), _dtype_code(q.dtype),
-                                   _stream(stream, q.device)))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, L, d, int(n_shards),
+            int(causal), _layout(layout), _dtype_code(q.dtype))
+    if visits is None:
+        _check(library().ring_attn_fwd(*args, _stream(stream, q.device)))
+    else:
+        _check(library().ring_attn_fwd_tile_visits(*args, _ptr(visits), _stream(stream, q.device)))
     return out, lse
 
 
@@ -214,6 +238,22 @@ def bwd_workspace_size(B, H, Hkv, L, d, grad_dtype=torch.float32):
 def bwd(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigzag",
         grad_dtype=torch.float32, dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Ring Attention backward.  Returns (dq, dk, dv) in grad_dtype."""
+    return _bwd(q, k, v, out, lse, dout, n_shards, causal, layout, grad_dtype, dq, dk, dv,
+                workspace, None, stream)
+
+
+def bwd_tile_visits(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigzag",
+                    grad_dtype=torch.float32, stream=None):
+    """ring_attn_bwd_tile_visits: the backward plus the count of (128-row query tile, 128-row K/V
+    tile) pairs computed per (query shard, key shard).  Returns (dq, dk, dv, visits [n, n] int64)."""
+    visits = _visits(n_shards, q.device)
+    dq, dk, dv = _bwd(q, k, v, out, lse, dout, n_shards, causal, layout, grad_dtype, None, None,
+                      None, None, visits, stream)
+    return dq, dk, dv, visits
+
+
+def _bwd(q, k, v, out, lse, dout, n_shards, causal, layout, grad_dtype, dq, dk, dv, workspace,
+         visits, stream):
     B, H, Hkv, L, d = _dims(q, k)
     if dq is None:
         dq = torch.empty((B, H, L, d), dtype=grad_dtype, device=q.device)
@@ -224,11 +264,13 @@ def bwd(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigzag",
     need = bwd_workspace_size(B, H, Hkv, L, d, grad_dtype)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    _check(library().ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
-                                   _ptr(dq), _ptr(dk), _ptr(dv), _dtype_code(grad_dtype),
-                                   _ptr(workspace), workspace.numel(), B, H, Hkv, L, d,
-                                   int(n_shards), int(causal), _layout(layout),
-                                   _dtype_code(q.dtype), _stream(stream, q.device)))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+            _ptr(dv), _dtype_code(grad_dtype), _ptr(workspace), workspace.numel(), B, H, Hkv, L, d,
+            int(n_shards), int(causal), _layout(layout), _dtype_code(q.dtype))
+    if visits is None:
+        _check(library().ring_attn_bwd(*args, _stream(stream, q.device)))
+    else:
+        _check(library().ring_attn_bwd_tile_visits(*args, _ptr(visits), _stream(stream, q.device)))
     return dq, dk, dv
 
 

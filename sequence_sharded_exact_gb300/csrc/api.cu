@@ -171,26 +171,51 @@ ra_status ring_attn_bwd_path(int B, int H, int Hkv, int L, int d, int n_shards, 
     return RA_OK;
 }
 
-ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
-                        int H, int Hkv, int L, int d, int n_shards, int causal, int layout,
-                        int dtype, void* stream)
+namespace {
+
+ra_status fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, const Problem& p,
+                   unsigned long long* visits, void* stream)
 {
-    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
     ra_status st = check_problem(p);
     if (st != RA_OK) return st;
     if ((st = check_ptrs({q, k, v, out, lse})) != RA_OK) return st;
+    const bool tc = tc_fwd_supported(p);
+    if (visits) {
+        if ((st = check_ptrs({visits})) != RA_OK) return st;
+        if (!tc) return fail(RA_ERR_UNSUPPORTED, "tile visits are counted on the tensor-core path only");
+    }
     if ((st = check_device()) != RA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (tc_fwd_supported(p)) {
+    if (tc) {
         unsigned int* sw = status_word(&e);
         if (!sw) return cuda_fail(e, "status word");
-        e = launch_fwd_tc(p, q, k, v, out, lse, kFwdFused, 0, sw, s);
+        e = launch_fwd_tc(p, q, k, v, out, lse, kFwdFused, 0, sw, s, visits);
     } else {
         e = launch_fwd_simt(p, q, k, v, out, lse, kFwdFused, 0, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "ring_attn_fwd launch");
     return RA_OK;
+}
+
+}  // namespace
+
+ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                        int H, int Hkv, int L, int d, int n_shards, int causal, int layout,
+                        int dtype, void* stream)
+{
+    return fwd_impl(q, k, v, out, lse, Problem{B, H, Hkv, L, d, n_shards, causal, layout, dtype},
+                    nullptr, stream);
+}
+
+ra_status ring_attn_fwd_tile_visits(const void* q, const void* k, const void* v, void* out,
+                                    float* lse, int B, int H, int Hkv, int L, int d, int n_shards,
+                                    int causal, int layout, int dtype,
+                                    unsigned long long* visits, void* stream)
+{
+    if (!visits) return fail(RA_ERR_INVALID_ARG, "visits is NULL");
+    return fwd_impl(q, k, v, out, lse, Problem{B, H, Hkv, L, d, n_shards, causal, layout, dtype},
+                    visits, stream);
 }
 
 ra_status ring_attn_ring_step_fwd(const void* q, const void* k, const void* v, float* o_part,
@@ -286,18 +311,23 @@ size_t ring_attn_bwd_workspace_size(int B, int H, int Hkv, int L, int d, int gra
     return bytes;
 }
 
-ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
-                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                        int grad_dtype, void* workspace, size_t workspace_bytes, int B, int H,
-                        int Hkv, int L, int d, int n_shards, int causal, int layout, int dtype,
-                        void* stream)
+namespace {
+
+ra_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, int grad_dtype, void* workspace,
+                   size_t workspace_bytes, const Problem& p, unsigned long long* visits, void* stream)
 {
-    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    const int B = p.B, H = p.H, Hkv = p.Hkv, L = p.L, d = p.d, dtype = p.dtype;
     ra_status st = check_problem(p);
     if (st != RA_OK) return st;
     if (grad_dtype != RA_F32 && grad_dtype != RA_BF16)
         return fail(RA_ERR_INVALID_ARG, "unknown grad dtype %d", grad_dtype);
     if ((st = check_ptrs({q, k, v, out, lse, dout, dq, dk, dv, workspace})) != RA_OK) return st;
+    const bool tc = tc_bwd_supported(p);
+    if (visits) {
+        if ((st = check_ptrs({visits})) != RA_OK) return st;
+        if (!tc) return fail(RA_ERR_UNSUPPORTED, "tile visits are counted on the tensor-core path only");
+    }
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     const size_t need = ring_attn_bwd_workspace_size(B, H, Hkv, L, d, grad_dtype);
@@ -310,7 +340,7 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
     float* D = reinterpret_cast<float*>(ws);
     cudaError_t e = launch_bwd_preprocess(out, dout, dtype, rows, d, D, s);
     if (e != cudaSuccess) return cuda_fail(e, "ring_attn_bwd preprocess launch");
-    if (tc_bwd_supported(p)) {
+    if (tc) {
         unsigned int* sw = status_word(&e);
         if (!sw) return cuda_fail(e, "status word");
         float* dq_acc = grad_dtype == RA_F32
@@ -318,7 +348,7 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
                             : reinterpret_cast<float*>(ws + align256((size_t)rows * sizeof(float)));
         e = launch_zero(dq_acc, rows * d, s);
         if (e == cudaSuccess)
-            e = launch_bwd_tc(p, q, k, v, dout, D, lse, dq_acc, dk, dv, grad_dtype, sw, s);
+            e = launch_bwd_tc(p, q, k, v, dout, D, lse, dq_acc, dk, dv, grad_dtype, sw, s, visits);
         if (e == cudaSuccess && grad_dtype != RA_F32)
             e = launch_convert(dq_acc, dq, grad_dtype, rows * d, 1.0f, s);
     } else {
@@ -326,6 +356,30 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
     }
     if (e != cudaSuccess) return cuda_fail(e, "ring_attn_bwd launch");
     return RA_OK;
+}
+
+}  // namespace
+
+ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        int grad_dtype, void* workspace, size_t workspace_bytes, int B, int H,
+                        int Hkv, int L, int d, int n_shards, int causal, int layout, int dtype,
+                        void* stream)
+{
+    return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, grad_dtype, workspace, workspace_bytes,
+                    Problem{B, H, Hkv, L, d, n_shards, causal, layout, dtype}, nullptr, stream);
+}
+
+ra_status ring_attn_bwd_tile_visits(const void* q, const void* k, const void* v, const void* out,
+                                    const float* lse, const void* dout, void* dq, void* dk,
+                                    void* dv, int grad_dtype, void* workspace,
+                                    size_t workspace_bytes, int B, int H, int Hkv, int L, int d,
+                                    int n_shards, int causal, int layout, int dtype,
+                                    unsigned long long* visits, void* stream)
+{
+    if (!visits) return fail(RA_ERR_INVALID_ARG, "visits is NULL");
+    return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, grad_dtype, workspace, workspace_bytes,
+                    Problem{B, H, Hkv, L, d, n_shards, causal, layout, dtype}, visits, stream);
 }
 
 ra_status ring_attn_device_status(unsigned int* status, void* stream)

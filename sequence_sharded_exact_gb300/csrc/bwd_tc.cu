@@ -91,6 +91,7 @@ struct BwdArgs {
     void* dv;
     int grad_bf16;
     unsigned int* status;
+    unsigned long long* visits;  // optional [n][n] tile-pair counter
     float scale, scale_log2;
 };
 
@@ -515,6 +516,7 @@ __device__ __forceinline__ void producer_role(const BwdArgs& a, uint32_t sbase, 
             for (int t = 0; t < u.ntiles; ++t, ++qc) {
                 int hh, qrow, qnat;
                 walk.next(hh, qrow, qnat);
+                if (a.visits) atomicAdd(a.visits + (long long)(qrow / a.geo.S) * a.geo.n + u.shard, 1ull);
                 const int stage = (int)(qc & 1);
                 const uint32_t use = qc >> 1;
                 if (use > 0 && !mbar_wait(bar(BAR_QD_EMPTY + stage), (use - 1) & 1, ctl)) { ok = false; break; }
@@ -740,7 +742,7 @@ bool tc_bwd_supported(const Problem& p)
 
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v, const void* dout,
                           const float* D, const float* lse, float* dq_acc, void* dk, void* dv, int grad_dtype,
-                          unsigned int* status, cudaStream_t s)
+                          unsigned int* status, cudaStream_t s, unsigned long long* visits)
 {
     CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_map(&tq, q, p.L, (long long)p.B * p.H) || !make_map(&tk, k, p.L, (long long)p.B * p.Hkv) ||
@@ -763,6 +765,7 @@ cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const 
     a.dv = dv;
     a.grad_bf16 = grad_dtype == 1;
     a.status = status;
+    a.visits = visits;
     a.scale = 1.0f / sqrtf((float)kHd);
     a.scale_log2 = a.scale * kLog2e;
     static bool attr_done[64];

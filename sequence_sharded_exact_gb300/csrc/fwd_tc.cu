@@ -88,6 +88,7 @@ struct FwdArgs {
     void* out;
     float* lse;
     unsigned int* status;
+    unsigned long long* visits;  // optional [n][n] tile-pair counter
     float scale_log2;
 };
 
@@ -402,6 +403,7 @@ __device__ __forceinline__ void producer_role(const FwdArgs& a, uint32_t sbase, 
             for (int jj = 0; jj < u.ntiles; ++jj, ++kc) {
                 int kv_row, kv_nat;
                 walk.next(kv_row, kv_nat);
+                if (a.visits) atomicAdd(a.visits + (long long)u.shard * a.geo.n + kv_row / a.geo.S, 1ull);
                 const int stage = (int)(kc % kStages);
                 const uint32_t use = kc / kStages;
                 // K and V stages are released separately: K once both S MMAs of its tile are done,
@@ -644,7 +646,8 @@ bool tc_fwd_supported(const Problem& p)
 }
 
 cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v, void* out,
-                          float* lse, int mode, int step, unsigned int* status, cudaStream_t s)
+                          float* lse, int mode, int step, unsigned int* status, cudaStream_t s,
+                          unsigned long long* visits)
 {
     CUtensorMap tq, tk, tv;
     if (!make_map(&tq, q, p.L, (long long)p.B * p.H) || !make_map(&tk, k, p.L, (long long)p.B * p.Hkv) ||
@@ -664,6 +667,7 @@ cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const 
     a.out = out;
     a.lse = lse;
     a.status = status;
+    a.visits = visits;
     a.scale_log2 = kLog2e / sqrtf((float)kHd);
 
     static bool attr_done[64];

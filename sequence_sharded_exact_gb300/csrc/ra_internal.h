@@ -35,14 +35,15 @@ cudaError_t launch_bwd_simt(const Problem& p, const void* q, const void* k, cons
 
 // Tensor-core kernels (TMA + tcgen05 + TMEM), bf16, d = 128, chunk length % 256 == 0.
 bool tc_fwd_supported(const Problem& p);
+// visits (optional, n x n): +1 at [query shard][key shard] for every tile pair computed.
 cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           void* out, float* lse, int mode, int step, unsigned int* status,
-                          cudaStream_t s);
+                          cudaStream_t s, unsigned long long* visits = nullptr);
 bool tc_bwd_supported(const Problem& p);
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v,
                           const void* dout, const float* D, const float* lse, float* dq_acc,
                           void* dk, void* dv, int grad_dtype, unsigned int* status,
-                          cudaStream_t s);
+                          cudaStream_t s, unsigned long long* visits = nullptr);
 
 // HBM-bound helper kernels.
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part,

@@ -110,3 +110,23 @@ def test_workspace_sizes(lib):
     assert binding.bwd_workspace_size(1, 32, 8, 65536, 128, torch.float32) >= 32 * 65536 * 4
     assert binding.bwd_workspace_size(1, 32, 8, 65536, 128, torch.bfloat16) >= 32 * 65536 * 129 * 4
     assert lib.ring_attn_fwd_stepwise_workspace_size(1, 2, 1024, 128) >= 2 * 2 * 1024 * 128 * 4
+
+
+def test_tile_visits_argument_errors(lib):
+    """The counted entry points refuse a NULL counter, and problems off the tensor-core path,
+    before any CUDA call."""
+    P = ctypes.c_void_p
+    ptrs = [P(256)] * 5
+    st = lib.ring_attn_fwd_tile_visits(*ptrs, 1, 2, 2, 1024, 128, 4, 1, 1, 1, None, None)
+    assert st == binding.RA_ERR_INVALID_ARG
+    # d = 64 takes the CUDA-core path, which does not count tiles
+    st = lib.ring_attn_fwd_tile_visits(*ptrs, 1, 2, 2, 1024, 64, 4, 1, 1, 1, P(256), None)
+    assert st == binding.RA_ERR_UNSUPPORTED
+    assert "tensor-core" in lib.ring_attn_last_error().decode()
+    bptrs = [P(256)] * 9
+    st = lib.ring_attn_bwd_tile_visits(*bptrs, 0, P(256), 1 << 20, 1, 2, 2, 600, 128, 3, 1, 1, 1,
+                                       P(256), None)
+    assert st == binding.RA_ERR_UNSUPPORTED
+    st = lib.ring_attn_bwd_tile_visits(*bptrs, 0, P(256), 1 << 20, 1, 2, 2, 1024, 128, 4, 1, 1, 1,
+                                       None, None)
+    assert st == binding.RA_ERR_INVALID_ARG
