@@ -58,10 +58,11 @@ def _load():
         lib.oracle_attn_bwd_dkv_rows.argtypes = bcommon + [Lg, P, P, P]
         lib.oracle_attn_bwd.argtypes = bcommon + [P, P, P]
         lib.oracle_shard_tiles.argtypes = [Lg, I, I, I, I, P]
+        lib.oracle_rope.argtypes = [P, Lg, Lg, I, I, I, ctypes.c_double, I, P]
         lib.oracle_num_threads.argtypes = []
         for f in ("oracle_attn_fwd_rows", "oracle_attn_fwd", "oracle_ring_fwd",
                   "oracle_attn_bwd_dq_rows", "oracle_attn_bwd_dkv_rows", "oracle_attn_bwd",
-                  "oracle_shard_tiles", "oracle_num_threads"):
+                  "oracle_shard_tiles", "oracle_rope", "oracle_num_threads"):
             getattr(lib, f).restype = I
         _lib = lib
         return lib
@@ -187,3 +188,14 @@ def shard_tiles(L, n, causal, layout, tile=128):
     _check(_load().oracle_shard_tiles(int(L), int(n), int(causal), _layout(layout), int(tile),
                                       _ptr(out)), "shard_tiles")
     return out
+
+
+def rope(x, n, layout, base=10000.0, inverse=False):
+    """Rotary position embedding of every row of x [..., L, d] by its natural position (float64)."""
+    x = _f32(x)
+    L, d = x.shape[-2], x.shape[-1]
+    nheads = int(np.prod(x.shape[:-2])) if x.ndim > 2 else 1
+    y = np.empty(x.shape, np.float64)
+    _check(_load().oracle_rope(_ptr(x), nheads, L, d, int(n), _layout(layout), float(base), int(bool(inverse)),
+                               _ptr(y)), "rope")
+    return y

@@ -33,6 +33,7 @@
  *    to rank+1 and receives from rank-1).
  *  - running max starts at -infinity (the page's -1e4 fails when all scores are below -1e4); a
  *    block in which a row sees no key leaves that row's state unchanged.
+ *  - rotary positions (oracle_rope): natural positions, RoFormer pair rotation (see there).
  *  - backward (absent from the pages): the plain derivative of the forward definition,
  *    P = exp(s - lse), D = <dO, O>, dS = P (dO.v - D), dQ = scale dS K, dK = scale dS^T Q,
  *    dV = P^T dO, with dK and dV summed over the query heads of a group.
@@ -447,6 +448,43 @@ int oracle_attn_bwd(const float* q, const float* k, const float* v, const float*
     }
     free(rows);
     return st;
+}
+
+/* Rotary position embedding with natural positions.  [CP-30] asks how position information must be
+ * treated once K/V blocks travel round the ring; reading C17: every row is rotated by the angle of
+ * its NATURAL position p (its place in the whole sequence, from the layout), never by its buffer
+ * row or its index inside a shard, so a K/V block carries its positions with it.  The rotation is
+ * the RoFormer one (not given by the pages, reading C18): for i in [0, d/2) with
+ * theta_i = base^(-2i/d), the pair (x[2i], x[2i+1]) turns by the angle p * theta_i:
+ *   y[2i]   = x[2i] cos(p theta_i) - x[2i+1] sin(p theta_i)
+ *   y[2i+1] = x[2i] sin(p theta_i) + x[2i+1] cos(p theta_i).
+ * inverse != 0 turns by -p * theta_i instead (the transposed rotation: what maps the gradient with
+ * respect to the rotated rows back to the unrotated ones).
+ * x and y are [nheads][L][d] (nheads = B * H); d even. */
+int oracle_rope(const float* x, long nheads, long L, int d, int n, int layout, double base, int inverse,
+                double* y)
+{
+    if (nheads < 1 || L < 1 || d < 2 || d % 2 != 0 || n < 1 || L % n != 0 || base <= 0.0)
+        return ORACLE_BAD_ARGS;
+    if (layout != 0 && layout != 1 && layout != 2) return ORACLE_BAD_ARGS;
+    if (layout == 1 && L % (2L * n) != 0) return ORACLE_BAD_ARGS;
+    const double sign = inverse ? -1.0 : 1.0;
+#pragma omp parallel for schedule(static)
+    for (long hr = 0; hr < nheads * L; ++hr) {
+        const long r = hr % L;
+        const double p = (double)oracle_natural_position(r, L, n, layout);
+        const float* xr = x + hr * d;
+        double* yr = y + hr * d;
+        for (int i = 0; i < d / 2; ++i) {
+            const double theta = pow(base, -2.0 * i / d);
+            const double ang = sign * p * theta;
+            const double c = cos(ang), sn = sin(ang);
+            const double x0 = xr[2 * i], x1 = xr[2 * i + 1];
+            yr[2 * i] = x0 * c - x1 * sn;
+            yr[2 * i + 1] = x0 * sn + x1 * c;
+        }
+    }
+    return ORACLE_OK;
 }
 
 /* Number of OpenMP threads the oracle runs on (1 without OpenMP). */

@@ -337,3 +337,107 @@ def test_synth_recipe():
     changed = (plain["k"] != spiked["k"]).any(dim=-1).sum().item()
     assert changed == 10
     assert a["q"].dtype == torch.bfloat16
+
+
+# ------------------------------------------------------------------------------------------------
+# Rotary positions (reading C17: natural positions follow the rows; C18: RoFormer pair rotation)
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("layout,n", [("contiguous", 4), ("zigzag", 4), ("striped", 4), ("zigzag", 1)])
+def test_rope_is_complex_multiplication_by_natural_position(layout, n):
+    """Pair (x0, x1) as the complex number x0 + i x1 is multiplied by exp(i p theta_j),
+    theta_j = base^(-2j/d), p = the row's natural position (numpy complex128 exponential)."""
+    L, d, base = 32, 8, 500.0
+    x = rand((2, 3, L, d), 201)
+    y = oracle.rope(x, n, layout, base=base)
+    pos = buffer_to_natural(L, n, layout)
+    theta = base ** (-np.arange(d // 2) * 2.0 / d)
+    z = x[..., 0::2].astype(np.float64) + 1j * x[..., 1::2].astype(np.float64)
+    rot = z * np.exp(1j * pos[:, None] * theta[None, :])
+    np.testing.assert_allclose(y[..., 0::2], rot.real, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(y[..., 1::2], rot.imag, rtol=0, atol=1e-12)
+
+
+def test_rope_identity_at_position_zero_and_norms():
+    L, d = 16, 16
+    x = rand((1, 2, L, d), 202)
+    y = oracle.rope(x, 2, "contiguous")
+    np.testing.assert_array_equal(y[:, :, 0], x[:, :, 0].astype(np.float64))  # p = 0: angle 0
+    pair = lambda a: a[..., 0::2] ** 2 + a[..., 1::2] ** 2
+    np.testing.assert_allclose(pair(y), pair(x.astype(np.float64)), rtol=1e-12, atol=1e-12)
+
+
+def test_rope_inverse_undoes_forward():
+    L, d = 24, 8
+    x = rand((1, 1, L, d), 203).astype(np.float64)
+    for layout, n in (("contiguous", 3), ("zigzag", 3), ("striped", 3)):
+        fwd = oracle.rope(x, n, layout)
+        # forward rotation of x (exact float32 input) then the inverse in float64 by the transpose
+        inv_of_x = oracle.rope(x, n, layout, inverse=True)
+        # <R x, R x'> = <x, x'> and R^T R = I: check via the bilinear identity on random pairs
+        xp = rand((1, 1, L, d), 204)
+        lhs = (fwd * oracle.rope(xp, n, layout)).sum(axis=-1)
+        np.testing.assert_allclose(lhs, (x * xp).sum(axis=-1), rtol=1e-12, atol=1e-12)
+        rhs = (inv_of_x * xp).sum(axis=-1)
+        np.testing.assert_allclose(rhs, (x * oracle.rope(xp, n, layout)).sum(axis=-1), rtol=1e-12, atol=1e-12)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    """<R(p) q, R(t) k> is unchanged when both positions move by the same shift s (the property
+    that lets K/V blocks travel with their positions)."""
+    L, d = 64, 16
+    q1, k1 = rand((d,), 205), rand((d,), 206)
+    base_pairs = [(5, 2), (9, 9), (20, 3)]
+    for shift in (1, 17, 40):
+        for p, t in base_pairs:
+            xq = np.zeros((1, 1, L, d), np.float32)
+            xk = np.zeros((1, 1, L, d), np.float32)
+            xq[0, 0, p], xk[0, 0, t] = q1, k1
+            s0 = float((oracle.rope(xq, 1, "contiguous")[0, 0, p] * oracle.rope(xk, 1, "contiguous")[0, 0, t]).sum())
+            xq2, xk2 = np.zeros_like(xq), np.zeros_like(xk)
+            xq2[0, 0, p + shift], xk2[0, 0, t + shift] = q1, k1
+            s1 = float((oracle.rope(xq2, 1, "contiguous")[0, 0, p + shift] *
+                        oracle.rope(xk2, 1, "contiguous")[0, 0, t + shift]).sum())
+            assert abs(s0 - s1) <= 1e-11 * max(1.0, abs(s0)), (shift, p, t, s0, s1)
+
+
+def test_rope_layout_equivariance():
+    """Rotating a sharded buffer equals rotating the natural-order sequence, then sharding."""
+    L, d = 32, 8
+    xn = rand((2, 2, L, d), 207)
+    yn = oracle.rope(xn, 1, "contiguous")
+    for layout, n in (("zigzag", 4), ("striped", 4), ("contiguous", 4)):
+        perm = buffer_to_natural(L, n, layout)
+        np.testing.assert_array_equal(oracle.rope(xn[:, :, perm], n, layout), yn[:, :, perm])
+
+
+def test_rope_attention_gradient_chain_matches_autograd():
+    """d/dq of sum(attn(R q, R k, v) * dout) = R^T (attention's dQ at the rotated inputs), and the
+    same for k: the oracle's chain (attention backward at the rotated inputs, then the inverse
+    rotation) against torch float64 autograd through a rotation written as a complex product and
+    scaled_dot_product_attention, in natural order."""
+    B, H, Hkv, L, d, n = 1, 4, 2, 32, 8, 4
+    causal, layout, base = True, "zigzag", 100.0
+    q, k, v, do = (rand(s, i) for i, s in enumerate(
+        [(B, H, L, d), (B, Hkv, L, d), (B, Hkv, L, d), (B, H, L, d)], start=211))
+    qr = oracle.rope(q, n, layout, base=base).astype(np.float32)
+    kr = oracle.rope(k, n, layout, base=base).astype(np.float32)
+    dq_r, dk_r, _ = oracle.attn_bwd(qr, kr, v, do, n, causal, layout)
+    dq = oracle.rope(dq_r, n, layout, base=base, inverse=True)
+    dk = oracle.rope(dk_r, n, layout, base=base, inverse=True)
+
+    perm = buffer_to_natural(L, n, layout)
+    inv = np.argsort(perm)
+    nat = lambda a: torch.from_numpy(a[:, :, inv].astype(np.float64))
+    tq, tk, tv, tdo = nat(q).requires_grad_(True), nat(k).requires_grad_(True), nat(v), nat(do)
+    theta = torch.tensor(base ** (-np.arange(d // 2) * 2.0 / d), dtype=torch.float64)
+    rot = torch.polar(torch.ones(L, d // 2, dtype=torch.float64), torch.arange(L, dtype=torch.float64)[:, None] * theta)
+
+    def rotate(x):
+        xc = torch.view_as_complex(x.reshape(*x.shape[:-1], d // 2, 2).contiguous())
+        return torch.view_as_real(xc * rot).reshape(x.shape)
+
+    out = torch.nn.functional.scaled_dot_product_attention(rotate(tq), rotate(tk), tv, is_causal=True,
+                                                           enable_gqa=True)
+    out.backward(tdo)
+    np.testing.assert_allclose(dq[:, :, inv], tq.grad.numpy(), rtol=0, atol=2e-6)
+    np.testing.assert_allclose(dk[:, :, inv], tk.grad.numpy(), rtol=0, atol=2e-6)
