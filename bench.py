@@ -439,6 +439,14 @@ def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
     res["lse_merge"] = {"GB/s": gbytes / (statistics.mean(ms) / 1e3), "peak_GB/s": hbm,
                         "frac": gbytes / (statistics.mean(ms) / 1e3) / hbm, "ms": statistics.mean(ms)}
     del ws, out2, lse2, part, la, lb, o_acc
+    # rotary positions on a copy of the workload's q, in place; bytes = read + write of q per launch
+    qr = x["q"].clone()
+    qb = qr.numel() * qr.element_size()
+    ms = time_launches(lambda: ra.rope(qr, n, w["layout"], stream=stream), 5, 2, stream)
+    per = statistics.mean(ms)
+    res["rope_q"] = {"GB/s": 2 * qb / 1e9 / (per / 1e3), "peak_GB/s": hbm,
+                     "frac": 2 * qb / 1e9 / (per / 1e3) / hbm, "ms": per}
+    del qr
     # training workload: forward + backward
     t = synth.WORKLOADS[TRAIN_WORKLOAD]
     xt = synth.make_workload(TRAIN_WORKLOAD, device=dev, gen_device=dev)

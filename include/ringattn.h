@@ -200,6 +200,24 @@ RA_API ra_status ring_attn_bwd_tile_visits(const void* q, const void* k, const v
                                            int layout, int dtype, unsigned long long* visits,
                                            void* stream);
 
+/*
+ * ring_attn_rope -- rotary position embedding, in place, of a [B][H][L][d] buffer stored in the
+ * layout's order (q with its H query heads, or k with its Hkv heads; pass that head count as H).
+ * LLM-101-CN "distributed hands-on code", section 6 (the questions after 6.2), asks how positions
+ * must be handled when K/V blocks travel round the ring: here row r turns by the angle of its
+ * NATURAL position p(r) (its place in the whole sequence, from the layout -- never its buffer row or
+ * shard-local index), so the blocks carry their positions with them.  Rotation (RoFormer): for
+ * i in [0, d/2), theta_i = base^(-2i/d), the pair (x[2i], x[2i+1]) turns by p * theta_i:
+ *   x'[2i] = x[2i] cos - x[2i+1] sin,   x'[2i+1] = x[2i] sin + x[2i+1] cos.
+ *   x: DEVICE pointer, dtype RA_BF16 or RA_F32, 16-byte aligned, overwritten.
+ *   base > 0 and finite (10000 is the usual value).
+ *   inverse != 0 turns by -p * theta_i: applied to dq and dk from ring_attn_bwd (computed with the
+ *   rotated q and k) it gives the gradients with respect to the unrotated q and k.
+ *   L % n_shards == 0 (zigzag: L % 2n == 0); d in {64, 128}.  Stream-ordered, no host sync.
+ */
+RA_API ra_status ring_attn_rope(void* x, int B, int H, int L, int d, int n_shards, int layout, int dtype,
+                                double base, int inverse, void* stream);
+
 /* Which kernel path ring_attn_fwd / ring_attn_bwd take for these arguments (RA_PATH_*), written
  * to *path (HOST pointer).  Same argument checks as the calls themselves; no CUDA call. */
 RA_API ra_status ring_attn_fwd_path(int B, int H, int Hkv, int L, int d, int n_shards, int causal,

@@ -450,8 +450,8 @@ int oracle_attn_bwd(const float* q, const float* k, const float* v, const float*
     return st;
 }
 
-/* Rotary position embedding with natural positions.  [CP-30] asks how position information must be
- * treated once K/V blocks travel round the ring; reading C17: every row is rotated by the angle of
+/* Rotary position embedding with natural positions.  [LLM101] section 6 (the questions after 6.2)
+ * asks how position information must be treated once K/V blocks travel round the ring; reading C17: every row is rotated by the angle of
  * its NATURAL position p (its place in the whole sequence, from the layout), never by its buffer
  * row or its index inside a shard, so a K/V block carries its positions with it.  The rotation is
  * the RoFormer one (not given by the pages, reading C18): for i in [0, d/2) with

@@ -19,5 +19,6 @@ from .binding import (  # noqa: F401
     library,
     lse_merge,
     ring_step_fwd,
+    rope,
     shard_tiles,
 )

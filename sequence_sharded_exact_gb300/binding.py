@@ -29,6 +29,7 @@ EXPORTS = (
     "ring_attn_shard_tiles", "ring_attn_fwd_path", "ring_attn_bwd_path", "ring_attn_device_status",
     "ring_attn_last_error", "ring_attn_abi_version", "ring_attn_bwd_static_scratch",
     "ring_attn_bwd_static_scratch_capacity", "ring_attn_fwd_tile_visits", "ring_attn_bwd_tile_visits",
+    "ring_attn_rope",
 )
 
 
@@ -76,6 +77,8 @@ def library():
         lib.ring_attn_bwd_tile_visits.argtypes = [P, P, P, P, P, P, P, P, P, I, P, SZ, I, I, I, I, I,
                                                   I, I, I, I, P, P]
         lib.ring_attn_bwd_tile_visits.restype = ctypes.c_int
+        lib.ring_attn_rope.argtypes = [P, I, I, I, I, I, I, I, ctypes.c_double, I, P]
+        lib.ring_attn_rope.restype = ctypes.c_int
         lib.ring_attn_bwd_static_scratch_capacity.argtypes = []
         lib.ring_attn_bwd_static_scratch_capacity.restype = SZ
         for name in EXPORTS:
@@ -302,6 +305,19 @@ def shard_tiles(L, n_shards, causal=True, layout="zigzag", tile=128):
     _check(library().ring_attn_shard_tiles(int(L), int(n_shards), int(causal), _layout(layout),
                                            int(tile), arr))
     return [int(x) for x in arr]
+
+
+def rope(x, n_shards, layout="zigzag", base=10000.0, inverse=False, stream=None):
+    """ring_attn_rope: rotary position embedding of x [B, H, L, d] (bf16 or float32) in place, each row
+    by its natural position under the layout; inverse=True turns the other way (for gradients).
+    Returns x."""
+    if x.dim() != 4:
+        raise ValueError("x must be [B, H, L, d]")
+    _need(x, "x", x.device)
+    B, H, L, d = (int(s) for s in x.shape)
+    _check(library().ring_attn_rope(_ptr(x), B, H, L, d, int(n_shards), _layout(layout), _dtype_code(x.dtype),
+                                    float(base), int(bool(inverse)), _stream(stream, x.device)))
+    return x
 
 
 def device_status(stream=None, device=None):

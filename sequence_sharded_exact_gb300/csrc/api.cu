@@ -382,6 +382,20 @@ ra_status ring_attn_bwd_tile_visits(const void* q, const void* k, const void* v,
                     Problem{B, H, Hkv, L, d, n_shards, causal, layout, dtype}, visits, stream);
 }
 
+ra_status ring_attn_rope(void* x, int B, int H, int L, int d, int n_shards, int layout, int dtype,
+                         double base, int inverse, void* stream)
+{
+    Problem p{B, H, H, L, d, n_shards, 0, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if (!(base > 0.0) || !isfinite(base)) return fail(RA_ERR_INVALID_ARG, "base must be positive and finite");
+    if ((st = check_ptrs({x})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaError_t e = launch_rope(p, x, base, inverse, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_rope launch");
+    return RA_OK;
+}
+
 ra_status ring_attn_device_status(unsigned int* status, void* stream)
 {
     if (!status) return fail(RA_ERR_INVALID_ARG, "status is NULL");

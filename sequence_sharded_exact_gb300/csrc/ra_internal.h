@@ -46,6 +46,8 @@ cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const 
                           cudaStream_t s, unsigned long long* visits = nullptr);
 
 // HBM-bound helper kernels.
+// Rotary position embedding by natural position, in place, of a [B][H][L][d] buffer (p.H heads).
+cudaError_t launch_rope(const Problem& p, void* x, double base, int inverse, cudaStream_t s);
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part,
                              const float* lse_part, long long rows, int d, cudaStream_t s);
 cudaError_t launch_convert(const float* src, void* dst, int dst_dtype, long long count,

@@ -130,3 +130,13 @@ def test_tile_visits_argument_errors(lib):
     st = lib.ring_attn_bwd_tile_visits(*bptrs, 0, P(256), 1 << 20, 1, 2, 2, 1024, 128, 4, 1, 1, 1,
                                        None, None)
     assert st == binding.RA_ERR_INVALID_ARG
+
+
+def test_rope_argument_errors(lib):
+    P = ctypes.c_void_p
+    # base must be positive and finite; d in {64, 128}; x not NULL -- all before any CUDA call
+    assert lib.ring_attn_rope(P(256), 1, 2, 1024, 128, 4, 1, 1, 0.0, 0, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_rope(P(256), 1, 2, 1024, 128, 4, 1, 1, float("inf"), 0, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_rope(P(256), 1, 2, 1024, 96, 4, 1, 1, 10000.0, 0, None) == binding.RA_ERR_UNSUPPORTED
+    assert lib.ring_attn_rope(None, 1, 2, 1024, 128, 4, 1, 1, 10000.0, 0, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_rope(P(256), 1, 2, 1020, 128, 4, 1, 1, 10000.0, 0, None) == binding.RA_ERR_INVALID_ARG
