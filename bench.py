@@ -447,6 +447,25 @@ def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
     res["rope_q"] = {"GB/s": 2 * qb / 1e9 / (per / 1e3), "peak_GB/s": hbm,
                      "frac": 2 * qb / 1e9 / (per / 1e3) / hbm, "ms": per}
     del qr
+    # Ulysses variant on the same workload: token split in, three all-to-alls, attention per shard
+    # over the whole sequence, two all-to-alls back (Hkv must divide by n)
+    if H % n == 0 and Hkv % n == 0 and w["d"] in (64, 128):
+        S = L // n
+        tok = lambda t: t.view(B, t.shape[1], n, S, d).permute(2, 0, 3, 1, 4).contiguous()
+        qt, kt, vt = tok(x["q"]), tok(x["k"]), tok(x["v"])
+        ot = torch.empty_like(qt)
+        lt_ = torch.empty((n, B, S, H), dtype=torch.float32, device=dev)
+        wsu = torch.empty(ra.library().ring_attn_ulysses_workspace_size(B, H, Hkv, L, d, 1), dtype=torch.uint8,
+                          device=dev)
+        ms = time_launches(lambda: ra.ulysses_fwd(qt, kt, vt, n, w["causal"], w["layout"], out=ot, lse=lt_,
+                                                  workspace=wsu, stream=stream), 3, 1, stream)
+        hs = torch.empty(n, B, H // n, L, d, dtype=qt.dtype, device=dev)
+        ams = time_launches(lambda: ra.ulysses_a2a(qt, n, w["layout"], 0, dst=hs, stream=stream), 5, 2, stream)
+        qbytes = qt.numel() * qt.element_size()
+        res["ulysses_fwd"] = {"tflops": flops / (statistics.mean(ms) / 1e3) / 1e12, "ms": statistics.mean(ms),
+                              "a2a_q_GB/s": 2 * qbytes / 1e9 / (statistics.mean(ams) / 1e3),
+                              "a2a_q_ms": statistics.mean(ams)}
+        del qt, kt, vt, ot, lt_, wsu, hs
     # training workload: forward + backward
     t = synth.WORKLOADS[TRAIN_WORKLOAD]
     xt = synth.make_workload(TRAIN_WORKLOAD, device=dev, gen_device=dev)

@@ -218,6 +218,32 @@ RA_API ra_status ring_attn_bwd_tile_visits(const void* q, const void* k, const v
 RA_API ra_status ring_attn_rope(void* x, int B, int H, int L, int d, int n_shards, int layout, int dtype,
                                 double base, int inverse, void* stream);
 
+/*
+ * DeepSpeed-Ulysses, the other context-parallel design ("Lecture 30: TP/PP/SP/CP", sections 3.3 and
+ * 3.4).  Shard i of n holds all heads of its S = L / n tokens; an all-to-all turns that into H / n
+ * heads of the whole sequence, each shard runs ordinary attention over the full sequence for its
+ * heads, and a second all-to-all brings the output back.  Heads must divide by n: H % n_shards == 0
+ * and Hkv % n_shards == 0, else RA_ERR_INVALID_ARG (checked before anything runs).  On one GPU the
+ * shards are slices of one allocation and the all-to-alls are row permutations.
+ *   Token split (inputs and outputs):  q, out [n][B][S][H][d], k, v [n][B][S][Hkv][d],
+ *   lse [n][B][S][H] float32; local token s of shard i is natural position p(i * S + s) under the
+ *   layout, as for the ring (contiguous, zigzag or striped).
+ *   Head split (inside):  [n][B][H/n][L][d], natural token order, heads h -> shard h / (H/n).
+ *
+ * ring_attn_ulysses_a2a -- one all-to-all: direction 0 token split -> head split, 1 the reverse.
+ *   src, dst: DEVICE, distinct, 16-byte aligned; rows of d elements of dtype (d * size a multiple
+ *   of 4 bytes; pass d = 1 with RA_F32 for an lse-shaped tensor); H is that tensor's head count.
+ * ring_attn_ulysses_fwd -- the whole forward: three all-to-alls in, attention on every shard, two
+ *   back.  Same results as ring_attn_fwd (exact attention), in the token split.
+ *   workspace: DEVICE, 256-byte aligned, at least ring_attn_ulysses_workspace_size(...) bytes.
+ */
+RA_API ra_status ring_attn_ulysses_a2a(const void* src, void* dst, int B, int H, int L, int d, int n_shards,
+                                       int layout, int dtype, int direction, void* stream);
+RA_API ra_status ring_attn_ulysses_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                                       int B, int H, int Hkv, int L, int d, int n_shards, int causal, int layout,
+                                       int dtype, void* workspace, size_t workspace_bytes, void* stream);
+RA_API size_t ring_attn_ulysses_workspace_size(int B, int H, int Hkv, int L, int d, int dtype);
+
 /* Which kernel path ring_attn_fwd / ring_attn_bwd take for these arguments (RA_PATH_*), written
  * to *path (HOST pointer).  Same argument checks as the calls themselves; no CUDA call. */
 RA_API ra_status ring_attn_fwd_path(int B, int H, int Hkv, int L, int d, int n_shards, int causal,

@@ -21,4 +21,6 @@ from .binding import (  # noqa: F401
     ring_step_fwd,
     rope,
     shard_tiles,
+    ulysses_a2a,
+    ulysses_fwd,
 )

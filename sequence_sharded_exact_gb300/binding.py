@@ -29,7 +29,7 @@ EXPORTS = (
     "ring_attn_shard_tiles", "ring_attn_fwd_path", "ring_attn_bwd_path", "ring_attn_device_status",
     "ring_attn_last_error", "ring_attn_abi_version", "ring_attn_bwd_static_scratch",
     "ring_attn_bwd_static_scratch_capacity", "ring_attn_fwd_tile_visits", "ring_attn_bwd_tile_visits",
-    "ring_attn_rope",
+    "ring_attn_rope", "ring_attn_ulysses_a2a", "ring_attn_ulysses_fwd", "ring_attn_ulysses_workspace_size",
 )
 
 
@@ -79,6 +79,12 @@ def library():
         lib.ring_attn_bwd_tile_visits.restype = ctypes.c_int
         lib.ring_attn_rope.argtypes = [P, I, I, I, I, I, I, I, ctypes.c_double, I, P]
         lib.ring_attn_rope.restype = ctypes.c_int
+        lib.ring_attn_ulysses_a2a.argtypes = [P, P, I, I, I, I, I, I, I, I, P]
+        lib.ring_attn_ulysses_a2a.restype = ctypes.c_int
+        lib.ring_attn_ulysses_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P]
+        lib.ring_attn_ulysses_fwd.restype = ctypes.c_int
+        lib.ring_attn_ulysses_workspace_size.argtypes = [I, I, I, I, I, I]
+        lib.ring_attn_ulysses_workspace_size.restype = SZ
         lib.ring_attn_bwd_static_scratch_capacity.argtypes = []
         lib.ring_attn_bwd_static_scratch_capacity.restype = SZ
         for name in EXPORTS:
@@ -318,6 +324,63 @@ def rope(x, n_shards, layout="zigzag", base=10000.0, inverse=False, stream=None)
     _check(library().ring_attn_rope(_ptr(x), B, H, L, d, int(n_shards), _layout(layout), _dtype_code(x.dtype),
                                     float(base), int(bool(inverse)), _stream(stream, x.device)))
     return x
+
+
+def ulysses_a2a(src, n_shards, layout="contiguous", direction=0, dst=None, stream=None):
+    """ring_attn_ulysses_a2a.  direction 0: src [n, B, S, H, d] (token split) -> [n, B, H/n, L, d]
+    (head split); direction 1 the reverse.  A 4-D src [n, B, S, H] (lse) moves rows of one float."""
+    _need(src, "src", src.device)
+    if direction == 0:
+        if src.dim() == 5:
+            n, B, S, H, d = (int(s) for s in src.shape)
+            shape = (n, B, H // n, n * S, d)
+        else:
+            n, B, S, H = (int(s) for s in src.shape)
+            d = 1
+            shape = (n, B, H // n, n * S)
+    else:
+        if src.dim() == 5:
+            n, B, Hn, L, d = (int(s) for s in src.shape)
+            S, H = L // n, Hn * n
+            shape = (n, B, S, H, d)
+        else:
+            n, B, Hn, L = (int(s) for s in src.shape)
+            S, H, d = L // n, Hn * n, 1
+            shape = (n, B, S, H)
+    if n != n_shards:
+        raise ValueError("the leading dimension of src must be n_shards")
+    if dst is None:
+        dst = torch.empty(shape, dtype=src.dtype, device=src.device)
+    _need(dst, "dst", src.device)
+    _check(library().ring_attn_ulysses_a2a(_ptr(src), _ptr(dst), B, H, n * S, d, n, _layout(layout),
+                                           _dtype_code(src.dtype), int(direction), _stream(stream, src.device)))
+    return dst
+
+
+def ulysses_fwd(q, k, v, n_shards, causal=True, layout="contiguous", out=None, lse=None, workspace=None,
+                stream=None):
+    """ring_attn_ulysses_fwd: q [n, B, S, H, d], k and v [n, B, S, Hkv, d] (token split).  Returns
+    (out [n, B, S, H, d], lse [n, B, S, H] float32)."""
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, nm, q.device)
+        if t.dim() != 5:
+            raise ValueError(f"{nm} must be [n, B, S, heads, d]")
+    n, B, S, H, d = (int(s) for s in q.shape)
+    Hkv = int(k.shape[3])
+    L = n * S
+    if n != n_shards:
+        raise ValueError("the leading dimension of q must be n_shards")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((n, B, S, H), dtype=torch.float32, device=q.device)
+    need = int(library().ring_attn_ulysses_workspace_size(B, H, Hkv, L, d, _dtype_code(q.dtype)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(library().ring_attn_ulysses_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, L, d, n,
+                                           int(causal), _layout(layout), _dtype_code(q.dtype), _ptr(workspace),
+                                           workspace.numel(), _stream(stream, q.device)))
+    return out, lse
 
 
 def device_status(stream=None, device=None):

@@ -396,6 +396,101 @@ ra_status ring_attn_rope(void* x, int B, int H, int L, int d, int n_shards, int 
     return RA_OK;
 }
 
+namespace {
+
+ra_status check_ulysses_heads(const Problem& p)
+{
+    if (p.H % p.n != 0 || p.Hkv % p.n != 0)
+        return fail(RA_ERR_INVALID_ARG,
+                    "Ulysses splits heads across the shards: H (%d) and Hkv (%d) must be multiples of n_shards (%d)",
+                    p.H, p.Hkv, p.n);
+    return RA_OK;
+}
+
+size_t elem_size(int dtype) { return dtype == RA_F32 ? 4 : 2; }
+
+}  // namespace
+
+ra_status ring_attn_ulysses_a2a(const void* src, void* dst, int B, int H, int L, int d, int n_shards, int layout,
+                                int dtype, int direction, void* stream)
+{
+    Problem p{B, H, H, L, 64, n_shards, 0, layout, dtype};  // d checked below: any row length
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if (d < 1 || (long long)d * elem_size(dtype) % 4 != 0)
+        return fail(RA_ERR_INVALID_ARG, "row of %d elements is not a whole number of 4-byte words", d);
+    if ((long long)B * H * L * d * (long long)elem_size(dtype) / 4 >= (1LL << 32))
+        return fail(RA_ERR_UNSUPPORTED, "tensor of 2^34 bytes or more");
+    if (direction != 0 && direction != 1) return fail(RA_ERR_INVALID_ARG, "direction must be 0 or 1");
+    if ((st = check_ulysses_heads(p)) != RA_OK) return st;
+    if ((st = check_ptrs({src, dst})) != RA_OK) return st;
+    if (src == dst) return fail(RA_ERR_INVALID_ARG, "src and dst must not be the same buffer");
+    if ((st = check_device()) != RA_OK) return st;
+    cudaError_t e = launch_ulysses_a2a(p.geo(), B, H, (int)(d * elem_size(dtype)), src, dst, direction,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_ulysses_a2a launch");
+    return RA_OK;
+}
+
+size_t ring_attn_ulysses_workspace_size(int B, int H, int Hkv, int L, int d, int dtype)
+{
+    if (B < 1 || H < 1 || Hkv < 1 || L < 1 || d < 1) return 0;
+    const size_t e = elem_size(dtype);
+    const size_t qrows = (size_t)B * H * L, kvrows = (size_t)B * Hkv * L;
+    // head-split q, k, v, out, lse
+    return 2 * align256(qrows * d * e) + 2 * align256(kvrows * d * e) + align256(qrows * sizeof(float));
+}
+
+ra_status ring_attn_ulysses_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+                                int Hkv, int L, int d, int n_shards, int causal, int layout, int dtype,
+                                void* workspace, size_t workspace_bytes, void* stream)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if ((st = check_ulysses_heads(p)) != RA_OK) return st;
+    if ((long long)B * H * L * d * (long long)elem_size(dtype) / 4 >= (1LL << 32))
+        return fail(RA_ERR_UNSUPPORTED, "tensor of 2^34 bytes or more");
+    if ((st = check_ptrs({q, k, v, out, lse, workspace})) != RA_OK) return st;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const size_t need = ring_attn_ulysses_workspace_size(B, H, Hkv, L, d, dtype);
+    if (workspace_bytes < need)
+        return fail(RA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    if ((st = check_device()) != RA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t e = elem_size(dtype);
+    const size_t qrows = (size_t)B * H * L, kvrows = (size_t)B * Hkv * L;
+    char* ws = static_cast<char*>(workspace);
+    void* qh = ws;
+    void* kh = ws + align256(qrows * d * e);
+    void* vh = static_cast<char*>(kh) + align256(kvrows * d * e);
+    void* oh = static_cast<char*>(vh) + align256(kvrows * d * e);
+    float* lh = reinterpret_cast<float*>(static_cast<char*>(oh) + align256(qrows * d * e));
+    const Geometry geo = p.geo();
+    const int row = (int)(d * e);
+    // first all-to-all: token split -> head split
+    cudaError_t err = launch_ulysses_a2a(geo, B, H, row, q, qh, 0, s);
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, Hkv, row, k, kh, 0, s);
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, Hkv, row, v, vh, 0, s);
+    // each rank: ordinary attention over the whole sequence (natural order) for its H / n heads, all
+    // ranks in one launch as a batch of n * B problems
+    if (err == cudaSuccess) {
+        const Problem pr{n_shards * B, H / n_shards, Hkv / n_shards, L, d, 1, causal, RA_LAYOUT_CONTIGUOUS, dtype};
+        if (tc_fwd_supported(pr)) {
+            unsigned int* sw = status_word(&err);
+            if (sw) err = launch_fwd_tc(pr, qh, kh, vh, oh, lh, kFwdFused, 0, sw, s);
+        } else {
+            err = launch_fwd_simt(pr, qh, kh, vh, oh, lh, kFwdFused, 0, s);
+        }
+    }
+    // second all-to-all: head split -> token split, for out and lse
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, H, row, oh, out, 1, s);
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, H, 4, lh, lse, 1, s);
+    if (err != cudaSuccess) return cuda_fail(err, "ring_attn_ulysses_fwd launch");
+    return RA_OK;
+}
+
 ra_status ring_attn_device_status(unsigned int* status, void* stream)
 {
     if (!status) return fail(RA_ERR_INVALID_ARG, "status is NULL");

@@ -48,6 +48,10 @@ cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const 
 // HBM-bound helper kernels.
 // Rotary position embedding by natural position, in place, of a [B][H][L][d] buffer (p.H heads).
 cudaError_t launch_rope(const Problem& p, void* x, double base, int inverse, cudaStream_t s);
+// Ulysses all-to-all re-layout between the token split [n][B][S][H][row] and the head split
+// [n][B][H/n][L][row] (direction 0 token -> head, 1 back); row_bytes a multiple of 4.
+cudaError_t launch_ulysses_a2a(const Geometry& geo, int B, int H, int row_bytes, const void* src, void* dst,
+                               int direction, cudaStream_t s);
 cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part,
                              const float* lse_part, long long rows, int d, cudaStream_t s);
 cudaError_t launch_convert(const float* src, void* dst, int dst_dtype, long long count,

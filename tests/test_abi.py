@@ -140,3 +140,21 @@ def test_rope_argument_errors(lib):
     assert lib.ring_attn_rope(P(256), 1, 2, 1024, 96, 4, 1, 1, 10000.0, 0, None) == binding.RA_ERR_UNSUPPORTED
     assert lib.ring_attn_rope(None, 1, 2, 1024, 128, 4, 1, 1, 10000.0, 0, None) == binding.RA_ERR_INVALID_ARG
     assert lib.ring_attn_rope(P(256), 1, 2, 1020, 128, 4, 1, 1, 10000.0, 0, None) == binding.RA_ERR_INVALID_ARG
+
+
+def test_ulysses_head_divisibility_and_workspace(lib):
+    """Ulysses splits the heads across the shards: H and Hkv must divide by n (checked before any
+    CUDA call).  The workspace holds the head-split q, k, v, out and lse."""
+    P = ctypes.c_void_p
+    ptrs = [P(256)] * 5
+    st = lib.ring_attn_ulysses_fwd(*ptrs, 1, 12, 4, 1024, 128, 8, 1, 0, 1, P(256), 1 << 30, None)
+    assert st == binding.RA_ERR_INVALID_ARG and "multiples of n_shards" in lib.ring_attn_last_error().decode()
+    st = lib.ring_attn_ulysses_fwd(*ptrs, 1, 16, 4, 1024, 128, 8, 1, 0, 1, P(256), 1 << 30, None)
+    assert st == binding.RA_ERR_INVALID_ARG  # Hkv = 4 < 8 shards
+    st = lib.ring_attn_ulysses_a2a(P(256), P(512), 1, 6, 1024, 128, 4, 0, 1, 0, None)
+    assert st == binding.RA_ERR_INVALID_ARG
+    st = lib.ring_attn_ulysses_a2a(P(256), P(512), 1, 8, 1024, 3, 4, 0, 1, 0, None)
+    assert st == binding.RA_ERR_INVALID_ARG  # 3 bf16 = 6 bytes per row
+    B, H, Hkv, L, d = 1, 32, 8, 131072, 128
+    want = 2 * B * H * L * d * 2 + 2 * B * Hkv * L * d * 2 + B * H * L * 4
+    assert binding.library().ring_attn_ulysses_workspace_size(B, H, Hkv, L, d, 1) == want
