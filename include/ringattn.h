@@ -243,6 +243,20 @@ RA_API ra_status ring_attn_ulysses_fwd(const void* q, const void* k, const void*
                                        int B, int H, int Hkv, int L, int d, int n_shards, int causal, int layout,
                                        int dtype, void* workspace, size_t workspace_bytes, void* stream);
 RA_API size_t ring_attn_ulysses_workspace_size(int B, int H, int Hkv, int L, int d, int dtype);
+/*
+ * ring_attn_ulysses_bwd -- the backward of ring_attn_ulysses_fwd: all-to-alls of q, k, v, out,
+ *   dout and lse into the head split, the backward of ring_attn_bwd on every shard over the whole
+ *   sequence, and all-to-alls of dq, dk, dv back.  All tensors in the token split (lse as returned
+ *   by ring_attn_ulysses_fwd); dq [n][B][S][H][d], dk, dv [n][B][S][Hkv][d] in grad_dtype.
+ *   workspace: DEVICE, 256-byte aligned, at least ring_attn_ulysses_bwd_workspace_size(...) bytes.
+ */
+RA_API ra_status ring_attn_ulysses_bwd(const void* q, const void* k, const void* v, const void* out,
+                                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                       int grad_dtype, void* workspace, size_t workspace_bytes, int B, int H,
+                                       int Hkv, int L, int d, int n_shards, int causal, int layout, int dtype,
+                                       void* stream);
+RA_API size_t ring_attn_ulysses_bwd_workspace_size(int B, int H, int Hkv, int L, int d, int n_shards, int dtype,
+                                                   int grad_dtype);
 
 /* Which kernel path ring_attn_fwd / ring_attn_bwd take for these arguments (RA_PATH_*), written
  * to *path (HOST pointer).  Same argument checks as the calls themselves; no CUDA call. */

@@ -22,5 +22,6 @@ from .binding import (  # noqa: F401
     rope,
     shard_tiles,
     ulysses_a2a,
+    ulysses_bwd,
     ulysses_fwd,
 )

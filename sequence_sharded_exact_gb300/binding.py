@@ -30,6 +30,7 @@ EXPORTS = (
     "ring_attn_last_error", "ring_attn_abi_version", "ring_attn_bwd_static_scratch",
     "ring_attn_bwd_static_scratch_capacity", "ring_attn_fwd_tile_visits", "ring_attn_bwd_tile_visits",
     "ring_attn_rope", "ring_attn_ulysses_a2a", "ring_attn_ulysses_fwd", "ring_attn_ulysses_workspace_size",
+    "ring_attn_ulysses_bwd", "ring_attn_ulysses_bwd_workspace_size",
 )
 
 
@@ -85,6 +86,10 @@ def library():
         lib.ring_attn_ulysses_fwd.restype = ctypes.c_int
         lib.ring_attn_ulysses_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.ring_attn_ulysses_workspace_size.restype = SZ
+        lib.ring_attn_ulysses_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, P, SZ, I, I, I, I, I, I, I, I, I, P]
+        lib.ring_attn_ulysses_bwd.restype = ctypes.c_int
+        lib.ring_attn_ulysses_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+        lib.ring_attn_ulysses_bwd_workspace_size.restype = SZ
         lib.ring_attn_bwd_static_scratch_capacity.argtypes = []
         lib.ring_attn_bwd_static_scratch_capacity.restype = SZ
         for name in EXPORTS:
@@ -381,6 +386,29 @@ def ulysses_fwd(q, k, v, n_shards, causal=True, layout="contiguous", out=None, l
                                            int(causal), _layout(layout), _dtype_code(q.dtype), _ptr(workspace),
                                            workspace.numel(), _stream(stream, q.device)))
     return out, lse
+
+
+def ulysses_bwd(q, k, v, out, lse, dout, n_shards, causal=True, layout="contiguous", grad_dtype=torch.float32,
+                workspace=None, stream=None):
+    """ring_attn_ulysses_bwd: token-split inputs as for ulysses_fwd (plus out, lse from it and dout
+    [n, B, S, H, d]).  Returns (dq, dk, dv) in the token split, grad_dtype."""
+    n, B, S, H, d = (int(s) for s in q.shape)
+    Hkv = int(k.shape[3])
+    L = n * S
+    dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
+    dk = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+    dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
+    need = int(library().ring_attn_ulysses_bwd_workspace_size(B, H, Hkv, L, d, n, _dtype_code(q.dtype),
+                                                              _dtype_code(grad_dtype)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"), (dout, "dout")):
+        _need(t, nm, q.device)
+    _check(library().ring_attn_ulysses_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                           _ptr(dk), _ptr(dv), _dtype_code(grad_dtype), _ptr(workspace),
+                                           workspace.numel(), B, H, Hkv, L, d, n, int(causal), _layout(layout),
+                                           _dtype_code(q.dtype), _stream(stream, q.device)))
+    return dq, dk, dv
 
 
 def device_status(stream=None, device=None):

@@ -491,6 +491,75 @@ ra_status ring_attn_ulysses_fwd(const void* q, const void* k, const void* v, voi
     return RA_OK;
 }
 
+size_t ring_attn_ulysses_bwd_workspace_size(int B, int H, int Hkv, int L, int d, int n_shards, int dtype,
+                                            int grad_dtype)
+{
+    if (B < 1 || H < 1 || Hkv < 1 || L < 1 || d < 1 || n_shards < 1 || H % n_shards || Hkv % n_shards) return 0;
+    const size_t e = elem_size(dtype), ge = elem_size(grad_dtype);
+    const size_t qrows = (size_t)B * H * L, kvrows = (size_t)B * Hkv * L;
+    // head-split q, out, dout, k, v, lse, dq, dk, dv, then the per-shard backward's own workspace
+    return 3 * align256(qrows * d * e) + 2 * align256(kvrows * d * e) + align256(qrows * sizeof(float)) +
+           align256(qrows * d * ge) + 2 * align256(kvrows * d * ge) +
+           align256(ring_attn_bwd_workspace_size(n_shards * B, H / n_shards, Hkv / n_shards, L, d, grad_dtype));
+}
+
+ra_status ring_attn_ulysses_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                                const void* dout, void* dq, void* dk, void* dv, int grad_dtype, void* workspace,
+                                size_t workspace_bytes, int B, int H, int Hkv, int L, int d, int n_shards,
+                                int causal, int layout, int dtype, void* stream)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if ((st = check_ulysses_heads(p)) != RA_OK) return st;
+    if (grad_dtype != RA_F32 && grad_dtype != RA_BF16)
+        return fail(RA_ERR_INVALID_ARG, "unknown grad dtype %d", grad_dtype);
+    if ((long long)B * H * L * d >= (1LL << 32))  // the float32 dq all-to-all indexes 4-byte words in 32 bits
+        return fail(RA_ERR_UNSUPPORTED, "tensor of 2^32 elements or more");
+    if ((st = check_ptrs({q, k, v, out, lse, dout, dq, dk, dv, workspace})) != RA_OK) return st;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const size_t need = ring_attn_ulysses_bwd_workspace_size(B, H, Hkv, L, d, n_shards, dtype, grad_dtype);
+    if (workspace_bytes < need)
+        return fail(RA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    if ((st = check_device()) != RA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t e = elem_size(dtype), ge = elem_size(grad_dtype);
+    const size_t qrows = (size_t)B * H * L, kvrows = (size_t)B * Hkv * L;
+    char* w = static_cast<char*>(workspace);
+    auto take = [&](size_t bytes) { char* x = w; w += align256(bytes); return x; };
+    void* qh = take(qrows * d * e);
+    void* oh = take(qrows * d * e);
+    void* doh = take(qrows * d * e);
+    void* kh = take(kvrows * d * e);
+    void* vh = take(kvrows * d * e);
+    float* lh = reinterpret_cast<float*>(take(qrows * sizeof(float)));
+    void* dqh = take(qrows * d * ge);
+    void* dkh = take(kvrows * d * ge);
+    void* dvh = take(kvrows * d * ge);
+    const int pn = n_shards;
+    const size_t inner = ring_attn_bwd_workspace_size(pn * B, H / pn, Hkv / pn, L, d, grad_dtype);
+    void* iw = take(inner);
+    const Geometry geo = p.geo();
+    const int row = (int)(d * e), grow = (int)(d * ge);
+    cudaError_t err = launch_ulysses_a2a(geo, B, H, row, q, qh, 0, s);
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, H, row, out, oh, 0, s);
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, H, row, dout, doh, 0, s);
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, Hkv, row, k, kh, 0, s);
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, Hkv, row, v, vh, 0, s);
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, H, 4, lse, lh, 0, s);
+    if (err != cudaSuccess) return cuda_fail(err, "ring_attn_ulysses_bwd launch");
+    // every shard: the ordinary backward over the whole sequence for its heads (one call, n * B problems)
+    st = bwd_impl(qh, kh, vh, oh, lh, doh, dqh, dkh, dvh, grad_dtype, iw, inner,
+                  Problem{pn * B, H / pn, Hkv / pn, L, d, 1, causal, RA_LAYOUT_CONTIGUOUS, dtype}, nullptr, stream);
+    if (st != RA_OK) return st;
+    err = launch_ulysses_a2a(geo, B, H, grow, dqh, dq, 1, s);
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, Hkv, grow, dkh, dk, 1, s);
+    if (err == cudaSuccess) err = launch_ulysses_a2a(geo, B, Hkv, grow, dvh, dv, 1, s);
+    if (err != cudaSuccess) return cuda_fail(err, "ring_attn_ulysses_bwd launch");
+    return RA_OK;
+}
+
 ra_status ring_attn_device_status(unsigned int* status, void* stream)
 {
     if (!status) return fail(RA_ERR_INVALID_ARG, "status is NULL");

@@ -115,3 +115,25 @@ def test_ulysses_equals_ring_on_the_long_context_workload():
     idx = torch.from_numpy(rows).to(DEV)
     assert_close(to_np(o_buf[idx]), ref_o, torch.bfloat16, "sampled out")
     assert_close(to_np(l_buf[idx]), ref_l, torch.bfloat16, "sampled lse")
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,d,n,causal,layout,dtype", [
+    (1, 8, 4, 1024, 128, 4, True, "zigzag", torch.bfloat16),    # tensor-core backward per shard
+    (1, 4, 4, 512, 128, 2, False, "contiguous", torch.bfloat16),
+    (1, 4, 2, 384, 64, 2, True, "striped", torch.float32),      # CUDA-core backward per shard
+])
+@pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
+def test_ulysses_bwd_matches_oracle(B, H, Hkv, L, d, n, causal, layout, dtype, grad_dtype):
+    if dtype == torch.float32 and grad_dtype == torch.bfloat16:
+        pytest.skip("bf16 gradients are only offered for bf16 inputs in this suite")
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=dtype, seed=L + 7 * H, with_dout=True)
+    tok = {t: torch.from_numpy(to_token_split(x[t].float().numpy(), n)).to(dtype).to(DEV)
+           for t in ("q", "k", "v", "dout")}
+    out, lse = ra.ulysses_fwd(tok["q"], tok["k"], tok["v"], n, causal, layout)
+    dq, dk, dv = ra.ulysses_bwd(tok["q"], tok["k"], tok["v"], out, lse, tok["dout"], n, causal, layout,
+                                grad_dtype=grad_dtype)
+    torch.cuda.synchronize()
+    rq, rk, rv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], n, causal, layout)
+    for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        assert got.dtype == grad_dtype
+        assert_close(to_np(got), to_token_split(ref, n), dtype, name, stored_bf16=grad_dtype == torch.bfloat16)
