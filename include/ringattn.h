@@ -126,6 +126,24 @@ RA_API ra_status ring_attn_fwd_stepwise(const void* q, const void* k, const void
 RA_API size_t ring_attn_fwd_stepwise_workspace_size(int B, int H, int L, int d);
 
 /*
+ * ring_attn_fwd_host -- ring_attn_fwd on HOST buffers: q, k, v are read from host memory and out,
+ * lse written back to host memory, with the copies overlapped with the compute.  The problem is
+ * cut into its B * Hkv kv-head groups (each group: the G = H / Hkv query heads that share a kv
+ * head); while group g runs on `stream`, the inputs of group g + 1 are copied in and the results of
+ * group g - 1 copied out on two copy streams of the library (one H2D, one D2H), through two device
+ * slots of the workspace.  Each copy is one cudaMemcpyAsync of a contiguous slice.
+ *   q, k, v, out, lse: HOST pointers with the layouts of ring_attn_fwd; page-locked memory lets the
+ *   copies run asynchronously and overlap (pageable memory works but serialises them).
+ *   workspace: DEVICE, 256-byte aligned, >= ring_attn_fwd_host_workspace_size(H, Hkv, L, d, dtype).
+ *   Stream-ordered: when `stream` completes, out and lse are on the host.  One call at a time per
+ *   device enqueues (a library mutex); calls on one device run one after another.
+ */
+RA_API ra_status ring_attn_fwd_host(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                                    int H, int Hkv, int L, int d, int n_shards, int causal, int layout,
+                                    int dtype, void* workspace, size_t workspace_bytes, void* stream);
+RA_API size_t ring_attn_fwd_host_workspace_size(int H, int Hkv, int L, int d, int dtype);
+
+/*
  * ring_attn_bwd -- gradients of sum(out * dout) with respect to q, k and v, recomputing the
  * attention weights P = exp(s - lse) from the saved lse (the pages give no backward; this is the
  * derivative of the forward definition): D = rowsum(dout * out), dS = P (dout . v - D),

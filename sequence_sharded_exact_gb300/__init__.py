@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     bwd_workspace_size,
     device_status,
     fwd,
+    fwd_host,
     fwd_stepwise,
     fwd_tile_visits,
     bwd,

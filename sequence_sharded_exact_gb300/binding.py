@@ -30,7 +30,8 @@ EXPORTS = (
     "ring_attn_last_error", "ring_attn_abi_version", "ring_attn_bwd_static_scratch",
     "ring_attn_bwd_static_scratch_capacity", "ring_attn_fwd_tile_visits", "ring_attn_bwd_tile_visits",
     "ring_attn_rope", "ring_attn_ulysses_a2a", "ring_attn_ulysses_fwd", "ring_attn_ulysses_workspace_size",
-    "ring_attn_ulysses_bwd", "ring_attn_ulysses_bwd_workspace_size",
+    "ring_attn_ulysses_bwd", "ring_attn_ulysses_bwd_workspace_size", "ring_attn_fwd_host",
+    "ring_attn_fwd_host_workspace_size",
 )
 
 
@@ -90,6 +91,10 @@ def library():
         lib.ring_attn_ulysses_bwd.restype = ctypes.c_int
         lib.ring_attn_ulysses_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         lib.ring_attn_ulysses_bwd_workspace_size.restype = SZ
+        lib.ring_attn_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P]
+        lib.ring_attn_fwd_host.restype = ctypes.c_int
+        lib.ring_attn_fwd_host_workspace_size.argtypes = [I, I, I, I, I]
+        lib.ring_attn_fwd_host_workspace_size.restype = SZ
         lib.ring_attn_bwd_static_scratch_capacity.argtypes = []
         lib.ring_attn_bwd_static_scratch_capacity.restype = SZ
         for name in EXPORTS:
@@ -195,6 +200,28 @@ def _fwd(q, k, v, n_shards, causal, layout, out, lse, visits, stream):
         _check(library().ring_attn_fwd(*args, _stream(stream, q.device)))
     else:
         _check(library().ring_attn_fwd_tile_visits(*args, _ptr(visits), _stream(stream, q.device)))
+    return out, lse
+
+
+def fwd_host(q, k, v, n_shards, causal=True, layout="zigzag", out=None, lse=None, workspace=None, device=None,
+             stream=None):
+    """ring_attn_fwd_host: q, k, v are CPU tensors (page-locked for overlap); returns CPU (out, lse).
+    The copies in and out overlap the compute of other kv-head groups."""
+    B, H, Hkv, L, d = _dims(q, k)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous CPU tensor")
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, pin_memory=True)
+    need = int(library().ring_attn_fwd_host_workspace_size(H, Hkv, L, d, _dtype_code(q.dtype)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check(library().ring_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, L, d,
+                                        int(n_shards), int(causal), _layout(layout), _dtype_code(q.dtype),
+                                        _ptr(workspace), workspace.numel(), _stream(stream, dev)))
     return out, lse
 
 

@@ -560,6 +560,114 @@ ra_status ring_attn_ulysses_bwd(const void* q, const void* k, const void* v, con
     return RA_OK;
 }
 
+namespace {
+
+// Copy streams and events of the host-buffer forward, created once per device.
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t entry = nullptr, in_done[2] = {}, compute_done[2] = {}, out_done[2] = {};
+    std::mutex mu;  // one host-buffer forward enqueues at a time per device (the events are shared)
+};
+HostPipe g_pipe[kMaxDevices];
+
+cudaError_t host_pipe_init(HostPipe& hp)
+{
+    if (hp.ready) return cudaSuccess;
+    cudaError_t e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.entry, cudaEventDisableTiming);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+        e = cudaEventCreateWithFlags(&hp.in_done[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.compute_done[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.out_done[i], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess) hp.ready = true;
+    return e;
+}
+
+}  // namespace
+
+size_t ring_attn_fwd_host_workspace_size(int H, int Hkv, int L, int d, int dtype)
+{
+    if (H < 1 || Hkv < 1 || L < 1 || d < 1 || H % Hkv) return 0;
+    const size_t e = elem_size(dtype), G = (size_t)(H / Hkv), rows = (size_t)L;
+    // per slot: q and out of one kv group's query heads, its k and v, its lse; two slots
+    const size_t slot = 2 * align256(G * rows * d * e) + 2 * align256(rows * d * e) + align256(G * rows * 4);
+    return 2 * slot;
+}
+
+ra_status ring_attn_fwd_host(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+                             int Hkv, int L, int d, int n_shards, int causal, int layout, int dtype, void* workspace,
+                             size_t workspace_bytes, void* stream)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if (!q || !k || !v || !out || !lse) return fail(RA_ERR_INVALID_ARG, "a host buffer is NULL");
+    if ((st = check_ptrs({workspace})) != RA_OK) return st;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const size_t need = ring_attn_fwd_host_workspace_size(H, Hkv, L, d, dtype);
+    if (workspace_bytes < need)
+        return fail(RA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    if ((st = check_device()) != RA_OK) return st;
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return fail(RA_ERR_NO_DEVICE, "device index out of range");
+    HostPipe& hp = g_pipe[dev];
+    std::lock_guard<std::mutex> lock(hp.mu);
+    cudaError_t e = host_pipe_init(hp);
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_fwd_host streams");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int* sw = nullptr;
+    const Problem pg{1, H / Hkv, 1, L, d, n_shards, causal, layout, dtype};  // one kv group
+    const bool tc = tc_fwd_supported(pg);
+    if (tc && !(sw = status_word(&e))) return cuda_fail(e, "status word");
+    const size_t es = elem_size(dtype), G = (size_t)(H / Hkv);
+    const size_t qbytes = G * L * d * es, kbytes = (size_t)L * d * es, lbytes = G * L * 4;
+    char* base = static_cast<char*>(workspace);
+    const size_t slot_bytes = 2 * align256(qbytes) + 2 * align256(kbytes) + align256(lbytes);
+    // earlier work on the caller's stream (a previous call using this workspace) comes first
+    e = cudaEventRecord(hp.entry, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.h2d, hp.entry, 0);
+    const int groups = B * Hkv;
+    for (int gi = 0; gi < groups && e == cudaSuccess; ++gi) {
+        const int sl = gi & 1;
+        char* w = base + sl * slot_bytes;
+        char* dq = w;
+        char* dout = dq + align256(qbytes);
+        char* dk = dout + align256(qbytes);
+        char* dv = dk + align256(kbytes);
+        float* dl = reinterpret_cast<float*>(dv + align256(kbytes));
+        // the slot is free once the group two back has been copied out
+        if (gi >= 2) e = cudaStreamWaitEvent(hp.h2d, hp.out_done[sl], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dq, static_cast<const char*>(q) + (size_t)gi * qbytes, qbytes,
+                                                  cudaMemcpyHostToDevice, hp.h2d);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dk, static_cast<const char*>(k) + (size_t)gi * kbytes, kbytes,
+                                                  cudaMemcpyHostToDevice, hp.h2d);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dv, static_cast<const char*>(v) + (size_t)gi * kbytes, kbytes,
+                                                  cudaMemcpyHostToDevice, hp.h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(hp.in_done[sl], hp.h2d);
+        // the group's attention on the caller's stream
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp.in_done[sl], 0);
+        if (e == cudaSuccess)
+            e = tc ? launch_fwd_tc(pg, dq, dk, dv, dout, dl, kFwdFused, 0, sw, s)
+                   : launch_fwd_simt(pg, dq, dk, dv, dout, dl, kFwdFused, 0, s);
+        if (e == cudaSuccess) e = cudaEventRecord(hp.compute_done[sl], s);
+        // and its results back
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.compute_done[sl], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(static_cast<char*>(out) + (size_t)gi * qbytes, dout, qbytes,
+                                                  cudaMemcpyDeviceToHost, hp.d2h);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(reinterpret_cast<char*>(lse) + (size_t)gi * lbytes, dl, lbytes,
+                                                  cudaMemcpyDeviceToHost, hp.d2h);
+        if (e == cudaSuccess) e = cudaEventRecord(hp.out_done[sl], hp.d2h);
+    }
+    // the caller's stream completes only after the last results are on the host
+    for (int sl = 0; sl < 2 && sl < groups && e == cudaSuccess; ++sl) e = cudaStreamWaitEvent(s, hp.out_done[sl], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_fwd_host");
+    return RA_OK;
+}
+
 ra_status ring_attn_device_status(unsigned int* status, void* stream)
 {
     if (!status) return fail(RA_ERR_INVALID_ARG, "status is NULL");

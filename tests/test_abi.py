@@ -60,7 +60,9 @@ def _fwd(lib, **kw):
     (dict(layout=7), binding.RA_ERR_INVALID_ARG),
     (dict(dtype=5), binding.RA_ERR_INVALID_ARG),
     (dict(causal=2), binding.RA_ERR_INVALID_ARG),
-    (dict(B=0), binding.RA_ERR_INVALID_ARG),
+    (dict(B=0), binding.RA_ERR_INVALID_ARG),                   # empty problem
+    (dict(L=0), binding.RA_ERR_INVALID_ARG),
+    (dict(B=256, H=32, Hkv=8, L=1 << 20, n=8), binding.RA_ERR_UNSUPPORTED),  # 2^40 elements of q
 ])
 def test_argument_errors_before_any_cuda_call(lib, kw, status):
     assert _fwd(lib, **kw) == status
@@ -158,3 +160,16 @@ def test_ulysses_head_divisibility_and_workspace(lib):
     B, H, Hkv, L, d = 1, 32, 8, 131072, 128
     want = 2 * B * H * L * d * 2 + 2 * B * Hkv * L * d * 2 + B * H * L * 4
     assert binding.library().ring_attn_ulysses_workspace_size(B, H, Hkv, L, d, 1) == want
+
+
+def test_fwd_host_argument_errors(lib):
+    P = ctypes.c_void_p
+    need = lib.ring_attn_fwd_host_workspace_size(32, 8, 131072, 128, 1)
+    # per slot: q and out of 4 heads (2 x 128 MiB), k and v (2 x 32 MiB), lse (2 MiB); two slots
+    assert need == 2 * (2 * 4 * 131072 * 128 * 2 + 2 * 131072 * 128 * 2 + 4 * 131072 * 4)
+    ptrs = [P(4096)] * 5
+    st = lib.ring_attn_fwd_host(P(4096), None, P(4096), P(4096), P(4096), 1, 32, 8, 131072, 128, 8, 1, 1, 1,
+                                P(256), need, None)
+    assert st == binding.RA_ERR_INVALID_ARG
+    st = lib.ring_attn_fwd_host(*ptrs, 1, 32, 8, 131072, 128, 8, 1, 1, 1, P(256), need - 1, None)
+    assert st == binding.RA_ERR_INVALID_ARG and "workspace too small" in lib.ring_attn_last_error().decode()

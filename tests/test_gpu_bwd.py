@@ -69,6 +69,10 @@ BWD_CASES = [
     (1, 2, 1, 600, 128, 3, True, "contiguous", torch.bfloat16),
     (1, 2, 1, 384, 64, 3, True, "striped", torch.float32),
     (1, 2, 2, 600, 128, 3, True, "striped", torch.bfloat16),
+    # degenerate shards: one row per zigzag chunk / per shard, a single token
+    (1, 2, 1, 8, 64, 4, True, "zigzag", torch.float32),
+    (1, 1, 1, 3, 64, 3, True, "striped", torch.float32),
+    (1, 1, 1, 1, 64, 1, True, "contiguous", torch.float32),
 ]
 
 

@@ -85,6 +85,11 @@ SIMT_CASES = [
     (1, 2, 1, 300, 64, 3, False, "contiguous", torch.float32),
     (1, 2, 2, 384, 128, 3, True, "striped", torch.bfloat16),       # S = 128: below a block
     (1, 2, 1, 600, 64, 5, True, "striped", torch.float32),
+    # degenerate shards: one row per shard / per zigzag chunk
+    (1, 2, 1, 4, 64, 4, True, "contiguous", torch.float32),
+    (1, 2, 2, 8, 128, 4, True, "zigzag", torch.bfloat16),
+    (2, 1, 1, 6, 64, 3, True, "striped", torch.float32),
+    (1, 1, 1, 1, 64, 1, True, "contiguous", torch.float32),        # a single token
 ]
 
 
@@ -191,3 +196,22 @@ def test_striped_ring_step_first_rows(d, L, dtype):
                 assert torch.count_nonzero(o[:, :, i * S]).item() == 0
             else:
                 assert np.all(np.isfinite(rows[:, :, 0]))
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,d,n,layout,dtype,pinned", [
+    (2, 4, 2, 2048, 128, 4, "zigzag", torch.bfloat16, True),   # tensor-core groups
+    (1, 2, 1, 600, 64, 3, "striped", torch.float32, True),     # CUDA-core groups
+    (1, 4, 4, 1024, 128, 2, "contiguous", torch.bfloat16, False),
+])
+def test_fwd_host_equals_device_forward(B, H, Hkv, L, d, n, layout, dtype, pinned):
+    """ring_attn_fwd_host (host buffers, per-group copies overlapped with compute) returns exactly
+    what ring_attn_fwd returns on device-resident inputs (same kernels, no atomics)."""
+    x = inputs(B, H, Hkv, L, d, dtype, seed=L + 17)
+    hq, hk, hv = (x[t].pin_memory() if pinned else x[t].clone() for t in ("q", "k", "v"))
+    out_h, lse_h = ra.fwd_host(hq, hk, hv, n, True, layout)
+    torch.cuda.current_stream().synchronize()
+    out_d, lse_d = ra.fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), n, True, layout)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
+    ref_o, ref_l = oracle.attn_fwd(x["q"], x["k"], x["v"], n, True, layout)
+    assert_close(to_np(out_h), ref_o, dtype, "out")
