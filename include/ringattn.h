@@ -283,6 +283,17 @@ RA_API ra_status ring_attn_fwd_path(int B, int H, int Hkv, int L, int d, int n_s
 RA_API ra_status ring_attn_bwd_path(int B, int H, int Hkv, int L, int d, int n_shards, int causal,
                              int layout, int dtype, int* path);
 
+/*
+ * ring_attn_selftest_bounded_wait -- exercises the failure path of the kernels' bounded waits
+ * without a fault: one GPU thread waits, through the kernels' own bounded-wait routine, on an
+ * mbarrier that nothing will complete.  After limit_ns (1e3 .. 1e8 ns) the wait gives up, sets
+ * RA_DEVICE_TIMEOUT in the device status word (read it with ring_attn_device_status) and the
+ * kernel returns; the context stays usable.  *returned (DEVICE pointer to an unsigned int,
+ * 16-byte aligned) receives 1 when the wait gave up, 2 if it had completed.
+ */
+RA_API ra_status ring_attn_selftest_bounded_wait(unsigned long long limit_ns, unsigned int* returned,
+                                                 void* stream);
+
 /* Reads the device status word of the current device into *status (HOST pointer; bits
  * RA_DEVICE_*), then clears it.  Synchronises `stream`. */
 RA_API ra_status ring_attn_device_status(unsigned int* status, void* stream);

@@ -31,7 +31,7 @@ EXPORTS = (
     "ring_attn_bwd_static_scratch_capacity", "ring_attn_fwd_tile_visits", "ring_attn_bwd_tile_visits",
     "ring_attn_rope", "ring_attn_ulysses_a2a", "ring_attn_ulysses_fwd", "ring_attn_ulysses_workspace_size",
     "ring_attn_ulysses_bwd", "ring_attn_ulysses_bwd_workspace_size", "ring_attn_fwd_host",
-    "ring_attn_fwd_host_workspace_size",
+    "ring_attn_fwd_host_workspace_size", "ring_attn_selftest_bounded_wait",
 )
 
 
@@ -95,6 +95,8 @@ def library():
         lib.ring_attn_fwd_host.restype = ctypes.c_int
         lib.ring_attn_fwd_host_workspace_size.argtypes = [I, I, I, I, I]
         lib.ring_attn_fwd_host_workspace_size.restype = SZ
+        lib.ring_attn_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, P, P]
+        lib.ring_attn_selftest_bounded_wait.restype = ctypes.c_int
         lib.ring_attn_bwd_static_scratch_capacity.argtypes = []
         lib.ring_attn_bwd_static_scratch_capacity.restype = SZ
         for name in EXPORTS:
@@ -436,6 +438,15 @@ def ulysses_bwd(q, k, v, out, lse, dout, n_shards, causal=True, layout="contiguo
                                            workspace.numel(), B, H, Hkv, L, d, n, int(causal), _layout(layout),
                                            _dtype_code(q.dtype), _stream(stream, q.device)))
     return dq, dk, dv
+
+
+def selftest_bounded_wait(limit_ns=2_000_000, stream=None, device=None):
+    """ring_attn_selftest_bounded_wait: a GPU wait that nothing completes runs out after limit_ns.
+    Returns the kernel's report (1: gave up, 2: completed); the status word then has the timeout bit."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    flag = torch.zeros(4, dtype=torch.int32, device=dev)
+    _check(library().ring_attn_selftest_bounded_wait(int(limit_ns), _ptr(flag), _stream(stream, dev)))
+    return int(flag[0].item())
 
 
 def device_status(stream=None, device=None):

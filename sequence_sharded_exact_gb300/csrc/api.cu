@@ -668,6 +668,22 @@ ra_status ring_attn_fwd_host(const void* q, const void* k, const void* v, void* 
     return RA_OK;
 }
 
+ra_status ring_attn_selftest_bounded_wait(unsigned long long limit_ns, unsigned int* returned, void* stream)
+{
+    if (limit_ns < 1000ull || limit_ns > 100000000ull)
+        return fail(RA_ERR_INVALID_ARG, "limit_ns must be in [1e3, 1e8] (1 us to 100 ms)");
+    ra_status st = check_ptrs({returned});
+    if (st != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaError_t e;
+    unsigned int* sw = status_word(&e);
+    if (!sw) return cuda_fail(e, "status word");
+    e = launch_bounded_wait_selftest(sw, limit_ns, static_cast<unsigned int*>(returned),
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_selftest_bounded_wait launch");
+    return RA_OK;
+}
+
 ra_status ring_attn_device_status(unsigned int* status, void* stream)
 {
     if (!status) return fail(RA_ERR_INVALID_ARG, "status is NULL");

@@ -60,6 +60,11 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, int dtype, 
                                   int d, float* D, cudaStream_t s);
 cudaError_t launch_zero(float* dst, long long count, cudaStream_t s);
 
+// One thread waits on an mbarrier nothing completes (bounded wait of limit_ns); *returned = 1 when
+// the wait gave up (and the timeout bit is set in *status), 2 if it completed.
+cudaError_t launch_bounded_wait_selftest(unsigned int* status, unsigned long long limit_ns, unsigned int* returned,
+                                         cudaStream_t s);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

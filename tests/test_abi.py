@@ -173,3 +173,10 @@ def test_fwd_host_argument_errors(lib):
     assert st == binding.RA_ERR_INVALID_ARG
     st = lib.ring_attn_fwd_host(*ptrs, 1, 32, 8, 131072, 128, 8, 1, 1, 1, P(256), need - 1, None)
     assert st == binding.RA_ERR_INVALID_ARG and "workspace too small" in lib.ring_attn_last_error().decode()
+
+
+def test_selftest_bounded_wait_argument_errors(lib):
+    P = ctypes.c_void_p
+    assert lib.ring_attn_selftest_bounded_wait(10, P(256), None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_selftest_bounded_wait(10**9, P(256), None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_selftest_bounded_wait(10**6, None, None) == binding.RA_ERR_INVALID_ARG
