@@ -15,7 +15,17 @@ constexpr unsigned kFull = 0xffffffffu;
 // Merge of two normalised partial results of the same rows (online softmax across ring steps,
 // LLM-101-CN "distributed hands-on code" section 6.2, rewritten for normalised partials):
 //   lse = max(a, b) + log(1 + exp(-|a - b|)),  o = exp(a - lse) o_a + exp(b - lse) o_b.
-// One warp per row; every lane reads both lse values before lane 0 overwrites lse_acc.
+// One warp per row.  For d = 128 (one float4 per lane) a warp takes four rows at a time and issues
+// every load of them before it needs any, so that enough bytes are in flight to keep
+// HBM busy; every lane reads both lse values before lane 0 overwrites lse_acc.
+__device__ __forceinline__ void merge_weights(float a, float b, float& wa, float& wb, float& lse)
+{
+    const float mx = fmaxf(a, b);
+    lse = mx + log1pf(expf(-fabsf(a - b)));
+    wa = expf(a - lse);
+    wb = expf(b - lse);
+}
+
 __global__ void __launch_bounds__(256)
 lse_merge_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
                  const float* __restrict__ o_part, const float* __restrict__ lse_part,
@@ -23,16 +33,42 @@ lse_merge_kernel(float* __restrict__ o_acc, float* __restrict__ lse_acc,
 {
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-    for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
-         row += warps) {
+    const long long w0 = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (d == 128) {
+        constexpr int R = 4;  // rows per warp per iteration, all loaded before any is used
+        for (long long r0 = R * w0; r0 < rows; r0 += R * warps) {
+            float a[R], b[R];
+            float4 x[R], y[R];
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                const long long r = r0 + k < rows ? r0 + k : r0;
+                a[k] = lse_acc[r];
+                b[k] = lse_part[r];
+                x[k] = reinterpret_cast<const float4*>(o_acc + r * 128)[lane];
+                y[k] = reinterpret_cast<const float4*>(o_part + r * 128)[lane];
+            }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                const long long r = r0 + k;
+                if (r >= rows || b[k] == -INFINITY) continue;  // an empty partial leaves the row unchanged
+                float wa, wb, lse;
+                merge_weights(a[k], b[k], wa, wb, lse);
+                reinterpret_cast<float4*>(o_acc + r * 128)[lane] =
+                    make_float4(wa * x[k].x + wb * y[k].x, wa * x[k].y + wb * y[k].y, wa * x[k].z + wb * y[k].z,
+                                wa * x[k].w + wb * y[k].w);
+                if (lane == 0) lse_acc[r] = lse;
+            }
+        }
+        return;
+    }
+    for (long long row = w0; row < rows; row += warps) {
         const float a = lse_acc[row];
         const float b = lse_part[row];
         __syncwarp();
         if (b == -INFINITY) continue;
-        const float mx = fmaxf(a, b);
-        const float lse = mx + log1pf(expf(-fabsf(a - b)));
-        const float wa = expf(a - lse);
-        const float wb = expf(b - lse);
+        float wa, wb, lse;
+        merge_weights(a, b, wa, wb, lse);
         float* oa = o_acc + row * d;
         const float* ob = o_part + row * d;
         if ((d & 3) == 0) {

@@ -149,9 +149,9 @@ def test_constant_v_gives_constant_output():
     assert err <= 2e-2 * max(1.0, c.float().abs().max().item())
 
 
-def test_lse_merge_kernel():
+@pytest.mark.parametrize("rows,d", [(1000, 128), (999, 128), (1, 128), (333, 64)])
+def test_lse_merge_kernel(rows, d):
     """Merging two partials of a row set equals the log-sum-exp combination of their weights."""
-    rows, d = 1000, 128
     g = torch.Generator().manual_seed(4)
     oa, ob = torch.randn(rows, d, generator=g), torch.randn(rows, d, generator=g)
     la, lb = torch.randn(rows, generator=g) * 5, torch.randn(rows, generator=g) * 5
