@@ -482,6 +482,21 @@ def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
                               "a2a_q_GB/s": 2 * qbytes / 1e9 / (statistics.mean(ams) / 1e3),
                               "a2a_q_ms": statistics.mean(ams)}
         del qt, kt, vt, ot, lt_, wsu, hs
+    # causal work per shard: the host scheduler's tile counts for the contiguous 8K configuration and
+    # for this workload, and the tile pairs the forward kernel computed on the device, per shard pair
+    c8 = synth.WORKLOADS["causal_contig_8k"]
+    sched = {}
+    for name, ww in (("causal_contig_8k", c8), (args.workload, w)):
+        for lay in ("contiguous", "zigzag", "striped"):
+            if lay == "zigzag" and ww["L"] % (2 * ww["n"]):
+                continue
+            t = ra.shard_tiles(ww["L"], ww["n"], ww["causal"], lay)
+            sched[f"{name}/{lay}"] = {"tiles_per_shard_per_head": t, "max_over_mean": max(t) / (sum(t) / len(t))}
+    _, _, visits = ra.fwd_tile_visits(x["q"], x["k"], x["v"], n, w["causal"], w["layout"], stream=stream)
+    per_shard = visits.sum(dim=1).tolist()
+    sched["device_visits_" + w["layout"]] = {"tile_pairs_per_query_shard": per_shard,
+                                             "max_over_mean": max(per_shard) / (sum(per_shard) / len(per_shard))}
+    res["causal_work_per_shard"] = sched
     # training workload: forward + backward
     t = synth.WORKLOADS[TRAIN_WORKLOAD]
     xt = synth.make_workload(TRAIN_WORKLOAD, device=dev, gen_device=dev)
