@@ -49,6 +49,8 @@ TC_BWD_CASES = [
     (1, 2, 1, 1536, 3, True, "striped"),     # 4 tiles per shard: two mirrored pairs
     (1, 2, 2, 384, 3, True, "striped"),      # one tile per shard
     (2, 2, 2, 512, 2, False, "striped"),
+    (1, 8, 1, 1024, 2, True, "zigzag"),      # GQA 8:1
+    (2, 4, 2, 1024, 4, True, "striped"),
 ]
 
 

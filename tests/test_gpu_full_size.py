@@ -108,3 +108,22 @@ def test_full_size_training_backward(name):
     for got, ref, what in ((dk.view(-1, d)[idx], ref_dk, "dk"), (dv.view(-1, d)[idx], ref_dv, "dv")):
         ma, rl = errors(to_np(got), ref)
         assert ma <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"{what} {ma:.3e} {rl:.3e}"
+
+
+def test_forward_at_262144_tokens_sampled_rows():
+    """The largest sequence in the suite: L = 262144 over 16 zigzag shards (positions up to 2^18),
+    8 query heads on 2 kv heads; sampled rows (with chunk edges) against the oracle."""
+    B, H, Hkv, L, d, n = 1, 8, 2, 262144, 128, 16
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=torch.bfloat16, seed=262144, device=DEV, gen_device=DEV)
+    assert ra.fwd_path(B, H, Hkv, L, d, n, True, "zigzag", torch.bfloat16) == "tcgen05"
+    out, lse = ra.fwd(x["q"], x["k"], x["v"], n, True, "zigzag")
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all().item() and torch.isfinite(lse).all().item()
+    w = dict(B=B, H=H, L=L, n=n, layout="zigzag")
+    rows = sampled_rows(w, 160, seed=3)
+    host = {t: x[t].cpu() for t in ("q", "k", "v")}
+    ref_o, ref_l = oracle.attn_fwd_rows(host["q"], host["k"], host["v"], n, True, "zigzag", rows)
+    idx = torch.from_numpy(rows).to(DEV)
+    for got, ref, what in ((to_np(out.view(-1, d)[idx]), ref_o, "out"), (to_np(lse.view(-1)[idx]), ref_l, "lse")):
+        ma, rl = errors(got, ref)
+        assert ma <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"{what}: {ma:.3e} {rl:.3e}"
