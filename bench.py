@@ -428,13 +428,14 @@ def main():
 
 
 def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
-    """Training workload (fwd + bwd), stepwise ring with LSE merge, and the merge bandwidth."""
+    """Training workload (fwd + bwd), stepwise ring (steps folded into a running result), and the
+    LSE merge bandwidth."""
     from sequence_sharded_exact_gb300 import synth
 
     res = {}
     B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
     steps = max(2, min(args.steps, 5))
-    # stepwise ring: n ring-step launches + n-1 merges + conversion
+    # stepwise ring: n ring-step launches (steps 1.. fold into the running result) + conversion
     ws = torch.empty(ra.library().ring_attn_fwd_stepwise_workspace_size(B, H, L, d),
                      dtype=torch.uint8, device=dev)
     out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
@@ -443,7 +444,7 @@ def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
                        steps, 1, stream)
     flops = fwd_flops(B, H, L, d, w["causal"])
     res["stepwise_fwd"] = {"tflops": flops / (statistics.mean(ms) / 1e3) / 1e12,
-                           "ms": statistics.mean(ms), "launches": 2 * n}
+                           "ms": statistics.mean(ms), "launches": n + 1}
     # LSE merge kernel alone: bytes = rows * (3 d + 3) * 4 (read o_acc, o_part, write o_acc, lse)
     rows = B * H * L
     o_acc = ws[: rows * d * 4].view(torch.float32).view(rows, d)

@@ -103,6 +103,20 @@ RA_API ra_status ring_attn_ring_step_fwd(const void* q, const void* k, const voi
                                   void* stream);
 
 /*
+ * ring_attn_ring_step_fwd_accumulate -- ring step `step` folded straight into a running result,
+ * in place: the block result of step `step` (as ring_attn_ring_step_fwd computes it) is merged into
+ * (o_acc, lse_acc) in the kernel's epilogue, as ring_attn_lse_merge would merge it, without the
+ * partial ever going to memory (the running (M, L, O) update of LLM-101-CN section 6.2 across
+ * steps).  o_acc [B][H][L][d] and lse_acc [B][H][L] float32: a valid running state -- finite o_acc
+ * rows; lse_acc = -infinity marks a row with nothing yet (its o_acc is then ignored).  A row that
+ * sees no key at this step is left unchanged.
+ */
+RA_API ra_status ring_attn_ring_step_fwd_accumulate(const void* q, const void* k, const void* v, float* o_acc,
+                                                    float* lse_acc, int B, int H, int Hkv, int L, int d,
+                                                    int n_shards, int step, int causal, int layout, int dtype,
+                                                    void* stream);
+
+/*
  * ring_attn_lse_merge -- fold one partial result into a running one, in place:
  *   lse = max(a, b) + log(1 + exp(-|a - b|)),  o = exp(a - lse) o_acc + exp(b - lse) o_part,
  * with a = lse_acc, b = lse_part (the online-softmax merge across ring steps, LLM-101-CN 6.2,
@@ -114,8 +128,9 @@ RA_API ra_status ring_attn_lse_merge(float* o_acc, float* lse_acc, const float* 
 
 /*
  * ring_attn_fwd_stepwise -- the ring forward run step by step, as the multi-device algorithm
- * does it: n_shards launches of the ring step followed by the LSE merge, then the conversion of
- * the float32 accumulator into `out`.  Same arguments and results as ring_attn_fwd, plus
+ * does it: n_shards launches, step 0 writing a float32 running output and lse and every later
+ * step folding its block into them (ring_attn_ring_step_fwd_accumulate), then the conversion of
+ * the float32 output into `out`.  Same arguments and results as ring_attn_fwd, plus
  *   workspace: device memory of at least ring_attn_fwd_stepwise_workspace_size(...) bytes,
  *   256-byte aligned, owned by the caller; its contents on entry do not matter.
  */

@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     library,
     lse_merge,
     ring_step_fwd,
+    ring_step_fwd_accumulate,
     rope,
     shard_tiles,
     ulysses_a2a,

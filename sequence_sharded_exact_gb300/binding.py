@@ -31,6 +31,7 @@ EXPORTS = (
     "ring_attn_bwd_static_scratch_capacity", "ring_attn_fwd_tile_visits", "ring_attn_bwd_tile_visits",
     "ring_attn_rope", "ring_attn_ulysses_a2a", "ring_attn_ulysses_fwd", "ring_attn_ulysses_workspace_size",
     "ring_attn_ulysses_bwd", "ring_attn_ulysses_bwd_workspace_size", "ring_attn_fwd_host",
+    "ring_attn_ring_step_fwd_accumulate",
     "ring_attn_fwd_host_workspace_size", "ring_attn_selftest_bounded_wait",
 )
 
@@ -97,6 +98,8 @@ def library():
         lib.ring_attn_fwd_host_workspace_size.restype = SZ
         lib.ring_attn_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, P, P]
         lib.ring_attn_selftest_bounded_wait.restype = ctypes.c_int
+        lib.ring_attn_ring_step_fwd_accumulate.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
+        lib.ring_attn_ring_step_fwd_accumulate.restype = ctypes.c_int
         lib.ring_attn_bwd_static_scratch_capacity.argtypes = []
         lib.ring_attn_bwd_static_scratch_capacity.restype = SZ
         for name in EXPORTS:
@@ -240,6 +243,21 @@ def ring_step_fwd(q, k, v, n_shards, step, causal=True, layout="zigzag", o_part=
                                              int(step), int(causal), _layout(layout),
                                              _dtype_code(q.dtype), _stream(stream, q.device)))
     return o_part, lse_part
+
+
+def ring_step_fwd_accumulate(q, k, v, n_shards, step, o_acc, lse_acc, causal=True, layout="zigzag", stream=None):
+    """ring_attn_ring_step_fwd_accumulate: fold ring step `step` into (o_acc float32 [B,H,L,d],
+    lse_acc [B,H,L]) in place.  Returns (o_acc, lse_acc)."""
+    B, H, Hkv, L, d = _dims(q, k)
+    for t, nm in ((o_acc, "o_acc"), (lse_acc, "lse_acc")):
+        _need(t, nm, q.device)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{nm} must be float32")
+    _check(library().ring_attn_ring_step_fwd_accumulate(_ptr(q), _ptr(k), _ptr(v), _ptr(o_acc), _ptr(lse_acc), B, H,
+                                                        Hkv, L, d, int(n_shards), int(step), int(causal),
+                                                        _layout(layout), _dtype_code(q.dtype),
+                                                        _stream(stream, q.device)))
+    return o_acc, lse_acc
 
 
 def lse_merge(o_acc, lse_acc, o_part, lse_part, stream=None):

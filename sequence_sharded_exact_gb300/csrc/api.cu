@@ -243,6 +243,30 @@ ra_status ring_attn_ring_step_fwd(const void* q, const void* k, const void* v, f
     return RA_OK;
 }
 
+ra_status ring_attn_ring_step_fwd_accumulate(const void* q, const void* k, const void* v, float* o_acc,
+                                             float* lse_acc, int B, int H, int Hkv, int L, int d, int n_shards,
+                                             int step, int causal, int layout, int dtype, void* stream)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if (step < 0 || step >= n_shards)
+        return fail(RA_ERR_INVALID_ARG, "step %d outside [0, n_shards)", step);
+    if ((st = check_ptrs({q, k, v, o_acc, lse_acc})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (tc_fwd_supported(p)) {
+        unsigned int* sw = status_word(&e);
+        if (!sw) return cuda_fail(e, "status word");
+        e = launch_fwd_tc(p, q, k, v, o_acc, lse_acc, kFwdRingStepAcc, step, sw, s);
+    } else {
+        e = launch_fwd_simt(p, q, k, v, o_acc, lse_acc, kFwdRingStepAcc, step, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_ring_step_fwd_accumulate launch");
+    return RA_OK;
+}
+
 ra_status ring_attn_lse_merge(float* o_acc, float* lse_acc, const float* o_part,
                               const float* lse_part, long long rows, int d, void* stream)
 {
@@ -261,7 +285,7 @@ size_t ring_attn_fwd_stepwise_workspace_size(int B, int H, int L, int d)
 {
     if (B < 1 || H < 1 || L < 1 || d < 1) return 0;
     const size_t rows = (size_t)B * H * L;
-    return 2 * align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+    return align256(rows * d * sizeof(float));  // the float32 running output
 }
 
 ra_status ring_attn_fwd_stepwise(const void* q, const void* k, const void* v, void* out,
@@ -281,20 +305,16 @@ ra_status ring_attn_fwd_stepwise(const void* q, const void* k, const void* v, vo
     if ((st = check_device()) != RA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const long long rows = p.q_rows();
-    char* ws = static_cast<char*>(workspace);
-    float* o_acc = reinterpret_cast<float*>(ws);
-    float* o_part = reinterpret_cast<float*>(ws + align256((size_t)rows * d * sizeof(float)));
-    float* lse_part = reinterpret_cast<float*>(ws + 2 * align256((size_t)rows * d * sizeof(float)));
+    float* o_acc = static_cast<float*>(workspace);
     const bool tc = tc_fwd_supported(p);
     cudaError_t e = cudaSuccess;
     unsigned int* sw = nullptr;
     if (tc && !(sw = status_word(&e))) return cuda_fail(e, "status word");
+    // step 0 writes the running (o, lse); every later step folds its block into it in its epilogue
     for (int step = 0; step < n_shards && e == cudaSuccess; ++step) {
-        float* o_dst = step == 0 ? o_acc : o_part;
-        float* l_dst = step == 0 ? lse : lse_part;
-        e = tc ? launch_fwd_tc(p, q, k, v, o_dst, l_dst, kFwdRingStep, step, sw, s)
-               : launch_fwd_simt(p, q, k, v, o_dst, l_dst, kFwdRingStep, step, s);
-        if (e == cudaSuccess && step > 0) e = launch_lse_merge(o_acc, lse, o_part, lse_part, rows, d, s);
+        const int mode = step == 0 ? kFwdRingStep : kFwdRingStepAcc;
+        e = tc ? launch_fwd_tc(p, q, k, v, o_acc, lse, mode, step, sw, s)
+               : launch_fwd_simt(p, q, k, v, o_acc, lse, mode, step, s);
     }
     if (e == cudaSuccess) e = launch_convert(o_acc, out, dtype, rows * d, 1.0f, s);
     if (e != cudaSuccess) return cuda_fail(e, "ring_attn_fwd_stepwise launch");

@@ -212,7 +212,8 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
             Unit u;
             if (!unit_of(a, item, member, u)) continue;
             const long long row_g = ((long long)u.b * a.H + u.h) * a.geo.L + u.r0 + w * kTile + rw;
-            if (u.ntiles == 0) {  // ring-step mode only: nothing visible from this block
+            if (u.ntiles == 0) {  // ring-step modes only: nothing visible from this block
+                if (a.mode == kFwdRingStepAcc) continue;  // the running result stays as it is
                 float* orow = static_cast<float*>(a.out) + row_g * kHd;
 #pragma unroll
                 for (int c = 0; c < kHd; c += 4)
@@ -351,6 +352,37 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
 #pragma unroll
                     for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                 }
+            } else if (a.mode == kFwdRingStepAcc) {
+                // fold this step into the running (out, lse): the online-softmax update across ring
+                // steps, on normalised results.  A row that saw no key in this step stays as it is;
+                // the TMEM loads stay warp-uniform, only the global update is per row.
+                const float acc = a.lse[row_g];
+                float wa = 1.f, wb = 0.f, lse = acc;
+                if (any) {
+                    const float b = (m_run + log2f(l_run)) * kLn2;
+                    const float mx = fmaxf(acc, b);
+                    lse = mx + log1pf(expf(-fabsf(acc - b)));
+                    wa = acc == -INFINITY ? 0.f : expf(acc - lse);
+                    wb = expf(b - lse) * inv;
+                }
+                float* orow = static_cast<float*>(a.out) + row_g * kHd;
+#pragma unroll 1
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(tO + c4 * 32, o);
+                    tmem_ld_wait(o);
+                    if (!any) continue;
+                    float4* dst = reinterpret_cast<float4*>(orow + c4 * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 x = dst[e];
+                        dst[e] = make_float4(wa * x.x + wb * __uint_as_float(o[4 * e]), wa * x.y + wb * __uint_as_float(o[4 * e + 1]),
+                                             wa * x.z + wb * __uint_as_float(o[4 * e + 2]),
+                                             wa * x.w + wb * __uint_as_float(o[4 * e + 3]));
+                    }
+                }
+                a.lse[row_g] = lse;
+                continue;
             } else {
                 float* orow = static_cast<float*>(a.out) + row_g * kHd;
 #pragma unroll 1

@@ -24,6 +24,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 enum FwdMode {
     kFwdFused = 0,     // all ring steps, write out (dtype) + lse
     kFwdRingStep = 1,  // one ring step, write float32 partial + lse (-inf when nothing visible)
+    kFwdRingStepAcc = 2,  // one ring step folded into a running float32 output + lse, in place
 };
 
 // SIMT (CUDA-core) kernels: any shape, f32 or bf16 inputs.

@@ -113,6 +113,20 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 #pragma unroll
         for (int e = 0; e < EPL; ++e) orow[lane + 32 * e] = from_f<T>(o[e] * inv);
         if (lane == 0) lse[row] = (m + log2f(l)) * kLn2;
+    } else if (mode == kFwdRingStepAcc) {
+        // fold this step into the running (out, lse); an empty step leaves the row as it is
+        if (!(l > 0.f)) return;
+        const float b = (m + log2f(l)) * kLn2;
+        const float acc = lse[row];
+        __syncwarp();  // every lane has read lse before lane 0 overwrites it
+        const float mx = fmaxf(acc, b);
+        const float nl = mx + log1pf(expf(-fabsf(acc - b)));
+        const float wa = acc == -INFINITY ? 0.f : expf(acc - nl);
+        const float wb = expf(b - nl) / l;
+        float* orow = static_cast<float*>(out) + row * D;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) orow[lane + 32 * e] = wa * orow[lane + 32 * e] + wb * o[e];
+        if (lane == 0) lse[row] = nl;
     } else {
         float* orow = static_cast<float*>(out) + row * D;
         const bool any = l > 0.f;

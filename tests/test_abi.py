@@ -111,7 +111,19 @@ def test_shard_tiles_workloads():
 def test_workspace_sizes(lib):
     assert binding.bwd_workspace_size(1, 32, 8, 65536, 128, torch.float32) >= 32 * 65536 * 4
     assert binding.bwd_workspace_size(1, 32, 8, 65536, 128, torch.bfloat16) >= 32 * 65536 * 129 * 4
-    assert lib.ring_attn_fwd_stepwise_workspace_size(1, 2, 1024, 128) >= 2 * 2 * 1024 * 128 * 4
+    assert lib.ring_attn_fwd_stepwise_workspace_size(1, 2, 1024, 128) >= 2 * 1024 * 128 * 4
+
+
+def test_ring_step_accumulate_argument_errors(lib):
+    """The folded ring step refuses a step outside [0, n_shards) and NULL running buffers before
+    any CUDA call."""
+    P = ctypes.c_void_p
+    ptrs = [P(256)] * 5
+    f = lib.ring_attn_ring_step_fwd_accumulate
+    assert f(*ptrs, 1, 2, 2, 1024, 128, 4, 4, 1, 1, 1, None) == binding.RA_ERR_INVALID_ARG
+    assert "step" in lib.ring_attn_last_error().decode()
+    assert f(*ptrs, 1, 2, 2, 1024, 128, 4, -1, 1, 1, 1, None) == binding.RA_ERR_INVALID_ARG
+    assert f(*ptrs[:3], None, P(256), 1, 2, 2, 1024, 128, 4, 0, 1, 1, 1, None) == binding.RA_ERR_INVALID_ARG
 
 
 def test_tile_visits_argument_errors(lib):

@@ -106,7 +106,8 @@ def test_simt_fwd_matches_oracle(B, H, Hkv, L, d, n, causal, layout, dtype):
     (1, 2, 1, 600, 64, 3, "striped", torch.float32),
 ])
 def test_stepwise_ring_matches_oracle_and_fused(B, H, Hkv, L, d, n, layout, dtype):
-    """n ring-step launches folded with the LSE merge equal full attention and the fused kernel."""
+    """n ring-step launches, each folded into the running result in its epilogue, equal full
+    attention and the fused kernel."""
     x = inputs(B, H, Hkv, L, d, dtype, seed=77)
     q, k, v = (x[t].to(DEV) for t in ("q", "k", "v"))
     out_s, lse_s = ra.fwd_stepwise(q, k, v, n, True, layout)
@@ -116,6 +117,59 @@ def test_stepwise_ring_matches_oracle_and_fused(B, H, Hkv, L, d, n, layout, dtyp
     assert_close(to_np(out_s), ref_o, dtype, "stepwise out")
     assert_close(to_np(lse_s), ref_l, dtype, "stepwise lse")
     assert_close(to_np(out_s), to_np(out_f), dtype, "stepwise vs fused")
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,d,n,layout,dtype", [
+    (1, 4, 2, 1024, 128, 4, "zigzag", torch.bfloat16),
+    (1, 2, 1, 600, 64, 3, "striped", torch.float32),
+])
+def test_ring_steps_with_lse_merge_match_oracle(B, H, Hkv, L, d, n, layout, dtype):
+    """n separate ring-step partials folded by the LSE merge kernel equal full attention (the
+    two-kernel form of the step loop)."""
+    x = inputs(B, H, Hkv, L, d, dtype, seed=78)
+    q, k, v = (x[t].to(DEV) for t in ("q", "k", "v"))
+    o_acc, l_acc = ra.ring_step_fwd(q, k, v, n, 0, True, layout)
+    for step in range(1, n):
+        o, lse = ra.ring_step_fwd(q, k, v, n, step, True, layout)
+        ra.lse_merge(o_acc, l_acc, o, lse)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attn_fwd(x["q"], x["k"], x["v"], n, True, layout)
+    assert_close(o_acc.cpu().numpy(), ref_o, dtype, "merged out")
+    assert_close(l_acc.cpu().numpy(), ref_l, dtype, "merged lse")
+
+
+@pytest.mark.parametrize("L,d,n,layout,dtype", [
+    (1024, 128, 4, "zigzag", torch.bfloat16),      # tensor-core epilogue
+    (2048, 128, 4, "striped", torch.bfloat16),
+    (1024, 128, 4, "contiguous", torch.bfloat16),  # rows that see nothing at a step
+    (600, 64, 3, "zigzag", torch.float32),         # CUDA-core epilogue
+    (400, 64, 4, "contiguous", torch.float32),
+])
+def test_ring_step_accumulate_equals_step_then_merge(L, d, n, layout, dtype):
+    """Folding a ring step into an arbitrary running state inside the kernel equals computing the
+    step's partial and merging it with the LSE merge: from a random state (finite rows, empty
+    rows with lse = -inf, rows with large lse gaps either way), at every step."""
+    B, H, Hkv = 1, 4, 2
+    x = inputs(B, H, Hkv, L, d, dtype, seed=79)
+    q, k, v = (x[t].to(DEV) for t in ("q", "k", "v"))
+    g = torch.Generator().manual_seed(80)
+    o0 = torch.randn(B, H, L, d, generator=g)
+    l0 = torch.randn(B, H, L, generator=g) * 4
+    l0[..., ::5] = float("-inf")
+    l0[..., 1::13] += 40.0
+    l0[..., 2::13] -= 40.0
+    for step in range(n):
+        o_ref, l_ref = o0.clone().to(DEV), l0.clone().to(DEV)
+        o, lse = ra.ring_step_fwd(q, k, v, n, step, True, layout)
+        ra.lse_merge(o_ref, l_ref, o, lse)
+        o_acc, l_acc = o0.clone().to(DEV), l0.clone().to(DEV)
+        ra.ring_step_fwd_accumulate(q, k, v, n, step, o_acc, l_acc, True, layout)
+        torch.cuda.synchronize()
+        seen = torch.isfinite(l_ref.cpu())  # rows empty before and after hold no defined output
+        assert torch.equal(torch.isneginf(l_acc.cpu()), torch.isneginf(l_ref.cpu())), step
+        dl = (l_acc.cpu() - l_ref.cpu())[seen].abs().max().item()
+        do = (o_acc.cpu() - o_ref.cpu())[seen].abs().max().item()
+        assert dl <= 1e-5 and do <= 2e-5, (step, dl, do)
 
 
 @pytest.mark.parametrize("d,L,dtype", [(128, 1024, torch.bfloat16), (64, 400, torch.float32)])
