@@ -577,15 +577,40 @@ __device__ __forceinline__ void producer_role(const BwdArgs& a, uint32_t sbase, 
 // ------------------------------------------------------------------------------------------------
 // MMA issuer (one thread)
 // ------------------------------------------------------------------------------------------------
+// Operand descriptors of the issue loops, as the low words of their shared-memory descriptors
+// (query-tile operands at stage 0): K-major views have LBO 16, N- or M-major views LBO = the
+// distance between their 64-element column blocks.  A stage or a k-step is a constant added to them.
+struct BwdDesc {
+    uint32_t q_k, q_n;    // Q tile, K-major (S^T) and N-major (dK)
+    uint32_t do_k, do_n;  // dO tile, K-major (dP^T) and N-major (dV)
+    uint32_t v_k;         // V tile, K-major (dP^T)
+    uint32_t k_m, ds_n;   // K tile M-major and dS^T N-major (dQ^T)
+};
+constexpr uint32_t kDescHi = sdesc_sw128_hi(1024);
+
+__device__ __forceinline__ BwdDesc make_desc(uint32_t sbase)
+{
+    BwdDesc d;
+    d.q_k = sdesc_sw128_lo(sbase + kSmemQ, 16);
+    d.q_n = sdesc_sw128_lo(sbase + kSmemQ, kQHalf);
+    d.do_k = sdesc_sw128_lo(sbase + kSmemDO, 16);
+    d.do_n = sdesc_sw128_lo(sbase + kSmemDO, kQHalf);
+    d.v_k = sdesc_sw128_lo(sbase + kSmemV, 16);
+    d.k_m = sdesc_sw128_lo(sbase + kSmemK, kKHalf);
+    d.ds_n = sdesc_sw128_lo(sbase + kSmemDS, kKHalf);
+    return d;
+}
+
 // S^T = K Q^T into TMEM columns [0, 64): A = K from TMEM (lane = key row, 8 columns per 16 head-dim
-// elements), B = Q K-major from shared memory.
-__device__ __forceinline__ void issue_st(uint32_t tmem, uint32_t sq)
+// elements), B = Q K-major from shared memory (stage st).
+__device__ __forceinline__ void issue_st(uint32_t tmem, const BwdDesc& dsc, uint32_t st)
 {
     constexpr uint32_t id = idesc_bf16_f32(128, 64, false, false);
+    const uint32_t qb = dsc.q_k + st * (kQBytes >> 4);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
         mma_ts(tmem + kColST, tmem + kColK + (uint32_t)kk * 8u,
-               sdesc_sw128(sq + (uint32_t)(kk >> 2) * kQHalf + (uint32_t)(kk & 3) * 32u, 16, 1024), id, kk > 0);
+               sdesc_at(qb, (uint32_t)(kk >> 2) * kQHalf + (uint32_t)(kk & 3) * 32u, kDescHi), id, kk > 0);
 }
 
 constexpr uint32_t kIdDK = idesc_bf16_f32(128, 128, false, true);  // dK: A dS^T (TMEM), B Q N-major
@@ -598,16 +623,18 @@ __device__ __forceinline__ uint32_t a_col(int kk) { return kk < 2 ? (uint32_t)kk
 
 // dK += dS^T Q for query tile gx (tile t of its unit), once phase B has finished, then wait until
 // the previous dQ^T has been read out; the dQ^T product itself is issued by the caller.
-__device__ __forceinline__ bool issue_dk(uint32_t sbase, uint32_t tmem, uint32_t gx, int t, const WaitCtl& ctl)
+__device__ __forceinline__ bool issue_dk(uint32_t sbase, uint32_t tmem, const BwdDesc& dsc, uint32_t gx, int t,
+                                         const WaitCtl& ctl)
 {
     auto bar = [&](int i) { return sbase + kSmemBar + 8u * (uint32_t)i; };
-    const uint32_t sq = sbase + kSmemQ + stage_of(gx) * kQBytes;
+    const uint32_t qb = dsc.q_n + stage_of(gx) * (kQBytes >> 4);
+    const uint32_t acc0 = t > 0 ? 1u : 0u;
     if (!mbar_wait(bar(BAR_DS_READY), gx & 1, ctl)) return false;
     tc_fence_after_sync();
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-        mma_ts(tmem + kColDK, tmem + kColDPT + a_col(kk), sdesc_sw128(sq + (uint32_t)kk * 2048u, kQHalf, 1024), kIdDK,
-               (t > 0 || kk > 0) ? 1u : 0u);
+        mma_ts(tmem + kColDK, tmem + kColDPT + a_col(kk), sdesc_at(qb, (uint32_t)kk * 2048u, kDescHi), kIdDK,
+               kk > 0 ? 1u : acc0);
     tc_commit(bar(BAR_Q_EMPTY + (int)stage_of(gx)));
     // dQ^T's columns: the previous tile's dQ^T must have been read out
     if (gx > 0 && !mbar_wait(bar(BAR_DQ_FREE), (gx - 1) & 1, ctl)) return false;
@@ -616,10 +643,10 @@ __device__ __forceinline__ bool issue_dk(uint32_t sbase, uint32_t tmem, uint32_t
 }
 
 // k-step kk of dQ^T = K^T dS^T.
-__device__ __forceinline__ void issue_dq_step(uint32_t sbase, uint32_t tmem, int kk)
+__device__ __forceinline__ void issue_dq_step(uint32_t tmem, const BwdDesc& dsc, int kk)
 {
-    mma_ss(tmem + kColDQ, sdesc_sw128(sbase + kSmemK + (uint32_t)kk * 2048u, kKHalf, 1024),
-           sdesc_sw128(sbase + kSmemDS + (uint32_t)kk * 2048u, kKHalf, 1024), kIdDQ, kk > 0);
+    mma_ss(tmem + kColDQ, sdesc_at(dsc.k_m, (uint32_t)kk * 2048u, kDescHi),
+           sdesc_at(dsc.ds_n, (uint32_t)kk * 2048u, kDescHi), kIdDQ, kk > 0);
 }
 
 __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint32_t tmem, const WaitCtl& ctl)
@@ -628,6 +655,7 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
     constexpr uint32_t id_dv = idesc_bf16_f32(128, 128, false, true);  // dV: A P^T (TMEM), B dO N-major
     uint32_t gt = 0, uc = 0;
     bool issued = false;
+    const BwdDesc dsc = make_desc(sbase);
     for (long long item = blockIdx.x; item < a.items; item += gridDim.x) {
         for (int member = 0; member < 2; ++member) {
             KvUnit u;
@@ -644,24 +672,24 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
             // the unit's first S^T; later ones are issued one tile ahead (below)
             if (!mbar_wait(bar(BAR_Q_FULL + (int)stage_of(gt)), phase_of(gt), ctl)) goto drain;
             tc_fence_after_sync();
-            issue_st(tmem, sbase + kSmemQ + stage_of(gt) * kQBytes);
+            issue_st(tmem, dsc, stage_of(gt));
             tc_commit(bar(BAR_ST_FULL));
             for (int t = 0; t < u.ntiles; ++t, ++gt) {
                 const uint32_t st = stage_of(gt), sp = phase_of(gt);
-                const uint32_t sd = sbase + kSmemDO + st * kQBytes;
+                const uint32_t dok = dsc.do_k + st * (kQBytes >> 4), don = dsc.do_n + st * (kQBytes >> 4);
                 // dK of the previous tile (its dS^T is ready when phase B ends; dK reads it from the
                 // dP^T columns, so it goes before the new dP^T)
-                if (t > 0 && !issue_dk(sbase, tmem, gt - 1, t - 1, ctl)) goto drain;
+                if (t > 0 && !issue_dk(sbase, tmem, dsc, gt - 1, t - 1, ctl)) goto drain;
                 // dP^T = V dO^T, its k-steps interleaved with those of the previous tile's dQ^T: two
                 // independent accumulators keep the tensor pipe busier than one chain at a time
                 if (!mbar_wait(bar(BAR_DO_FULL + (int)st), sp, ctl)) goto drain;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    if (t > 0) issue_dq_step(sbase, tmem, kk);
+                    if (t > 0) issue_dq_step(tmem, dsc, kk);
                     mma_ss(tmem + kColDPT,
-                           sdesc_sw128(sbase + kSmemV + (uint32_t)(kk >> 2) * kKHalf + (uint32_t)(kk & 3) * 32u, 16, 1024),
-                           sdesc_sw128(sd + (uint32_t)(kk >> 2) * kQHalf + (uint32_t)(kk & 3) * 32u, 16, 1024), kIdDP,
+                           sdesc_at(dsc.v_k, (uint32_t)(kk >> 2) * kKHalf + (uint32_t)(kk & 3) * 32u, kDescHi),
+                           sdesc_at(dok, (uint32_t)(kk >> 2) * kQHalf + (uint32_t)(kk & 3) * 32u, kDescHi), kIdDP,
                            kk > 0);
                 }
                 if (t > 0) tc_commit(bar(BAR_DQ_FULL));
@@ -672,7 +700,7 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
                 tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tmem + kColDV, tmem + kColST + a_col(kk), sdesc_sw128(sd + (uint32_t)kk * 2048u, kQHalf, 1024),
+                    mma_ts(tmem + kColDV, tmem + kColST + a_col(kk), sdesc_at(don, (uint32_t)kk * 2048u, kDescHi),
                            id_dv, (t > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(bar(BAR_DO_EMPTY + (int)st));
                 // next S^T, into the columns P^T leaves once the dV product above has read it
@@ -680,13 +708,13 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
                     const uint32_t nst = stage_of(gt + 1);
                     if (!mbar_wait(bar(BAR_Q_FULL + (int)nst), phase_of(gt + 1), ctl)) goto drain;
                     tc_fence_after_sync();
-                    issue_st(tmem, sbase + kSmemQ + nst * kQBytes);
+                    issue_st(tmem, dsc, nst);
                     tc_commit(bar(BAR_ST_FULL));
                 }
             }
-            if (!issue_dk(sbase, tmem, gt - 1, u.ntiles - 1, ctl)) goto drain;
+            if (!issue_dk(sbase, tmem, dsc, gt - 1, u.ntiles - 1, ctl)) goto drain;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) issue_dq_step(sbase, tmem, kk);
+            for (int kk = 0; kk < 8; ++kk) issue_dq_step(tmem, dsc, kk);
             tc_commit(bar(BAR_DQ_FULL));
             tc_commit(bar(BAR_KV_EMPTY));
             tc_commit(bar(BAR_ACC_FULL));

@@ -485,26 +485,36 @@ struct UnitCursor {
     }
 };
 
-__device__ __forceinline__ void issue_qk(uint32_t sbase, uint32_t tmem, int w, int stage)
+// Operand descriptors of the issue loops: low words of the Q, K and V tiles' descriptors (K and V
+// at stage 0), built once; a k-step or a stage is a constant added to them.
+struct FwdDesc {
+    uint32_t q, k, v;
+};
+constexpr uint32_t kDescHi = sdesc_sw128_hi(1024);
+
+__device__ __forceinline__ void issue_qk(const FwdDesc& dsc, uint32_t tmem, int w, int stage)
 {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+    const uint32_t kb = dsc.k + (uint32_t)stage * (kTileBytes >> 4);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         const uint32_t half = (uint32_t)(kk >> 2), koff = (uint32_t)(kk & 3) * 32u;
-        const uint64_t ad = sdesc_sw128(sbase + kSmemQ + ((uint32_t)w * 2 + half) * kHalfBytes + koff, 16, 1024);
-        const uint64_t bd = sdesc_sw128(sbase + kSmemK + (uint32_t)stage * kTileBytes + half * kHalfBytes + koff, 16, 1024);
+        const uint64_t ad = sdesc_at(dsc.q, ((uint32_t)w * 2 + half) * kHalfBytes + koff, kDescHi);
+        const uint64_t bd = sdesc_at(kb, half * kHalfBytes + koff, kDescHi);
         mma_ss(tmem + kColS0 + (uint32_t)w * 128, ad, bd, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t sbase, uint32_t tmem, int w, int stage, bool accumulate)
+__device__ __forceinline__ void issue_pv(const FwdDesc& dsc, uint32_t tmem, int w, int stage, bool accumulate)
 {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, true);
+    const uint32_t vb = dsc.v + (uint32_t)stage * (kTileBytes >> 4);
+    const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t bd = sdesc_sw128(sbase + kSmemV + (uint32_t)stage * kTileBytes + (uint32_t)kk * 2048u, kHalfBytes, 1024);
+        const uint64_t bd = sdesc_at(vb, (uint32_t)kk * 2048u, kDescHi);
         mma_ts(tmem + kColO0 + (uint32_t)w * 128, tmem + kColS0 + (uint32_t)w * 128 + (uint32_t)kk * 8, bd, idesc,
-               (accumulate || kk > 0) ? 1u : 0u);
+               kk > 0 ? 1u : acc0);
     }
 }
 
@@ -515,6 +525,10 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
     cur.item = blockIdx.x;
     cur.member = -1;
     bool issued = false;
+    FwdDesc dsc;
+    dsc.q = sdesc_sw128_lo(sbase + kSmemQ, 16);
+    dsc.k = sdesc_sw128_lo(sbase + kSmemK, 16);
+    dsc.v = sdesc_sw128_lo(sbase + kSmemV, kHalfBytes);
     if (cur.advance(a)) {
         issued = true;
         uint32_t kc = 0, tc = 0, qc = 0;
@@ -523,9 +537,9 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
         if (!mbar_wait(bar(BAR_Q_FULL), qc & 1, ctl)) goto drain;
         if (!mbar_wait(bar(BAR_K_FULL + 0), 0, ctl)) goto drain;
         tc_fence_after_sync();
-        issue_qk(sbase, tmem, 0, 0);
+        issue_qk(dsc, tmem, 0, 0);
         tc_commit(bar(BAR_S_FULL + 0));
-        issue_qk(sbase, tmem, 1, 0);
+        issue_qk(dsc, tmem, 1, 0);
         tc_commit(bar(BAR_S_FULL + 1));
         tc_commit(bar(BAR_K_EMPTY + 0));
         if (cur.u.ntiles == 1) tc_commit(bar(BAR_Q_EMPTY));
@@ -547,7 +561,7 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
             if (!mbar_wait(bar(BAR_V_FULL + stage), use & 1, ctl)) goto drain;
             if (!mbar_wait(bar(BAR_P_FULL + 0), tc & 1, ctl)) goto drain;
             tc_fence_after_sync();
-            issue_pv(sbase, tmem, 0, stage, jj > 0);
+            issue_pv(dsc, tmem, 0, stage, jj > 0);
             tc_commit(bar(BAR_O_DONE + 0));
             if (has_next) {
                 if (jn == 0) {
@@ -556,16 +570,16 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
                 }
                 if (!mbar_wait(bar(BAR_K_FULL + nstage), nuse & 1, ctl)) goto drain;
                 tc_fence_after_sync();
-                issue_qk(sbase, tmem, 0, nstage);
+                issue_qk(dsc, tmem, 0, nstage);
                 tc_commit(bar(BAR_S_FULL + 0));
             }
             if (!mbar_wait(bar(BAR_P_FULL + 1), tc & 1, ctl)) goto drain;
             tc_fence_after_sync();
-            issue_pv(sbase, tmem, 1, stage, jj > 0);
+            issue_pv(dsc, tmem, 1, stage, jj > 0);
             tc_commit(bar(BAR_O_DONE + 1));
             tc_commit(bar(BAR_V_EMPTY + stage));
             if (!has_next) break;
-            issue_qk(sbase, tmem, 1, nstage);
+            issue_qk(dsc, tmem, 1, nstage);
             tc_commit(bar(BAR_S_FULL + 1));
             tc_commit(bar(BAR_K_EMPTY + nstage));
             if (jn == nxt.u.ntiles - 1) tc_commit(bar(BAR_Q_EMPTY));

@@ -282,6 +282,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// The same descriptor as two 32-bit words, for the MMA issue loops: the low word holds the start
+// address (>> 4) and LBO, the high word SBO, the version and the layout -- a compile-time constant.
+// Moving the start address by a byte offset (a multiple of 16) adds offset >> 4 to the low word;
+// shared-memory addresses stay below 2^18, so nothing carries into LBO.  Every k-step of an
+// operand then costs one 32-bit add instead of rebuilding the 64-bit word.
+__device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo)
+{
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo)
+{
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint64_t sdesc_at(uint32_t lo, uint32_t byte_off, uint32_t hi)
+{
+    return ((uint64_t)hi << 32) | (uint64_t)(lo + (byte_off >> 4));
+}
+
 // 32 lanes x 32 consecutive 32-bit columns per warp; the warp's lane quarter is fixed by its
 // index within its warpgroup (lanes 32*(warp%4) .. +31).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
