@@ -77,6 +77,7 @@ typedef int ra_status;
 
 /* Device status bits (ring_attn_device_status). */
 #define RA_DEVICE_TIMEOUT 1u  /* a bounded wait inside a kernel ran out; the kernel stopped */
+#define RA_DEVICE_LAYOUT 2u   /* a kernel found its shared memory misaligned and did nothing */
 
 /*
  * ring_attn_fwd -- the whole ring forward in one launch.
@@ -214,7 +215,7 @@ RA_API ra_status ring_attn_shard_tiles(int L, int n_shards, int causal, int layo
  * count the work the tensor-core kernels do: for every tile pair a kernel computes, 1 is added to
  * visits[i * n_shards + j], i the shard of the query rows and j the shard of the key rows
  * (forward: a 256-row query block of one query head against a 128-row K/V tile; backward: a
- * 64-row query tile of one query head against a 128-row K/V tile).  The causal skip of M4-051
+ * 128-row query tile of one query head against a 128-row K/V tile).  The causal skip of M4-051
  * section 3 shows as visits[i][j] == 0 for every key shard whose positions all follow the query
  * shard's, and a computed pair always holds at least one visible (query, key) pair.
  *   visits: DEVICE array of n_shards * n_shards unsigned 64-bit counters, 16-byte aligned, added

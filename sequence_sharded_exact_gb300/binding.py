@@ -19,6 +19,7 @@ RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_NO_DEVICE, RA
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "striped": 2}
 PATHS = {1: "simt", 2: "tcgen05"}
 RA_DEVICE_TIMEOUT = 1
+RA_DEVICE_LAYOUT = 2
 
 _lock = threading.Lock()
 _lib = None

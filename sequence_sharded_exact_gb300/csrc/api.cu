@@ -13,6 +13,9 @@
 #include "../../include/ringattn.h"
 #include "ra_internal.h"
 
+static_assert(ra::kStatusTimeout == RA_DEVICE_TIMEOUT && ra::kStatusLayout == RA_DEVICE_LAYOUT,
+              "device status bits agree with the ABI");
+
 namespace ra {
 namespace {
 

@@ -19,6 +19,9 @@ struct Problem {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// bits of the device status word (the ABI's RA_DEVICE_* values; api.cu checks they agree)
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusLayout = 2u;
 
 // Output mode of a forward kernel.
 enum FwdMode {

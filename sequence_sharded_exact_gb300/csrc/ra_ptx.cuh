@@ -141,7 +141,7 @@ static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t par
             if (*ctl.abort) return false;
             if (global_timer_ns() - t0 > ctl.limit_ns) {
                 *ctl.abort = 1;
-                atomicOr(ctl.status, 1u);
+                atomicOr(ctl.status, kStatusTimeout);
                 return false;
             }
         }

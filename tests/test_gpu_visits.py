@@ -77,7 +77,7 @@ def test_backward_visits_exactly_the_visible_tiles(B, H, Hkv, L, n, causal, layo
     dq, dk, dv, visits = ra.bwd_tile_visits(q, k, v, out, lse, do, n, causal, layout)
     ref = ra.bwd(q, k, v, out, lse, do, n, causal, layout)
     torch.cuda.synchronize()
-    exp = expected_visits(B, H, L, n, causal, layout, q_tile=64)
+    exp = expected_visits(B, H, L, n, causal, layout, q_tile=128)
     assert np.array_equal(visits.cpu().numpy(), exp)
     for g, r, name in zip((dq, dk, dv), ref, ("dq", "dk", "dv")):
         assert_close(to_np(g), to_np(r), torch.float32, name, max_abs=1e-4)
