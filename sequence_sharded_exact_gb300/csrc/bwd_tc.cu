@@ -18,20 +18,20 @@
 //   * warp 12: TMA loads of the unit's K and V tiles and, through 2 stages, of each query tile's Q
 //     (with its lse) and dO (with its D); the vectors come by bulk copy into shared memory.
 //   * warp 13: tcgen05.mma issue, per query tile t, in this order:
-//       dV += P^T_t dO_t (P^T from TMEM), S^T_{t+1} = K Q_{t+1}^T, dK += dS^T_t Q_t (dS^T from
-//       TMEM), dQ^T_t = K^T dS^T_t (dS^T from shared memory), dP^T_{t+1} = V dO_{t+1}^T.
-//     S^T of the next tile runs while the math warps compute dS^T of this one.
+//       dV += P^T_t dO_t (P^T from TMEM), S^T_{t+1} = K Q_{t+1}^T, dQ^T_t = K^T dS^T_t,
+//       dK += dS^T_t Q_t (dS^T from shared memory for both), dP^T_{t+1} = V dO_{t+1}^T.
+//     S^T of the next tile runs while the math warps compute dS^T of this one; dQ^T goes before
+//     dK so that its read-out (which frees the columns of the next dP^T) overlaps dK.
 //   * warps 0-7 (two warpgroups, each owning 64 of the 128 query columns; thread = key row), per
 //     query tile t:
 //       phase A: P^T_t = 2^(S^T c - lse2) -> registers and, as bf16, TMEM (A operand of dV);
-//       phase B: dS^T_t = P^T_t (dP^T_t - D) / sqrt(d) -> shared memory (B operand of dQ^T) and,
-//         as bf16, TMEM (A operand of dK);
+//       phase B: dS^T_t = P^T_t (dP^T_t - D) / sqrt(d) -> shared memory (operand of dK and dQ^T);
 //     at the end of a unit, the dK, dV write-out.
 //   * warps 8-11 (thread = head-dim index): read dQ^T_t out of TMEM, free its columns and add it
 //     into the float32 accumulator in global memory with coalesced reductions (one warp
 //     instruction covers 32 consecutive head-dim entries of one query row).
-//   * TMEM columns: X = [0,128) S^T then P^T; Y = [128,256) dP^T, then dS^T, then dQ^T once dK has
-//     read dS^T; dK [256,384), dV [384,512).
+//   * TMEM columns: X = [0,128) S^T then P^T; Y = [128,256) dP^T, then dQ^T once phase B has read
+//     dP^T; dK [256,384), dV [384,512).
 //   * every wait is bounded; a wait that runs out sets the device status word and the CTA stops.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -285,10 +285,10 @@ __device__ __forceinline__ void phase_a(const BwdArgs& a, uint32_t tmem, uint32_
     tmem_st_wait();
 }
 
-// Phase B: dS^T = P^T (dP^T - D) / sqrt(d) for the warpgroup's query columns, in two halves of 32:
-// -> 128-byte-swizzled shared memory (query block w: key row r, its 128-byte row; the B operand of
-// dQ^T) and, as bf16 pairs, TMEM columns [64w, 64w+32) of Y (the A operand of dK).  Each half's
-// bf16 pairs land on dP^T columns of the first half, already read.
+// Phase B: dS^T = P^T (dP^T - D) / sqrt(d) for the warpgroup's query columns, in two halves of 32,
+// -> 128-byte-swizzled shared memory (query block w: key row r, its 128-byte row), where it is
+// both the A operand of dK (K-major: key rows, query columns contiguous) and the B operand of
+// dQ^T (N-major).
 __device__ __forceinline__ void phase_b(const BwdArgs& a, uint32_t sbase, uint32_t tmem, uint32_t lane_off, int w,
                                         int r, uint32_t s_d, const float (&p)[64])
 {
@@ -320,9 +320,7 @@ __device__ __forceinline__ void phase_b(const BwdArgs& a, uint32_t sbase, uint32
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128(region, r, hf * 4 + j)),
                          "r"(dsp[4 * j]), "r"(dsp[4 * j + 1]), "r"(dsp[4 * j + 2]), "r"(dsp[4 * j + 3])
                          : "memory");
-        tmem_st_32x32b_x16(ty + (uint32_t)hf * 16, dsp);
     }
-    tmem_st_wait();
 }
 
 // Per query tile t the warpgroups run phase A then phase B; dQ^T is the dQ warps' business.
@@ -567,10 +565,11 @@ struct BwdDesc {
     uint32_t q_k, do_k;   // Q and dO tiles, K-major (B of S^T and dP^T)
     uint32_t q_n, do_n;   // Q and dO tiles, N-major (B of dK and dV)
     uint32_t ds_n;        // dS^T, N-major (B of dQ^T)
+    uint32_t ds_k;        // dS^T, K-major (A of dK)
 };
 constexpr uint32_t kDescHi = sdesc_sw128_hi(1024);
 constexpr uint32_t kId = idesc_bf16_f32(128, 128, false, false);     // S^T, dP^T: both K-major
-constexpr uint32_t kIdTs = idesc_bf16_f32(128, 128, false, true);    // dV, dK: A TMEM, B N-major
+constexpr uint32_t kIdTs = idesc_bf16_f32(128, 128, false, true);    // dV (A TMEM), dK (A K-major): B N-major
 constexpr uint32_t kIdDQ = idesc_bf16_f32(128, 128, true, true);     // dQ^T: A M-major, B N-major
 
 __device__ __forceinline__ BwdDesc make_desc(uint32_t sbase)
@@ -584,6 +583,7 @@ __device__ __forceinline__ BwdDesc make_desc(uint32_t sbase)
     d.q_n = sdesc_sw128_lo(sbase + kSmemQ, kHalf);
     d.do_n = sdesc_sw128_lo(sbase + kSmemDO, kHalf);
     d.ds_n = sdesc_sw128_lo(sbase + kSmemDS, kHalf);
+    d.ds_k = sdesc_sw128_lo(sbase + kSmemDS, 16);
     return d;
 }
 
@@ -613,7 +613,7 @@ __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_lo, uin
 }
 
 // acc (tmem) += A (tmem, bf16 pairs) B over the 128 query rows, B N-major in shared memory
-// (dV += P^T dO, dK += dS^T Q)
+// (dV += P^T dO)
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, bool accumulate)
 {
     const uint32_t acc0 = accumulate ? 1u : 0u;
@@ -621,6 +621,18 @@ __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint3
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
         mma_ts(d_tmem, a_tmem + a_col(kk), sdesc_at(b_lo, (uint32_t)kk * 2048u, kDescHi), kIdTs, kk > 0 ? 1u : acc0);
+}
+
+// dK += dS^T Q over the 128 query rows: A = dS^T K-major (query block kk / 4, 16 queries = 32 bytes
+// of each 128-byte key row), B = Q N-major
+__device__ __forceinline__ void issue_dk(uint32_t tmem, const BwdDesc& dsc, uint32_t q_lo, bool accumulate)
+{
+    const uint32_t a_lo = opaque(dsc.ds_k), b_lo = opaque(q_lo);
+    const uint32_t acc0 = accumulate ? 1u : 0u;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + kColDK, sdesc_at(a_lo, (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u, kDescHi),
+               sdesc_at(b_lo, (uint32_t)kk * 2048u, kDescHi), kIdTs, kk > 0 ? 1u : acc0);
 }
 
 // dQ^T = K^T dS^T over the 128 key rows
@@ -678,13 +690,13 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
                     issue_kmajor(tmem + kColX, dsc.k_k, dsc.q_k + nst * kStageLo);
                     tc_commit(bar(BAR_ST_FULL));
                 }
-                // dK += dS^T Q (dS^T in Y), then dQ^T = K^T dS^T into Y once dK has read it
+                // dQ^T = K^T dS^T into Y (phase B has read dP^T out of it), then dK += dS^T Q
                 if (!mbar_wait(bar(BAR_DS_READY), gt & 1, ctl)) goto drain;
                 tc_fence_after_sync();
-                issue_ts(tmem + kColDK, tmem + kColY, dsc.q_n + st * kStageLo, t > 0);
-                tc_commit(bar(BAR_Q_EMPTY + (int)st));
                 issue_dq(tmem, dsc);
                 tc_commit(bar(BAR_DQ_FULL));
+                issue_dk(tmem, dsc, dsc.q_n + st * kStageLo, t > 0);
+                tc_commit(bar(BAR_Q_EMPTY + (int)st));
                 // next dP^T into Y, once dQ^T has been read out of it
                 if (more) {
                     if (!mbar_wait(bar(BAR_DQ_FREE), gt & 1, ctl)) goto drain;
