@@ -38,7 +38,7 @@ METRIC = "ring-attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor p
 # DRAM bytes (read + write) per launch of the dominant kernel, from ncu captures summarised in
 # profiles/ (the 32K capture scaled to 128K by rows: each Q/K/V/O byte moves once).  Update or drop
 # an entry whenever that kernel changes.
-TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4 * 649.4e6, ("zigzag_gqa_32k", "fwd"): 649.4e6}
+TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4 * 646.6e6, ("zigzag_gqa_32k", "fwd"): 646.6e6}
 
 
 def fwd_flops(B, H, L, d, causal):
