@@ -29,7 +29,8 @@
 //     at the end of a unit, the dK, dV write-out.
 //   * warps 8-11 (thread = head-dim index): read dQ^T_t out of TMEM, free its columns and add it
 //     into the float32 accumulator in global memory with coalesced reductions (one warp
-//     instruction covers 32 consecutive head-dim entries of one query row).
+//     instruction covers 32 consecutive head-dim entries of one query row), paced so that they do
+//     not crowd the other warps' shared-memory traffic out of the memory-instruction queue.
 //   * TMEM columns: X = [0,128) S^T then P^T; Y = [128,256) dP^T, then dQ^T once phase B has read
 //     dP^T; dK [256,384), dV [384,512).
 //   * every wait is bounded; a wait that runs out sets the device status word and the CTA stops.
