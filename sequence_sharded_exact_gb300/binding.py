@@ -276,7 +276,8 @@ def lse_merge(o_acc, lse_acc, o_part, lse_part, stream=None):
 
 def fwd_stepwise(q, k, v, n_shards, causal=True, layout="zigzag", out=None, lse=None,
                  workspace=None, stream=None):
-    """The ring forward run as n ring-step launches plus LSE merges (same results as fwd)."""
+    """The ring forward run as n ring-step launches, each folding its block into the running
+    result (same results as fwd)."""
     B, H, Hkv, L, d = _dims(q, k)
     if out is None:
         out = torch.empty_like(q)

@@ -120,6 +120,23 @@ def test_stepwise_ring_matches_oracle_and_fused(B, H, Hkv, L, d, n, layout, dtyp
 
 
 @pytest.mark.parametrize("B,H,Hkv,L,d,n,layout,dtype", [
+    (1, 4, 2, 1024, 128, 4, "zigzag", torch.bfloat16),       # tensor-core ring steps
+    (2, 2, 1, 768, 128, 3, "striped", torch.bfloat16),
+    (1, 2, 1, 600, 64, 3, "contiguous", torch.float32),      # CUDA-core ring steps
+])
+def test_stepwise_non_causal_matches_oracle(B, H, Hkv, L, d, n, layout, dtype):
+    """Without the causal mask every ring step sees the whole K/V shard: the folded steps equal full
+    (unmasked) attention."""
+    x = inputs(B, H, Hkv, L, d, dtype, seed=81)
+    q, k, v = (x[t].to(DEV) for t in ("q", "k", "v"))
+    out_s, lse_s = ra.fwd_stepwise(q, k, v, n, False, layout)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attn_fwd(x["q"], x["k"], x["v"], n, False, layout)
+    assert_close(to_np(out_s), ref_o, dtype, "stepwise out")
+    assert_close(to_np(lse_s), ref_l, dtype, "stepwise lse")
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,d,n,layout,dtype", [
     (1, 4, 2, 1024, 128, 4, "zigzag", torch.bfloat16),
     (1, 2, 1, 600, 64, 3, "striped", torch.float32),
 ])
