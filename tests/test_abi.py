@@ -172,6 +172,16 @@ def test_ulysses_head_divisibility_and_workspace(lib):
     B, H, Hkv, L, d = 1, 32, 8, 131072, 128
     want = 2 * B * H * L * d * 2 + 2 * B * Hkv * L * d * 2 + B * H * L * 4
     assert binding.library().ring_attn_ulysses_workspace_size(B, H, Hkv, L, d, 1) == want
+    # backward: head-split q, out, dout, k, v, lse, dq, dk, dv, plus the inner backward's workspace
+    # for n problems of H/n query heads (float32 gradients here)
+    n = 8
+    lib = binding.library()
+    inner = lib.ring_attn_bwd_workspace_size(n * B, H // n, Hkv // n, L, d, 0)
+    want_b = (3 * B * H * L * d * 2 + 2 * B * Hkv * L * d * 2 + B * H * L * 4 + B * H * L * d * 4
+              + 2 * B * Hkv * L * d * 4 + inner)
+    got_b = lib.ring_attn_ulysses_bwd_workspace_size(B, H, Hkv, L, d, n, 1, 0)
+    assert want_b <= got_b <= want_b + 10 * 256
+    assert lib.ring_attn_ulysses_bwd_workspace_size(B, 12, Hkv, L, d, n, 1, 0) == 0  # 12 heads over 8
 
 
 def test_fwd_host_argument_errors(lib):
