@@ -145,9 +145,11 @@ RA_API size_t ring_attn_fwd_stepwise_workspace_size(int B, int H, int L, int d);
  * ring_attn_fwd_host -- ring_attn_fwd on HOST buffers: q, k, v are read from host memory and out,
  * lse written back to host memory, with the copies overlapped with the compute.  The problem is
  * cut into its B * Hkv kv-head groups (each group: the G = H / Hkv query heads that share a kv
- * head); while group g runs on `stream`, the inputs of group g + 1 are copied in and the results of
- * group g - 1 copied out on two copy streams of the library (one H2D, one D2H), through two device
- * slots of the workspace.  Each copy is one cudaMemcpyAsync of a contiguous slice.
+ * head); while group g computes, the inputs of group g + 1 are copied in and the results of group
+ * g - 1 copied out on two copy streams of the library (one H2D, one D2H), through two device slots
+ * of the workspace.  The groups' kernels alternate between two compute streams of the library, so
+ * that one group's kernel starts on the SMs the previous one's last CTAs leave.  Each copy is one
+ * cudaMemcpyAsync of a contiguous slice.
  *   q, k, v, out, lse: HOST pointers with the layouts of ring_attn_fwd; page-locked memory lets the
  *   copies run asynchronously and overlap (pageable memory works but serialises them).
  *   workspace: DEVICE, 256-byte aligned, >= ring_attn_fwd_host_workspace_size(H, Hkv, L, d, dtype).

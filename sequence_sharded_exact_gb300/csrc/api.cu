@@ -589,6 +589,7 @@ namespace {
 struct HostPipe {
     bool ready = false;
     cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaStream_t comp[2] = {};  // the groups' kernels alternate between two streams (see below)
     cudaEvent_t entry = nullptr, in_done[2] = {}, compute_done[2] = {}, out_done[2] = {};
     std::mutex mu;  // one host-buffer forward enqueues at a time per device (the events are shared)
 };
@@ -599,6 +600,7 @@ cudaError_t host_pipe_init(HostPipe& hp)
     if (hp.ready) return cudaSuccess;
     cudaError_t e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&hp.comp[i], cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.entry, cudaEventDisableTiming);
     for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
         e = cudaEventCreateWithFlags(&hp.in_done[i], cudaEventDisableTiming);
@@ -653,6 +655,7 @@ ra_status ring_attn_fwd_host(const void* q, const void* k, const void* v, void* 
     // earlier work on the caller's stream (a previous call using this workspace) comes first
     e = cudaEventRecord(hp.entry, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.h2d, hp.entry, 0);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(hp.comp[i], hp.entry, 0);
     const int groups = B * Hkv;
     for (int gi = 0; gi < groups && e == cudaSuccess; ++gi) {
         const int sl = gi & 1;
@@ -671,12 +674,15 @@ ra_status ring_attn_fwd_host(const void* q, const void* k, const void* v, void* 
         if (e == cudaSuccess) e = cudaMemcpyAsync(dv, static_cast<const char*>(v) + (size_t)gi * kbytes, kbytes,
                                                   cudaMemcpyHostToDevice, hp.h2d);
         if (e == cudaSuccess) e = cudaEventRecord(hp.in_done[sl], hp.h2d);
-        // the group's attention on the caller's stream
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp.in_done[sl], 0);
+        // the group's attention, on the compute stream of its slot: consecutive groups' kernels sit
+        // on different streams, so the next one's CTAs take the SMs that the previous one's last
+        // CTAs leave (one persistent CTA per SM cannot keep every SM busy to the end)
+        cudaStream_t cs = hp.comp[sl];
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, hp.in_done[sl], 0);
         if (e == cudaSuccess)
-            e = tc ? launch_fwd_tc(pg, dq, dk, dv, dout, dl, kFwdFused, 0, sw, s)
-                   : launch_fwd_simt(pg, dq, dk, dv, dout, dl, kFwdFused, 0, s);
-        if (e == cudaSuccess) e = cudaEventRecord(hp.compute_done[sl], s);
+            e = tc ? launch_fwd_tc(pg, dq, dk, dv, dout, dl, kFwdFused, 0, sw, cs)
+                   : launch_fwd_simt(pg, dq, dk, dv, dout, dl, kFwdFused, 0, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(hp.compute_done[sl], cs);
         // and its results back
         if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.d2h, hp.compute_done[sl], 0);
         if (e == cudaSuccess) e = cudaMemcpyAsync(static_cast<char*>(out) + (size_t)gi * qbytes, dout, qbytes,
