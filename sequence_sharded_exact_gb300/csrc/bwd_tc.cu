@@ -169,6 +169,26 @@ __device__ __forceinline__ bool unit_of(const BwdArgs& a, long long item, int me
     return true;
 }
 
+// The CTA's sequence of units: whole mirrored pairs while every CTA gets one (items c, c + G, ...,
+// G = gridDim.x, c = blockIdx.x), then the pairs left over (fewer than G) split into their two
+// tiles, dealt one tile per CTA: the last round then costs about half a pair instead of a whole
+// one on some CTAs while the others idle (64K training: 2048 pairs = 13 rounds of 152 + 72).
+// Slot 2r + m is member m of round r's pair; slots from 2R on hold the split tiles.
+__device__ __forceinline__ int unit_slots(const BwdArgs& a)
+{
+    const long long G = gridDim.x, R = a.items / G, rem = a.items - R * G;
+    return (int)(2 * R + (2 * rem + G - 1) / G);
+}
+
+__device__ __forceinline__ bool unit_in_slot(const BwdArgs& a, int s, KvUnit& u)
+{
+    const long long G = gridDim.x, c = blockIdx.x, R = a.items / G;
+    if (s < 2 * R) return unit_of(a, (long long)(s >> 1) * G + c, s & 1, u);
+    const long long tu = c + (long long)(s - 2 * R) * G;  // tile index among the leftover pairs
+    if (tu >= 2 * (a.items - R * G)) return false;
+    return unit_of(a, R * G + (tu >> 1), (int)(tu & 1), u);
+}
+
 // Query tiles of a unit: heads of the group in turn, each walking the query shards in ring order.
 struct QWalk {
     Geometry geo;
@@ -333,10 +353,11 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     auto bar = [&](int i) { return sbase + kSmemBar + 8u * (uint32_t)i; };
     uint32_t gt = 0, uc = 0;
-    for (long long item = blockIdx.x; item < a.items; item += gridDim.x) {
-        for (int member = 0; member < 2; ++member) {
+    const int slots = unit_slots(a);
+    for (int slot = 0; slot < slots; ++slot) {
+        {
             KvUnit u;
-            if (!unit_of(a, item, member, u) || u.ntiles == 0) continue;
+            if (!unit_in_slot(a, slot, u) || u.ntiles == 0) continue;
             QWalk walk;
             walk.begin(a, u);
             for (int t = 0; t < u.ntiles; ++t, ++gt) {
@@ -453,10 +474,11 @@ __device__ __forceinline__ void dq_role(const BwdArgs& a, uint32_t sbase, uint32
     const uint32_t ty = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kColY;
     auto bar = [&](int i) { return sbase + kSmemBar + 8u * (uint32_t)i; };
     uint32_t gt = 0;
-    for (long long item = blockIdx.x; item < a.items; item += gridDim.x) {
-        for (int member = 0; member < 2; ++member) {
+    const int slots = unit_slots(a);
+    for (int slot = 0; slot < slots; ++slot) {
+        {
             KvUnit u;
-            if (!unit_of(a, item, member, u) || u.ntiles == 0) continue;
+            if (!unit_in_slot(a, slot, u) || u.ntiles == 0) continue;
             QWalk walk;
             walk.begin(a, u);
             for (int t = 0; t < u.ntiles; ++t, ++gt) {
@@ -505,10 +527,11 @@ __device__ __forceinline__ void producer_role(const BwdArgs& a, uint32_t sbase, 
     tma_prefetch_desc(tmDO);
     uint32_t uc = 0, qc = 0;
     bool ok = true;
-    for (long long item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
-        for (int member = 0; ok && member < 2; ++member) {
+    const int slots = unit_slots(a);
+    for (int slot = 0; ok && slot < slots; ++slot) {
+        {
             KvUnit u;
-            if (!unit_of(a, item, member, u) || u.ntiles == 0) continue;
+            if (!unit_in_slot(a, slot, u) || u.ntiles == 0) continue;
             if (uc > 0 && !mbar_wait(bar(BAR_KV_EMPTY), (uc - 1) & 1, ctl)) { ok = false; break; }
             const int zkv = u.b * a.Hkv + u.g;
             mbar_arrive_expect_tx(bar(BAR_KV_FULL), 2 * kTileBytes);
@@ -653,10 +676,11 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
     uint32_t gt = 0, uc = 0;
     bool issued = false;
     const BwdDesc dsc = make_desc(sbase);
-    for (long long item = blockIdx.x; item < a.items; item += gridDim.x) {
-        for (int member = 0; member < 2; ++member) {
+    const int slots = unit_slots(a);
+    for (int slot = 0; slot < slots; ++slot) {
+        {
             KvUnit u;
-            if (!unit_of(a, item, member, u) || u.ntiles == 0) continue;
+            if (!unit_in_slot(a, slot, u) || u.ntiles == 0) continue;
             if (!mbar_wait(bar(BAR_KV_FULL), uc & 1, ctl)) goto drain;
             issued = true;
             tc_fence_after_sync();
