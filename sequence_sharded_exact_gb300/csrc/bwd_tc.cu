@@ -12,7 +12,8 @@
 // so a K/V tile walks the query shards in that order.
 //
 // Design (one CTA per SM, persistent; a work unit is one 128-row K/V tile of one kv head, units in
-// mirrored pairs so that causal work is equal across CTAs; the unit walks 128-row query tiles, so
+// mirrored pairs so that causal work is equal across CTAs, the leftover pairs of the last round
+// split into single tiles; the unit walks 128-row query tiles, so
 // that every product is a 128 x 128 x 128 one -- an N = 64 instruction costs nearly as long as an
 // N = 128 one on this tensor core):
 //   * warp 12: TMA loads of the unit's K and V tiles and, through 2 stages, of each query tile's Q
