@@ -170,22 +170,33 @@ __device__ __forceinline__ bool unit_of(const BwdArgs& a, long long item, int me
     return true;
 }
 
-// The CTA's sequence of units: whole mirrored pairs while every CTA gets one (items c, c + G, ...,
-// G = gridDim.x, c = blockIdx.x), then the pairs left over (fewer than G) split into their two
-// tiles, dealt one tile per CTA: the last round then costs about half a pair instead of a whole
+// The CTA's sequence of units: mirrored pairs, items c, c + G, ... (G = gridDim.x, c = blockIdx.x).
+// When the pairs left for the last round fill at most half the CTAs, they are split into their two
+// tiles instead, one tile per CTA: the last round then costs about half a pair instead of a whole
 // one on some CTAs while the others idle (64K training: 2048 pairs = 13 rounds of 152 + 72).
-// Slot 2r + m is member m of round r's pair; slots from 2R on hold the split tiles.
+// Slot 2r + m is member m of round r's pair; the one slot after them holds a split tile.
+__device__ __forceinline__ bool split_last_round(const BwdArgs& a)
+{
+    const long long G = gridDim.x, rem = a.items % G;
+    return rem > 0 && 2 * rem <= G;
+}
+
 __device__ __forceinline__ int unit_slots(const BwdArgs& a)
 {
-    const long long G = gridDim.x, R = a.items / G, rem = a.items - R * G;
-    return (int)(2 * R + (2 * rem + G - 1) / G);
+    const long long G = gridDim.x;
+    const long long pair_rounds = split_last_round(a) ? a.items / G : (a.items + G - 1) / G;
+    return (int)(2 * pair_rounds + (split_last_round(a) ? 1 : 0));
 }
 
 __device__ __forceinline__ bool unit_in_slot(const BwdArgs& a, int s, KvUnit& u)
 {
     const long long G = gridDim.x, c = blockIdx.x, R = a.items / G;
-    if (s < 2 * R) return unit_of(a, (long long)(s >> 1) * G + c, s & 1, u);
-    const long long tu = c + (long long)(s - 2 * R) * G;  // tile index among the leftover pairs
+    const bool split = split_last_round(a);
+    if (!split || s < 2 * R) {
+        const long long item = (long long)(s >> 1) * G + c;
+        return item < a.items && unit_of(a, item, s & 1, u);
+    }
+    const long long tu = c;  // tile index among the leftover pairs (one slot: 2 rem <= G)
     if (tu >= 2 * (a.items - R * G)) return false;
     return unit_of(a, R * G + (tu >> 1), (int)(tu & 1), u);
 }
