@@ -288,11 +288,9 @@ __device__ __forceinline__ void phase_a(const BwdArgs& a, uint32_t tmem, uint32_
                                         uint32_t s_lse, float (&p)[64])
 {
     const uint32_t tx = tmem + lane_off + kColX + (uint32_t)w * 64;
-    uint32_t s0[32], s1[32];
-    tmem_ld_32x32b_x32(tx, s0);
-    tmem_ld_32x32b_x32(tx + 32, s1);
-    tmem_ld_wait(s0);
-    tmem_ld_wait(s1);
+    uint32_t sv[64];
+    tmem_ld_32x32b_x64(tx, sv);
+    tmem_ld_wait(sv);
     uint32_t pk[32];
     const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
     const float2 nl2e = make_float2(-kLog2e, -kLog2e);
@@ -302,8 +300,8 @@ __device__ __forceinline__ void phase_a(const BwdArgs& a, uint32_t tmem, uint32_
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = e4 * 4 + h * 2;
-            const uint32_t x0 = col < 32 ? s0[col] : s1[col - 32];
-            const uint32_t x1 = col < 32 ? s0[col + 1] : s1[col - 31];
+            const uint32_t x0 = sv[col];
+            const uint32_t x1 = sv[col + 1];
             const float2 lq = h == 0 ? make_float2(l4.x, l4.y) : make_float2(l4.z, l4.w);
             const float2 xv = fma2(make_float2(__uint_as_float(x0), __uint_as_float(x1)), sc2, mul2(lq, nl2e));
             float p0 = ex2_approx(xv.x), p1 = ex2_approx(xv.y);
@@ -469,10 +467,10 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v)
 // The pauses (1.6 us per tile) stay well inside a tile period (~2.3 us; at 140 ns the reductions
 // fell behind and the backward took 99 ms), and a tile whose successor is already waiting goes
 // out without pauses.
-__device__ __forceinline__ void red_group(float* dst, const uint32_t (&x)[32], int c0, uint32_t gap_ns)
+__device__ __forceinline__ void red_group(float* dst, const uint32_t (&x)[64], int c0, uint32_t gap_ns)
 {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < 8; ++g) {
         if (gap_ns) __nanosleep(gap_ns);
 #pragma unroll
         for (int c = 0; c < 8; ++c) red_add_f32(dst + (long long)(c0 + 8 * g + c) * kHd, __uint_as_float(x[8 * g + c]));
@@ -502,24 +500,18 @@ __device__ __forceinline__ void dq_role(const BwdArgs& a, uint32_t sbase, uint32
                 if (!mbar_wait(bar(BAR_DQ_FULL), gt & 1, ctl)) return;
                 tc_fence_after_sync();
                 __syncwarp();
-                uint32_t x0[32], x1[32], x2[32], x3[32];
-                tmem_ld_32x32b_x32(ty, x0);
-                tmem_ld_32x32b_x32(ty + 32, x1);
-                tmem_ld_32x32b_x32(ty + 64, x2);
-                tmem_ld_32x32b_x32(ty + 96, x3);
-                tmem_ld_wait(x0);
-                tmem_ld_wait(x1);
-                tmem_ld_wait(x2);
-                tmem_ld_wait(x3);
+                uint32_t xa[64], xb[64];
+                tmem_ld_32x32b_x64(ty, xa);
+                tmem_ld_32x32b_x64(ty + 64, xb);
+                tmem_ld_wait(xa);
+                tmem_ld_wait(xb);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(BAR_DQ_FREE));
                 const int zq = u.b * a.H + u.g * a.G + hh;
                 float* dst = a.dq_acc + ((long long)zq * a.geo.L + qrow) * kHd + dcol;
-                red_group(dst, x0, 0, gap_ns);
-                red_group(dst, x1, 32, gap_ns);
-                red_group(dst, x2, 64, gap_ns);
-                red_group(dst, x3, 96, gap_ns);
+                red_group(dst, xa, 0, gap_ns);
+                red_group(dst, xb, 64, gap_ns);
             }
         }
     }
