@@ -273,6 +273,7 @@ def test_striped_ring_step_first_rows(d, L, dtype):
     (2, 4, 2, 2048, 128, 4, "zigzag", torch.bfloat16, True),   # tensor-core groups
     (1, 2, 1, 600, 64, 3, "striped", torch.float32, True),     # CUDA-core groups
     (1, 4, 4, 1024, 128, 2, "contiguous", torch.bfloat16, False),
+    (2, 8, 4, 2048, 128, 4, "striped", torch.bfloat16, True),   # 8 groups over 2 slots, 2 streams
 ])
 def test_fwd_host_equals_device_forward(B, H, Hkv, L, d, n, layout, dtype, pinned):
     """ring_attn_fwd_host (host buffers, per-group copies overlapped with compute) returns exactly
@@ -286,3 +287,23 @@ def test_fwd_host_equals_device_forward(B, H, Hkv, L, d, n, layout, dtype, pinne
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
     ref_o, ref_l = oracle.attn_fwd(x["q"], x["k"], x["v"], n, True, layout)
     assert_close(to_np(out_h), ref_o, dtype, "out")
+
+
+def test_fwd_host_back_to_back_calls_share_a_workspace():
+    """Two host-buffer forwards enqueued back to back on one stream with one workspace (no sync in
+    between): the second call's copies and kernels wait for the first call's, so each returns the
+    device forward of its own inputs."""
+    B, H, Hkv, L, d, n = 1, 8, 4, 2048, 128, 4
+    xa = inputs(B, H, Hkv, L, d, torch.bfloat16, seed=91)
+    xb = inputs(B, H, Hkv, L, d, torch.bfloat16, seed=92)
+    ha = [xa[t].pin_memory() for t in ("q", "k", "v")]
+    hb = [xb[t].pin_memory() for t in ("q", "k", "v")]
+    need = ra.library().ring_attn_fwd_host_workspace_size(H, Hkv, L, d, 1)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    out_a, lse_a = ra.fwd_host(*ha, n, True, "zigzag", workspace=ws)
+    out_b, lse_b = ra.fwd_host(*hb, n, True, "zigzag", workspace=ws)
+    torch.cuda.current_stream().synchronize()
+    for x, o, l in ((xa, out_a, lse_a), (xb, out_b, lse_b)):
+        od, ld = ra.fwd(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), n, True, "zigzag")
+        torch.cuda.synchronize()
+        assert torch.equal(o, od.cpu()) and torch.equal(l, ld.cpu())
