@@ -36,9 +36,12 @@ TRAIN_WORKLOAD = "zigzag_gqa_64k_train"
 METRIC = "ring-attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from ncu captures summarised in
-# profiles/ (the 32K capture scaled to 128K by rows: each Q/K/V/O byte moves once).  Update or drop
-# an entry whenever that kernel changes.
-TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4 * 646.6e6, ("zigzag_gqa_32k", "fwd"): 646.6e6}
+# profiles/ (forward: the 32K capture scaled to 128K by rows, each Q/K/V/O byte moving once;
+# backward: single-pass captures of the kernel itself at 32K and at 64K).  Update or drop an entry
+# whenever that kernel changes.
+TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4 * 646.6e6, ("zigzag_gqa_32k", "fwd"): 646.6e6,
+                 ("zigzag_gqa_64k_train", "train"): 7.57e9 + 4.06e9,
+                 ("zigzag_gqa_32k", "train"): 2.526e9 + 1.408e9}
 
 
 def fwd_flops(B, H, L, d, causal):
