@@ -27,3 +27,4 @@ from .binding import (  # noqa: F401
     ulysses_bwd,
     ulysses_fwd,
 )
+from .autograd import ring_attention  # noqa: F401
