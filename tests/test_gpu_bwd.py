@@ -51,6 +51,8 @@ TC_BWD_CASES = [
     (2, 2, 2, 512, 2, False, "striped"),
     (1, 8, 1, 1024, 2, True, "zigzag"),      # GQA 8:1
     (2, 4, 2, 1024, 4, True, "striped"),
+    (4, 10, 5, 2048, 4, True, "zigzag"),     # 160 mirrored pairs: the last round's 8 split into tiles
+    (3, 6, 3, 1536, 3, False, "contiguous"), # odd head and batch counts, non-causal
 ]
 
 
