@@ -307,7 +307,7 @@ def bwd(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigzag",
 
 def bwd_tile_visits(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigzag",
                     grad_dtype=torch.float32, stream=None):
-    """ring_attn_bwd_tile_visits: the backward plus the count of (64-row query tile, 128-row K/V
+    """ring_attn_bwd_tile_visits: the backward plus the count of (128-row query tile, 128-row K/V
     tile) pairs computed per (query shard, key shard).  Returns (dq, dk, dv, visits [n, n] int64)."""
     visits = _visits(n_shards, q.device)
     dq, dk, dv = _bwd(q, k, v, out, lse, dout, n_shards, causal, layout, grad_dtype, None, None,
