@@ -44,6 +44,25 @@ TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4 * 646.6e6, ("zigzag_gqa_32k", "fw
                  ("zigzag_gqa_32k", "train"): 2.526e9 + 1.408e9}
 
 
+def copy_bandwidth(host, device_t, stream):
+    """This box's pinned host <-> device copy rates (GB/s), one large copy each way on `stream`: the
+    end-to-end number depends on them (machines in the same pool have differed by 10x)."""
+    n = min(host.numel(), device_t.numel())
+    h, d = host.view(-1)[:n], device_t.view(-1)[:n]
+    nbytes = n * host.element_size()
+    rates = {}
+    for name, (dst, src) in (("h2d", (d, h)), ("d2h", (h, d))):
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b.record(stream)
+        b.synchronize()
+        rates[name] = round(nbytes / (a.elapsed_time(b) / 1e3) / 1e9, 1)
+    return rates
+
+
 def fwd_flops(B, H, L, d, causal):
     """Algorithmic forward flops: 4 B H L^2 d (QK^T and PV), halved when causal."""
     f = 4.0 * B * H * L * L * d
@@ -406,7 +425,7 @@ def main():
         d2h = sum(t.numel() * t.element_size() for t in h_out)
         line["e2e"] = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "what": what,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": e2e_ms}
+                       "ms_per_step": e2e_ms, "copy_GBps": copy_bandwidth(h_in[0], ins[0], stream)}
         if not train:
             # the results that came back match the device-resident forward of the timed region
             line["e2e"]["matches_device_forward"] = bool(torch.equal(h_out[0], out.cpu()) and
