@@ -461,12 +461,12 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v)
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
-// The reductions go out in 16 groups of 8 per thread with a 100 ns pause between groups: issued at
+// The reductions go out in 16 groups of 8 per thread with an 80 ns pause between groups: issued at
 // once they fill the SM's memory-instruction queue, and every other warp's shared-memory and
-// barrier traffic then waits behind them (64K training backward: 78.5 ms unpaced, ~73.5 paced).
-// The pauses (1.6 us per tile) stay well inside a tile period (~2.3 us; at 140 ns the reductions
-// fell behind and the backward took 99 ms), and a tile whose successor is already waiting goes
-// out without pauses.
+// barrier traffic then waits behind them (64K training backward: ~78 ms unpaced, ~71 paced).
+// Pauses of 80-115 ns per group all give the same time; from ~130 ns on, the reductions fall
+// behind the tiles (90 ms and worse), so 80 ns keeps a wide margin on boxes that run the tiles
+// faster.  A tile whose successor is already waiting goes out without pauses.
 __device__ __forceinline__ void red_group(float* dst, const uint32_t (&x)[64], int c0, uint32_t gap_ns)
 {
 #pragma unroll
@@ -496,7 +496,7 @@ __device__ __forceinline__ void dq_role(const BwdArgs& a, uint32_t sbase, uint32
                 walk.next(hh, qrow, qnat);
                 (void)qnat;
                 const bool behind = __shfl_sync(0xffffffffu, mbar_test_wait(bar(BAR_DQ_FULL), gt & 1), 0) != 0;
-                const uint32_t gap_ns = behind ? 0u : 100u;
+                const uint32_t gap_ns = behind ? 0u : 80u;
                 if (!mbar_wait(bar(BAR_DQ_FULL), gt & 1, ctl)) return;
                 tc_fence_after_sync();
                 __syncwarp();
