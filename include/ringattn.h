@@ -132,8 +132,9 @@ RA_API ra_status ring_attn_lse_merge(float* o_acc, float* lse_acc, const float* 
  * does it: n_shards launches, step 0 writing a float32 running output and lse and every later
  * step folding its block into them (ring_attn_ring_step_fwd_accumulate), then the conversion of
  * the float32 output into `out`.  Same arguments and results as ring_attn_fwd, plus
- *   workspace: device memory of at least ring_attn_fwd_stepwise_workspace_size(...) bytes,
- *   256-byte aligned, owned by the caller; its contents on entry do not matter.
+ *   workspace: device memory of at least ring_attn_fwd_stepwise_workspace_size(...) bytes (the
+ *   float32 running output, B * H * L * d * 4 bytes rounded up to 256), 256-byte aligned, owned by
+ *   the caller; its contents on entry do not matter.  The running lse is `lse` itself.
  */
 RA_API ra_status ring_attn_fwd_stepwise(const void* q, const void* k, const void* v, void* out,
                                  float* lse, int B, int H, int Hkv, int L, int d, int n_shards,
