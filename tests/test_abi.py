@@ -79,7 +79,9 @@ def test_path_selection():
     assert binding.fwd_path(2, 8, 8, 8192, 128, 8, True, "contiguous", torch.bfloat16) == "tcgen05"
     assert binding.fwd_path(1, 1, 1, 256, 64, 4, False, "contiguous", torch.float32) == "simt"
     assert binding.fwd_path(1, 2, 2, 384, 128, 3, True, "zigzag", torch.bfloat16) == "simt"
-    assert binding.fwd_path(1, 2, 2, 512, 64, 2, True, "zigzag", torch.bfloat16) == "simt"
+    assert binding.fwd_path(1, 2, 2, 512, 64, 2, True, "zigzag", torch.bfloat16) == "simt"  # chunks of 128
+    assert binding.fwd_path(1, 8, 2, 2048, 64, 4, True, "zigzag", torch.bfloat16) == "tcgen05"
+    assert binding.bwd_path(1, 8, 2, 2048, 64, 4, True, "zigzag", torch.bfloat16) == "simt"
     # striped: the tensor-core paths need shards of whole 256-row (forward) / 128-row (backward) tiles
     assert binding.fwd_path(1, 32, 8, 131072, 128, 8, True, "striped", torch.bfloat16) == "tcgen05"
     assert binding.fwd_path(1, 2, 2, 384, 128, 3, True, "striped", torch.bfloat16) == "simt"

@@ -70,6 +70,38 @@ def test_tcgen05_fwd_matches_oracle(B, H, Hkv, L, n, causal, layout):
                  expect_path="tcgen05")
 
 
+TC_CASES_D64 = [
+    # B, H, Hkv, L, n, causal, layout  (head dim 64: the same kernel with one 64-column box per row)
+    (1, 2, 2, 512, 1, True, "contiguous"),
+    (2, 4, 2, 2048, 4, True, "zigzag"),
+    (1, 8, 2, 2048, 2, False, "zigzag"),
+    (1, 3, 1, 1280, 1, True, "contiguous"),
+    (1, 4, 2, 2048, 4, True, "striped"),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,n,causal,layout", TC_CASES_D64)
+def test_tcgen05_fwd_head_dim_64_matches_oracle(B, H, Hkv, L, n, causal, layout):
+    run_fwd_full(B, H, Hkv, L, 64, n, causal, layout, torch.bfloat16, seed=L + n + H + 64,
+                 expect_path="tcgen05")
+
+
+def test_tcgen05_fwd_head_dim_64_steps_and_host_buffers():
+    """Head dim 64 through the ring-step forms and the host-buffer forward: the same results as
+    the fused call (step folds: within the bf16 bound of the oracle; host buffers: identical)."""
+    B, H, Hkv, L, d, n = 1, 4, 2, 2048, 64, 4
+    x = inputs(B, H, Hkv, L, d, torch.bfloat16, seed=71)
+    q, k, v = (x[t].to(DEV) for t in ("q", "k", "v"))
+    out_f, lse_f = ra.fwd(q, k, v, n, True, "zigzag")
+    out_s, lse_s = ra.fwd_stepwise(q, k, v, n, True, "zigzag")
+    out_h, lse_h = ra.fwd_host(*(x[t].pin_memory() for t in ("q", "k", "v")), n, True, "zigzag")
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attn_fwd(x["q"], x["k"], x["v"], n, True, "zigzag")
+    assert_close(to_np(out_s), ref_o, torch.bfloat16, "stepwise out")
+    assert_close(to_np(lse_s), ref_l, torch.bfloat16, "stepwise lse")
+    assert torch.equal(out_h, out_f.cpu()) and torch.equal(lse_h, lse_f.cpu())
+
+
 def test_tcgen05_fwd_large_keys():
     """1% of key rows scaled x8: the running maximum jumps late in the walk."""
     run_fwd_full(1, 4, 2, 2048, 128, 4, True, "zigzag", torch.bfloat16, seed=5, spike=0.01,
