@@ -39,7 +39,7 @@ METRIC = "ring-attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor p
 # profiles/ (forward: the 32K capture scaled to 128K by rows, each Q/K/V/O byte moving once;
 # backward: single-pass captures of the kernel itself at 32K and at 64K).  Update or drop an entry
 # whenever that kernel changes.
-TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4 * 646.6e6, ("zigzag_gqa_32k", "fwd"): 646.6e6,
+TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4 * 650.5e6, ("zigzag_gqa_32k", "fwd"): 650.5e6,
                  ("zigzag_gqa_64k_train", "train"): 7.77e9 + 4.17e9,
                  ("zigzag_gqa_32k", "train"): 2.540e9 + 1.420e9}
 
