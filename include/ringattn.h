@@ -71,9 +71,9 @@ typedef int ra_status;
 
 /* Kernel paths reported by ring_attn_fwd_path / ring_attn_bwd_path. */
 #define RA_PATH_SIMT 1      /* CUDA-core kernels: any shape, f32 or bf16 */
-#define RA_PATH_TCGEN05 2   /* tensor-core kernels (TMA + tcgen05 + TMEM): bf16; forward d = 128
-                               or 64 with shard (contiguous, striped) or chunk (zigzag) length a
-                               multiple of 256; backward d = 128 with that length a multiple of 128 */
+#define RA_PATH_TCGEN05 2   /* tensor-core kernels (TMA + tcgen05 + TMEM): bf16, d = 128 or 64,
+                               shard (contiguous, striped) or chunk (zigzag) length a multiple of
+                               256 (forward) or 128 (backward) */
 
 /* Device status bits (ring_attn_device_status). */
 #define RA_DEVICE_TIMEOUT 1u  /* a bounded wait inside a kernel ran out; the kernel stopped */

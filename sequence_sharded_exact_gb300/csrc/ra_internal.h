@@ -37,8 +37,8 @@ cudaError_t launch_bwd_simt(const Problem& p, const void* q, const void* k, cons
                             const void* dout, const float* D, const float* lse, void* dq,
                             void* dk, void* dv, int grad_dtype, cudaStream_t s);
 
-// Tensor-core kernels (TMA + tcgen05 + TMEM), bf16: forward d = 128 or 64 with chunk length %
-// 256 == 0; backward d = 128 with chunk length % 128 == 0.
+// Tensor-core kernels (TMA + tcgen05 + TMEM), bf16, d = 128 or 64: forward with chunk length %
+// 256 == 0, backward with chunk length % 128 == 0.
 bool tc_fwd_supported(const Problem& p);
 // visits (optional, n x n): +1 at [query shard][key shard] for every tile pair computed.
 cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v,

@@ -81,7 +81,9 @@ def test_path_selection():
     assert binding.fwd_path(1, 2, 2, 384, 128, 3, True, "zigzag", torch.bfloat16) == "simt"
     assert binding.fwd_path(1, 2, 2, 512, 64, 2, True, "zigzag", torch.bfloat16) == "simt"  # chunks of 128
     assert binding.fwd_path(1, 8, 2, 2048, 64, 4, True, "zigzag", torch.bfloat16) == "tcgen05"
-    assert binding.bwd_path(1, 8, 2, 2048, 64, 4, True, "zigzag", torch.bfloat16) == "simt"
+    assert binding.bwd_path(1, 8, 2, 2048, 64, 4, True, "zigzag", torch.bfloat16) == "tcgen05"
+    assert binding.bwd_path(1, 2, 2, 512, 64, 4, True, "zigzag", torch.bfloat16) == "simt"  # chunks of 64
+    assert binding.bwd_path(1, 8, 2, 2048, 64, 4, True, "zigzag", torch.float32) == "simt"
     # striped: the tensor-core paths need shards of whole 256-row (forward) / 128-row (backward) tiles
     assert binding.fwd_path(1, 32, 8, 131072, 128, 8, True, "striped", torch.bfloat16) == "tcgen05"
     assert binding.fwd_path(1, 2, 2, 384, 128, 3, True, "striped", torch.bfloat16) == "simt"
@@ -135,7 +137,8 @@ def test_tile_visits_argument_errors(lib):
     ptrs = [P(256)] * 5
     st = lib.ring_attn_fwd_tile_visits(*ptrs, 1, 2, 2, 1024, 128, 4, 1, 1, 1, None, None)
     assert st == binding.RA_ERR_INVALID_ARG
-    # d = 64 takes the CUDA-core path, which does not count tiles
+    # chunks of 128 rows take the forward's CUDA-core path (its tensor-core tiles are 256 rows),
+    # which does not count tiles
     st = lib.ring_attn_fwd_tile_visits(*ptrs, 1, 2, 2, 1024, 64, 4, 1, 1, 1, P(256), None)
     assert st == binding.RA_ERR_UNSUPPORTED
     assert "tensor-core" in lib.ring_attn_last_error().decode()

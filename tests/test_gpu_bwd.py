@@ -63,6 +63,24 @@ def test_tcgen05_bwd_matches_oracle(B, H, Hkv, L, n, causal, layout, grad_dtype)
             expect_path="tcgen05")
 
 
+TC_BWD_CASES_D64 = [
+    # B, H, Hkv, L, n, causal, layout  (bf16, d = 64: the same kernel compiled for head dim 64)
+    (1, 2, 1, 512, 2, True, "contiguous"),
+    (1, 4, 2, 1024, 4, True, "zigzag"),
+    (1, 4, 2, 1024, 4, True, "striped"),
+    (2, 2, 2, 512, 2, False, "zigzag"),
+    (1, 4, 1, 1536, 3, True, "contiguous"),
+    (4, 10, 5, 2048, 4, True, "zigzag"),     # the last round's leftover pairs split into tiles
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,n,causal,layout", TC_BWD_CASES_D64)
+@pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
+def test_tcgen05_bwd_head_dim_64_matches_oracle(B, H, Hkv, L, n, causal, layout, grad_dtype):
+    run_bwd(B, H, Hkv, L, 64, n, causal, layout, torch.bfloat16, grad_dtype, seed=L * 5 + n,
+            expect_path="tcgen05")
+
+
 BWD_CASES = [
     # B, H, Hkv, L, d, n, causal, layout, dtype
     (1, 1, 1, 256, 64, 4, False, "contiguous", torch.float32),

@@ -50,9 +50,10 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("B,H,Hkv,L,n,causal,layout", CASES)
-def test_forward_visits_exactly_the_visible_blocks(B, H, Hkv, L, n, causal, layout):
-    x = synth.make_inputs(B, H, Hkv, L, 128, dtype=torch.bfloat16, seed=L + n, device=DEV)
+def test_forward_visits_exactly_the_visible_blocks(B, H, Hkv, L, n, causal, layout, d):
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=torch.bfloat16, seed=L + n, device=DEV)
     out, lse, visits = ra.fwd_tile_visits(x["q"], x["k"], x["v"], n, causal, layout)
     out2, lse2 = ra.fwd(x["q"], x["k"], x["v"], n, causal, layout)
     torch.cuda.synchronize()
@@ -68,9 +69,10 @@ def test_forward_visits_exactly_the_visible_blocks(B, H, Hkv, L, n, causal, layo
         assert np.array_equal(visits.cpu().numpy() == 0, pairs == 0)
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("B,H,Hkv,L,n,causal,layout", CASES)
-def test_backward_visits_exactly_the_visible_tiles(B, H, Hkv, L, n, causal, layout):
-    x = synth.make_inputs(B, H, Hkv, L, 128, dtype=torch.bfloat16, seed=L * 2 + n, with_dout=True,
+def test_backward_visits_exactly_the_visible_tiles(B, H, Hkv, L, n, causal, layout, d):
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=torch.bfloat16, seed=L * 2 + n, with_dout=True,
                           device=DEV)
     q, k, v, do = x["q"], x["k"], x["v"], x["dout"]
     out, lse = ra.fwd(q, k, v, n, causal, layout)
