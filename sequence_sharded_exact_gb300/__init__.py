@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     fwd_tile_visits,
     bwd,
     bwd_tile_visits,
+    bwd_static_scratch,
+    bwd_static_scratch_capacity,
     fwd_path,
     bwd_path,
     library,
@@ -22,6 +24,7 @@ from .binding import (  # noqa: F401
     ring_step_fwd,
     ring_step_fwd_accumulate,
     rope,
+    selftest_bounded_wait,
     shard_tiles,
     ulysses_a2a,
     ulysses_bwd,

@@ -54,8 +54,6 @@ def library():
                                     "`python -c 'import __graft_entry__ as g; g.build()'`")
         lib = ctypes.CDLL(LIB_PATH)
         P, I, LL, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t
-        shape = [I] * 9  # B H Hkv L d n causal layout dtype  (order varies per call, set below)
-        del shape
         lib.ring_attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P]
         lib.ring_attn_ring_step_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
         lib.ring_attn_lse_merge.argtypes = [P, P, P, P, LL, I, P]
@@ -152,11 +150,35 @@ def _dims(q, k):
     return int(B), int(H), int(Hkv), int(L), int(d)
 
 
-def _need(t, name, device):
+def _need(t, name, device, shape=None, dtype=None):
+    """The library takes raw pointers and trusts the sizes it is given: every tensor is checked here
+    (device, layout, shape, dtype) before its pointer is passed."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda or t.device != device:
         raise ValueError(f"{name} must be a CUDA tensor on {device}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, not {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, not {t.dtype}")
+
+
+def _need_qkv(q, k, v):
+    """q [B,H,L,d], k and v [B,Hkv,L,d] of q's dtype, all on q's device; returns (B, H, Hkv, L, d)."""
+    B, H, Hkv, L, d = _dims(q, k)
+    _need(q, "q", q.device)
+    _dtype_code(q.dtype)
+    _need(k, "k", q.device, (B, Hkv, L, d), q.dtype)
+    _need(v, "v", q.device, (B, Hkv, L, d), q.dtype)
+    return B, H, Hkv, L, d
+
+
+def _need_workspace(ws, need, device):
+    _need(ws, "workspace", device)
+    if ws.dtype != torch.uint8 or ws.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes")
 
 
 def fwd_path(B, H, Hkv, L, d, n_shards, causal, layout, dtype):
@@ -191,15 +213,13 @@ def fwd_tile_visits(q, k, v, n_shards, causal=True, layout="zigzag", stream=None
 
 
 def _fwd(q, k, v, n_shards, causal, layout, out, lse, visits, stream):
-    B, H, Hkv, L, d = _dims(q, k)
-    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
-        _need(t, nm, q.device)
+    B, H, Hkv, L, d = _need_qkv(q, k, v)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
-    _need(out, "out", q.device)
-    _need(lse, "lse", q.device)
+    _need(out, "out", q.device, q.shape, q.dtype)
+    _need(lse, "lse", q.device, (B, H, L), torch.float32)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, L, d, int(n_shards),
             int(causal), _layout(layout), _dtype_code(q.dtype))
     if visits is None:
@@ -215,16 +235,22 @@ def fwd_host(q, k, v, n_shards, causal=True, layout="zigzag", out=None, lse=None
     The copies in and out overlap the compute of other kv-head groups."""
     B, H, Hkv, L, d = _dims(q, k)
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
-        if t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{nm} must be a contiguous CPU tensor")
+    _dtype_code(q.dtype)
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
     if lse is None:
         lse = torch.empty((B, H, L), dtype=torch.float32, pin_memory=True)
+    for t, nm, shape, dt in ((q, "q", q.shape, q.dtype), (k, "k", (B, Hkv, L, d), q.dtype),
+                             (v, "v", (B, Hkv, L, d), q.dtype), (out, "out", q.shape, q.dtype),
+                             (lse, "lse", (B, H, L), torch.float32)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous CPU tensor")
+        if tuple(t.shape) != tuple(shape) or t.dtype != dt:
+            raise ValueError(f"{nm} must be {dt} of shape {tuple(shape)}")
     need = int(library().ring_attn_fwd_host_workspace_size(H, Hkv, L, d, _dtype_code(q.dtype)))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need_workspace(workspace, need, dev)
     _check(library().ring_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, L, d,
                                         int(n_shards), int(causal), _layout(layout), _dtype_code(q.dtype),
                                         _ptr(workspace), workspace.numel(), _stream(stream, dev)))
@@ -234,11 +260,13 @@ def fwd_host(q, k, v, n_shards, causal=True, layout="zigzag", out=None, lse=None
 def ring_step_fwd(q, k, v, n_shards, step, causal=True, layout="zigzag", o_part=None,
                   lse_part=None, stream=None):
     """One ring step for all shards.  Returns (o_part float32 [B,H,L,d], lse_part [B,H,L])."""
-    B, H, Hkv, L, d = _dims(q, k)
+    B, H, Hkv, L, d = _need_qkv(q, k, v)
     if o_part is None:
         o_part = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
     if lse_part is None:
         lse_part = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    _need(o_part, "o_part", q.device, (B, H, L, d), torch.float32)
+    _need(lse_part, "lse_part", q.device, (B, H, L), torch.float32)
     _check(library().ring_attn_ring_step_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o_part),
                                              _ptr(lse_part), B, H, Hkv, L, d, int(n_shards),
                                              int(step), int(causal), _layout(layout),
@@ -249,11 +277,9 @@ def ring_step_fwd(q, k, v, n_shards, step, causal=True, layout="zigzag", o_part=
 def ring_step_fwd_accumulate(q, k, v, n_shards, step, o_acc, lse_acc, causal=True, layout="zigzag", stream=None):
     """ring_attn_ring_step_fwd_accumulate: fold ring step `step` into (o_acc float32 [B,H,L,d],
     lse_acc [B,H,L]) in place.  Returns (o_acc, lse_acc)."""
-    B, H, Hkv, L, d = _dims(q, k)
-    for t, nm in ((o_acc, "o_acc"), (lse_acc, "lse_acc")):
-        _need(t, nm, q.device)
-        if t.dtype != torch.float32:
-            raise ValueError(f"{nm} must be float32")
+    B, H, Hkv, L, d = _need_qkv(q, k, v)
+    _need(o_acc, "o_acc", q.device, (B, H, L, d), torch.float32)
+    _need(lse_acc, "lse_acc", q.device, (B, H, L), torch.float32)
     _check(library().ring_attn_ring_step_fwd_accumulate(_ptr(q), _ptr(k), _ptr(v), _ptr(o_acc), _ptr(lse_acc), B, H,
                                                         Hkv, L, d, int(n_shards), int(step), int(causal),
                                                         _layout(layout), _dtype_code(q.dtype),
@@ -263,12 +289,14 @@ def ring_step_fwd_accumulate(q, k, v, n_shards, step, o_acc, lse_acc, causal=Tru
 
 def lse_merge(o_acc, lse_acc, o_part, lse_part, stream=None):
     """In-place merge of a partial (o_part, lse_part) into (o_acc, lse_acc); float32 tensors."""
+    if o_acc.dim() < 1 or tuple(lse_acc.shape) != tuple(o_acc.shape[:-1]):
+        raise ValueError("lse_acc must have the shape of o_acc without its last dimension")
     d = int(o_acc.shape[-1])
     rows = int(lse_acc.numel())
-    for t, nm in ((o_acc, "o_acc"), (lse_acc, "lse_acc"), (o_part, "o_part"), (lse_part, "lse_part")):
-        _need(t, nm, o_acc.device)
-        if t.dtype != torch.float32:
-            raise ValueError(f"{nm} must be float32")
+    _need(o_acc, "o_acc", o_acc.device, None, torch.float32)
+    _need(lse_acc, "lse_acc", o_acc.device, None, torch.float32)
+    _need(o_part, "o_part", o_acc.device, o_acc.shape, torch.float32)
+    _need(lse_part, "lse_part", o_acc.device, lse_acc.shape, torch.float32)
     _check(library().ring_attn_lse_merge(_ptr(o_acc), _ptr(lse_acc), _ptr(o_part), _ptr(lse_part),
                                          rows, d, _stream(stream, o_acc.device)))
     return o_acc, lse_acc
@@ -278,14 +306,17 @@ def fwd_stepwise(q, k, v, n_shards, causal=True, layout="zigzag", out=None, lse=
                  workspace=None, stream=None):
     """The ring forward run as n ring-step launches, each folding its block into the running
     result (same results as fwd)."""
-    B, H, Hkv, L, d = _dims(q, k)
+    B, H, Hkv, L, d = _need_qkv(q, k, v)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
-    need = library().ring_attn_fwd_stepwise_workspace_size(B, H, L, d)
+    _need(out, "out", q.device, q.shape, q.dtype)
+    _need(lse, "lse", q.device, (B, H, L), torch.float32)
+    need = int(library().ring_attn_fwd_stepwise_workspace_size(B, H, L, d))
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _need_workspace(workspace, need, q.device)
     _check(library().ring_attn_fwd_stepwise(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
                                             Hkv, L, d, int(n_shards), int(causal),
                                             _layout(layout), _dtype_code(q.dtype),
@@ -315,18 +346,36 @@ def bwd_tile_visits(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigz
     return dq, dk, dv, visits
 
 
+def _need_bwd_args(q, k, v, out, lse, dout, grad_dtype):
+    B, H, Hkv, L, d = _need_qkv(q, k, v)
+    _need(out, "out", q.device, q.shape, q.dtype)
+    _need(lse, "lse", q.device, (B, H, L), torch.float32)
+    _need(dout, "dout", q.device, q.shape, q.dtype)
+    _dtype_code(grad_dtype)
+    return B, H, Hkv, L, d
+
+
+def _need_grads(dq, dk, dv, device, dims, grad_dtype):
+    B, H, Hkv, L, d = dims
+    _need(dq, "dq", device, (B, H, L, d), grad_dtype)
+    _need(dk, "dk", device, (B, Hkv, L, d), grad_dtype)
+    _need(dv, "dv", device, (B, Hkv, L, d), grad_dtype)
+
+
 def _bwd(q, k, v, out, lse, dout, n_shards, causal, layout, grad_dtype, dq, dk, dv, workspace,
          visits, stream):
-    B, H, Hkv, L, d = _dims(q, k)
+    B, H, Hkv, L, d = _need_bwd_args(q, k, v, out, lse, dout, grad_dtype)
     if dq is None:
         dq = torch.empty((B, H, L, d), dtype=grad_dtype, device=q.device)
     if dk is None:
         dk = torch.empty((B, Hkv, L, d), dtype=grad_dtype, device=q.device)
     if dv is None:
         dv = torch.empty((B, Hkv, L, d), dtype=grad_dtype, device=q.device)
+    _need_grads(dq, dk, dv, q.device, (B, H, Hkv, L, d), grad_dtype)
     need = bwd_workspace_size(B, H, Hkv, L, d, grad_dtype)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _need_workspace(workspace, need, q.device)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
             _ptr(dv), _dtype_code(grad_dtype), _ptr(workspace), workspace.numel(), B, H, Hkv, L, d,
             int(n_shards), int(causal), _layout(layout), _dtype_code(q.dtype))
@@ -341,13 +390,14 @@ def bwd_static_scratch(q, k, v, out, lse, dout, n_shards, causal=True, layout="z
                        grad_dtype=torch.float32, dq=None, dk=None, dv=None, stream=None):
     """ring_attn_bwd_static_scratch: the backward with the library's static scratch (no workspace
     argument; the C call allocates nothing).  Returns (dq, dk, dv) in grad_dtype."""
-    B, H, Hkv, L, d = _dims(q, k)
+    B, H, Hkv, L, d = _need_bwd_args(q, k, v, out, lse, dout, grad_dtype)
     if dq is None:
         dq = torch.empty((B, H, L, d), dtype=grad_dtype, device=q.device)
     if dk is None:
         dk = torch.empty((B, Hkv, L, d), dtype=grad_dtype, device=q.device)
     if dv is None:
         dv = torch.empty((B, Hkv, L, d), dtype=grad_dtype, device=q.device)
+    _need_grads(dq, dk, dv, q.device, (B, H, Hkv, L, d), grad_dtype)
     _check(library().ring_attn_bwd_static_scratch(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
         _dtype_code(grad_dtype), B, H, Hkv, L, d, int(n_shards), int(causal), _layout(layout),
@@ -405,32 +455,44 @@ def ulysses_a2a(src, n_shards, layout="contiguous", direction=0, dst=None, strea
         raise ValueError("the leading dimension of src must be n_shards")
     if dst is None:
         dst = torch.empty(shape, dtype=src.dtype, device=src.device)
-    _need(dst, "dst", src.device)
+    _need(dst, "dst", src.device, shape, src.dtype)
     _check(library().ring_attn_ulysses_a2a(_ptr(src), _ptr(dst), B, H, n * S, d, n, _layout(layout),
                                            _dtype_code(src.dtype), int(direction), _stream(stream, src.device)))
     return dst
+
+
+def _need_ulysses_qkv(q, k, v, n_shards):
+    """q [n, B, S, H, d], k and v [n, B, S, Hkv, d] of q's dtype; returns (n, B, S, H, Hkv, d)."""
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        if not isinstance(t, torch.Tensor) or t.dim() != 5:
+            raise ValueError(f"{nm} must be [n, B, S, heads, d]")
+    n, B, S, H, d = (int(s) for s in q.shape)
+    Hkv = int(k.shape[3])
+    if n != n_shards:
+        raise ValueError("the leading dimension of q must be n_shards")
+    _need(q, "q", q.device)
+    _dtype_code(q.dtype)
+    _need(k, "k", q.device, (n, B, S, Hkv, d), q.dtype)
+    _need(v, "v", q.device, (n, B, S, Hkv, d), q.dtype)
+    return n, B, S, H, Hkv, d
 
 
 def ulysses_fwd(q, k, v, n_shards, causal=True, layout="contiguous", out=None, lse=None, workspace=None,
                 stream=None):
     """ring_attn_ulysses_fwd: q [n, B, S, H, d], k and v [n, B, S, Hkv, d] (token split).  Returns
     (out [n, B, S, H, d], lse [n, B, S, H] float32)."""
-    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
-        _need(t, nm, q.device)
-        if t.dim() != 5:
-            raise ValueError(f"{nm} must be [n, B, S, heads, d]")
-    n, B, S, H, d = (int(s) for s in q.shape)
-    Hkv = int(k.shape[3])
+    n, B, S, H, Hkv, d = _need_ulysses_qkv(q, k, v, n_shards)
     L = n * S
-    if n != n_shards:
-        raise ValueError("the leading dimension of q must be n_shards")
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((n, B, S, H), dtype=torch.float32, device=q.device)
+    _need(out, "out", q.device, q.shape, q.dtype)
+    _need(lse, "lse", q.device, (n, B, S, H), torch.float32)
     need = int(library().ring_attn_ulysses_workspace_size(B, H, Hkv, L, d, _dtype_code(q.dtype)))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _need_workspace(workspace, need, q.device)
     _check(library().ring_attn_ulysses_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, L, d, n,
                                            int(causal), _layout(layout), _dtype_code(q.dtype), _ptr(workspace),
                                            workspace.numel(), _stream(stream, q.device)))
@@ -441,9 +503,12 @@ def ulysses_bwd(q, k, v, out, lse, dout, n_shards, causal=True, layout="contiguo
                 workspace=None, stream=None):
     """ring_attn_ulysses_bwd: token-split inputs as for ulysses_fwd (plus out, lse from it and dout
     [n, B, S, H, d]).  Returns (dq, dk, dv) in the token split, grad_dtype."""
-    n, B, S, H, d = (int(s) for s in q.shape)
-    Hkv = int(k.shape[3])
+    n, B, S, H, Hkv, d = _need_ulysses_qkv(q, k, v, n_shards)
     L = n * S
+    _need(out, "out", q.device, q.shape, q.dtype)
+    _need(lse, "lse", q.device, (n, B, S, H), torch.float32)
+    _need(dout, "dout", q.device, q.shape, q.dtype)
+    _dtype_code(grad_dtype)
     dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
     dk = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
     dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
@@ -451,8 +516,7 @@ def ulysses_bwd(q, k, v, out, lse, dout, n_shards, causal=True, layout="contiguo
                                                               _dtype_code(grad_dtype)))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (lse, "lse"), (dout, "dout")):
-        _need(t, nm, q.device)
+    _need_workspace(workspace, need, q.device)
     _check(library().ring_attn_ulysses_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
                                            _ptr(dk), _ptr(dv), _dtype_code(grad_dtype), _ptr(workspace),
                                            workspace.numel(), B, H, Hkv, L, d, n, int(causal), _layout(layout),
