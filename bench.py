@@ -37,11 +37,10 @@ METRIC = "ring-attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor p
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from ncu captures summarised in
 # profiles/ (forward: the 32K capture scaled to 128K by rows, each Q/K/V/O byte moving once;
-# backward: single-pass captures of the kernel itself at 32K and at 64K).  Update or drop an entry
-# whenever that kernel changes.
+# backward: a single-pass capture of the kernel itself at 64K).  Update or drop an entry whenever
+# that kernel changes; a workload without an entry reports null.
 TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4 * 650.5e6, ("zigzag_gqa_32k", "fwd"): 650.5e6,
-                 ("zigzag_gqa_64k_train", "train"): 7.77e9 + 4.17e9,
-                 ("zigzag_gqa_32k", "train"): 2.540e9 + 1.420e9}
+                 ("zigzag_gqa_64k_train", "train"): 8.51e9 + 4.51e9}
 
 
 def copy_bandwidth(host, device_t, stream):
