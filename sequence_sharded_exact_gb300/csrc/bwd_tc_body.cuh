@@ -38,8 +38,10 @@
 //     dP^T; dK from 256, dV from 384 (head-dim columns each).
 //   * head dim 64: K, V, Q and dO tiles are one 128-byte-swizzle box wide instead of two, and
 //     dK, dV use 64 columns.  dQ^T = K^T dS^T keeps M = 128 (the tensor core's 128-lane layout,
-//     the one the dQ warps read): its rows 64-127 come from the shared memory after the K tile
-//     (the V tile) and are never read out; only warps 8-9 then have dQ rows to add.
+//     the one the dQ warps read) with K loaded twice, so that its rows 64-127 repeat rows 0-63:
+//     warps 8-9 add query columns 0-63, warps 10-11 columns 64-127.  dQ^T has TMEM columns of its
+//     own there (X 0, Y 128, dQ^T 256, dK 384, dV 448), so the next dP^T does not wait for the
+//     dQ read-out.
 //   * every wait is bounded; a wait that runs out sets the device status word and the CTA stops.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -64,8 +66,13 @@ constexpr uint32_t kTileBytes = kHalves * kHalf; // a 128-row K, V, Q or dO tile
 constexpr uint32_t kDsBytes = 2 * kHalf;         // dS^T: 128 keys x 128 queries (bf16)
 constexpr uint32_t kVecBytes = kQT * 4;          // lse or D of one query tile (float32)
 
-constexpr uint32_t kSmemK = 0;
-constexpr uint32_t kSmemV = kSmemK + kTileBytes;
+// Head dim 64 has TMEM and shared memory to spare: dQ^T gets columns of its own (so the next dP^T
+// need not wait for the dQ read-out), and K is loaded twice, back to back, so that the M = 128
+// product dQ^T = K^T dS^T computes its rows 0-63 twice and all four dQ warps can reduce (rows
+// 0-63 give the query columns 0-63, rows 64-127 the columns 64-127).
+constexpr bool kD64 = kHd == 64;
+constexpr uint32_t kSmemK = 0;                                   // d = 64: K, then K again
+constexpr uint32_t kSmemV = kSmemK + (kD64 ? 2 : 1) * kTileBytes;
 constexpr uint32_t kSmemQ = kSmemV + kTileBytes;                 // kStages x 32 KB
 constexpr uint32_t kSmemDO = kSmemQ + kStages * kTileBytes;      // kStages x 32 KB
 constexpr uint32_t kSmemDS = kSmemDO + kStages * kTileBytes;     // dS^T: 2 query blocks x 128 keys x 128 B
@@ -100,7 +107,9 @@ constexpr uint32_t kSmemBytes = kSmemAbort + 8;
 // RA_DEVICE_LAYOUT if not, instead of reserving 1 KB of slack that this layout does not have.
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-constexpr uint32_t kColX = 0, kColY = 128, kColDK = 256, kColDV = 384;
+constexpr uint32_t kColX = 0, kColY = 128;
+constexpr uint32_t kColDQ = kD64 ? 256 : kColY;  // d = 128: dQ^T reuses Y once phase B has read dP^T
+constexpr uint32_t kColDK = kD64 ? 384 : 256, kColDV = kD64 ? 448 : 384;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 struct BwdArgs {
@@ -490,7 +499,8 @@ __device__ __forceinline__ void dq_role(const BwdArgs& a, uint32_t sbase, uint32
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int dcol = (warp & 3) * 32 + lane;  // TMEM lane = head-dim index
-    const uint32_t ty = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kColY;
+    const uint32_t ty = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kColDQ;
+    const uint32_t dq_c0 = kD64 && (warp & 3) >= 2 ? 64u : 0u;  // d = 64: this warp's query columns
     auto bar = [&](int i) { return sbase + kSmemBar + 8u * (uint32_t)i; };
     uint32_t gt = 0;
     const int slots = unit_slots(a);
@@ -509,24 +519,37 @@ __device__ __forceinline__ void dq_role(const BwdArgs& a, uint32_t sbase, uint32
                 if (!mbar_wait(bar(BAR_DQ_FULL), gt & 1, ctl)) return;
                 tc_fence_after_sync();
                 __syncwarp();
-                if (kHd < 128 && (warp & 3) >= kHd / 32) {  // rows of dQ^T past the head dim
+                if constexpr (kD64) {
+                    // rows 0-63 (warps 8-9): query columns 0-63; rows 64-127 (warps 10-11, the same
+                    // values from the second copy of K): query columns 64-127
+                    uint32_t xa[64], xb[64];
+                    tmem_ld_32x32b_x64(ty, xa);
+                    tmem_ld_32x32b_x64(ty + 64, xb);
+                    tmem_ld_wait(xa);
+                    tmem_ld_wait(xb);
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(BAR_DQ_FREE));
-                    continue;
+                    const int zq = u.b * a.H + u.g * a.G + hh;
+                    float* dst = a.dq_acc + ((long long)zq * a.geo.L + qrow) * kHd + (dcol & 63);
+                    if (dq_c0 == 0)
+                        red_group(dst, xa, 0, gap_ns);
+                    else
+                        red_group(dst, xb, 64, gap_ns);
+                } else {
+                    uint32_t xa[64], xb[64];
+                    tmem_ld_32x32b_x64(ty, xa);
+                    tmem_ld_32x32b_x64(ty + 64, xb);
+                    tmem_ld_wait(xa);
+                    tmem_ld_wait(xb);
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(BAR_DQ_FREE));
+                    const int zq = u.b * a.H + u.g * a.G + hh;
+                    float* dst = a.dq_acc + ((long long)zq * a.geo.L + qrow) * kHd + dcol;
+                    red_group(dst, xa, 0, gap_ns);
+                    red_group(dst, xb, 64, gap_ns);
                 }
-                uint32_t xa[64], xb[64];
-                tmem_ld_32x32b_x64(ty, xa);
-                tmem_ld_32x32b_x64(ty + 64, xb);
-                tmem_ld_wait(xa);
-                tmem_ld_wait(xb);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BAR_DQ_FREE));
-                const int zq = u.b * a.H + u.g * a.G + hh;
-                float* dst = a.dq_acc + ((long long)zq * a.geo.L + qrow) * kHd + dcol;
-                red_group(dst, xa, 0, gap_ns);
-                red_group(dst, xb, 64, gap_ns);
             }
         }
     }
@@ -553,12 +576,14 @@ __device__ __forceinline__ void producer_role(const BwdArgs& a, uint32_t sbase, 
             if (!unit_in_slot(a, slot, u) || u.ntiles == 0) continue;
             if (uc > 0 && !mbar_wait(bar(BAR_KV_EMPTY), (uc - 1) & 1, ctl)) { ok = false; break; }
             const int zkv = u.b * a.Hkv + u.g;
-            mbar_arrive_expect_tx(bar(BAR_KV_FULL), 2 * kTileBytes);
+            mbar_arrive_expect_tx(bar(BAR_KV_FULL), (kD64 ? 3 : 2) * kTileBytes);
 #pragma unroll
             for (int half = 0; half < kHalves; ++half) {
                 tma_load_3d(sbase + kSmemK + (uint32_t)half * kHalf, tmK, bar(BAR_KV_FULL), half * 64, u.rk, zkv);
                 tma_load_3d(sbase + kSmemV + (uint32_t)half * kHalf, tmV, bar(BAR_KV_FULL), half * 64, u.rk, zkv);
             }
+            if constexpr (kD64)
+                tma_load_3d(sbase + kSmemK + kTileBytes, tmK, bar(BAR_KV_FULL), 0, u.rk, zkv);
             ++uc;
             QWalk walk;
             walk.begin(a, u);
@@ -686,7 +711,7 @@ __device__ __forceinline__ void issue_dq(uint32_t tmem, const BwdDesc& dsc)
     const uint32_t a_lo = opaque(dsc.k_m), b_lo = opaque(dsc.ds_n);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tmem + kColY, sdesc_at(a_lo, (uint32_t)kk * 2048u, kDescHi), sdesc_at(b_lo, (uint32_t)kk * 2048u, kDescHi),
+        mma_ss(tmem + kColDQ, sdesc_at(a_lo, (uint32_t)kk * 2048u, kDescHi), sdesc_at(b_lo, (uint32_t)kk * 2048u, kDescHi),
                kIdDQ, kk > 0);
 }
 
@@ -712,8 +737,8 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
                 tc_fence_after_sync();
                 issue_kmajor(tmem + kColX, dsc.k_k, dsc.q_k + st * kStageLo);
                 tc_commit(bar(BAR_ST_FULL));
-                // Y: the previous tile's dQ^T must have been read out
-                if (gt > 0 && !mbar_wait(bar(BAR_DQ_FREE), (gt - 1) & 1, ctl)) goto drain;
+                // Y: the previous tile's dQ^T must have been read out (d = 128, where it shares Y)
+                if (!kD64 && gt > 0 && !mbar_wait(bar(BAR_DQ_FREE), (gt - 1) & 1, ctl)) goto drain;
                 if (!mbar_wait(bar(BAR_DO_FULL + (int)st), sp, ctl)) goto drain;
                 tc_fence_after_sync();
                 issue_kmajor(tmem + kColY, dsc.v_k, dsc.do_k + st * kStageLo);
@@ -736,16 +761,18 @@ __device__ __forceinline__ void mma_role(const BwdArgs& a, uint32_t sbase, uint3
                     issue_kmajor(tmem + kColX, dsc.k_k, dsc.q_k + nst * kStageLo);
                     tc_commit(bar(BAR_ST_FULL));
                 }
-                // dQ^T = K^T dS^T into Y (phase B has read dP^T out of it), then dK += dS^T Q
+                // dQ^T = K^T dS^T (d = 128: into Y, whose dP^T phase B has read; d = 64: into its own
+                // columns, once the previous tile's dQ^T is out), then dK += dS^T Q
                 if (!mbar_wait(bar(BAR_DS_READY), gt & 1, ctl)) goto drain;
+                if (kD64 && gt > 0 && !mbar_wait(bar(BAR_DQ_FREE), (gt - 1) & 1, ctl)) goto drain;
                 tc_fence_after_sync();
                 issue_dq(tmem, dsc);
                 tc_commit(bar(BAR_DQ_FULL));
                 issue_dk(tmem, dsc, dsc.q_n + st * kStageLo, t > 0);
                 tc_commit(bar(BAR_Q_EMPTY + (int)st));
-                // next dP^T into Y, once dQ^T has been read out of it
+                // next dP^T into Y (d = 128: once dQ^T has been read out of it)
                 if (more) {
-                    if (!mbar_wait(bar(BAR_DQ_FREE), gt & 1, ctl)) goto drain;
+                    if (!kD64 && !mbar_wait(bar(BAR_DQ_FREE), gt & 1, ctl)) goto drain;
                     if (!mbar_wait(bar(BAR_DO_FULL + (int)nst), nsp, ctl)) goto drain;
                     tc_fence_after_sync();
                     issue_kmajor(tmem + kColY, dsc.v_k, dsc.do_k + nst * kStageLo);
