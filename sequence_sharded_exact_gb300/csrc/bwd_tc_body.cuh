@@ -34,8 +34,8 @@
 //     into the float32 accumulator in global memory with coalesced reductions (one warp
 //     instruction covers 32 consecutive head-dim entries of one query row), paced so that they do
 //     not crowd the other warps' shared-memory traffic out of the memory-instruction queue.
-//   * TMEM columns: X = [0,128) S^T then P^T; Y = [128,256) dP^T, then dQ^T once phase B has read
-//     dP^T; dK from 256, dV from 384 (head-dim columns each).
+//   * TMEM columns (head dim 128): X = [0,128) S^T then P^T; Y = [128,256) dP^T, then dQ^T once
+//     phase B has read dP^T; dK [256,384), dV [384,512).
 //   * head dim 64: K, V, Q and dO tiles are one 128-byte-swizzle box wide instead of two, and
 //     dK, dV use 64 columns.  dQ^T = K^T dS^T keeps M = 128 (the tensor core's 128-lane layout,
 //     the one the dQ warps read) with K loaded twice, so that its rows 64-127 repeat rows 0-63:
