@@ -1,0 +1,56 @@
+"""Host-side logic of bench.py (no GPU): the clock summary that decides whether a timed run is kept,
+the flop counts the TFLOP/s figures divide by, and the oracle's row sampling."""
+import numpy as np
+import pytest
+
+import bench
+
+
+def _line(sm, mx, hw="Not Active", hw_th="Not Active", sw_th="Not Active", cap="Not Active"):
+    # index, clocks.sm, clocks.max.sm, power.draw, active mask, then the four reasons
+    return f"0, {sm}, {mx}, 1200.5, 0x0, {hw}, {hw_th}, {sw_th}, {cap}"
+
+
+def test_clock_summary_median_max_and_reasons():
+    cs = bench.ClockSampler(0)
+    cs.lines = [_line(1950, 2070), _line(2010, 2070, cap="Active"), _line(1990, 2070),
+                "garbage", "0, [N/A], 2070, 0, 0x0, a, b, c, d"]
+    s = cs.summary()
+    assert s["sm_mhz"] == 1990 and s["sm_max_mhz"] == 2070 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+@pytest.mark.parametrize("field,name", [("hw", "hw_slowdown"), ("hw_th", "hw_thermal_slowdown"),
+                                        ("sw_th", "sw_thermal_slowdown")])
+def test_clock_summary_reports_each_rejecting_reason(field, name):
+    cs = bench.ClockSampler(0)
+    cs.lines = [_line(1500, 2070, **{field: "Active"}), _line(1600, 2070)]
+    assert name in cs.summary()["reasons"]
+
+
+def test_clock_summary_without_samples():
+    cs = bench.ClockSampler(0)
+    assert cs.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+
+def test_forward_flops():
+    assert bench.fwd_flops(1, 32, 131072, 128, False) == 4.0 * 32 * 131072 ** 2 * 128
+    assert bench.fwd_flops(1, 32, 131072, 128, True) == bench.fwd_flops(1, 32, 131072, 128, False) / 2
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_row_flops_sum_to_the_visible_pairs(layout, causal):
+    """Every layout is a permutation of positions, so the rows' visible keys add up to L(L+1)/2
+    per head (causal) or L^2 (not), whatever the layout."""
+    B, H, L, d, n = 1, 2, 96, 64, 3
+    total = sum(bench.row_flops(r, B, H, L, d, n, causal, layout) for r in range(B * H * L))
+    pairs = L * (L + 1) // 2 if causal else L * L
+    assert total == 4.0 * d * pairs * B * H
+
+
+def test_sample_rows_are_distinct_sorted_and_in_range():
+    rows = bench.sample_rows(2, 4, 1000, 500, seed=3)
+    assert len(rows) == 500 and np.all(np.diff(rows) > 0)
+    assert rows[0] >= 0 and rows[-1] < 2 * 4 * 1000
+    assert np.array_equal(rows, bench.sample_rows(2, 4, 1000, 500, seed=3))
