@@ -34,6 +34,20 @@ def test_header_declares_the_boundary():
     assert set(names) == set(binding.EXPORTS), "binding and header disagree"
 
 
+def test_binding_constants_match_the_header():
+    """The binding's status, layout, dtype, path and device-status codes are the header's."""
+    src = open(HEADER).read()
+    defs = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define (RA_\w+) (\d+)u?\b", src)}
+    for name in ("RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_NO_DEVICE",
+                 "RA_ERR_TIMEOUT", "RA_DEVICE_TIMEOUT", "RA_DEVICE_LAYOUT"):
+        assert getattr(binding, name) == defs[name], name
+    assert binding.LAYOUTS == {"contiguous": defs["RA_LAYOUT_CONTIGUOUS"], "zigzag": defs["RA_LAYOUT_ZIGZAG"],
+                               "striped": defs["RA_LAYOUT_STRIPED"]}
+    assert binding.PATHS == {defs["RA_PATH_SIMT"]: "simt", defs["RA_PATH_TCGEN05"]: "tcgen05"}
+    assert binding._dtype_code(torch.float32) == defs["RA_F32"]
+    assert binding._dtype_code(torch.bfloat16) == defs["RA_BF16"]
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
