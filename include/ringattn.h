@@ -60,7 +60,7 @@ typedef int ra_status;
 #define RA_ERR_UNSUPPORTED 2
 #define RA_ERR_CUDA 3
 #define RA_ERR_NO_DEVICE 4
-#define RA_ERR_TIMEOUT 5
+#define RA_ERR_TIMEOUT 5   /* returned by ring_attn_device_check: a bounded wait in a kernel ran out */
 
 #define RA_LAYOUT_CONTIGUOUS 0
 #define RA_LAYOUT_ZIGZAG 1
@@ -183,8 +183,9 @@ RA_API size_t ring_attn_bwd_workspace_size(int B, int H, int Hkv, int L, int d, 
 /*
  * ring_attn_bwd_static_scratch -- the backward of ring_attn_bwd for callers that cannot allocate
  * device memory (a host framework that owns all device memory as one pre-sized pool and passes
- * only input and output buffers, or a loop that may not call the allocator).  The paper has no
- * counterpart: this is an interface convenience, not part of the method.
+ * only input and output buffers, or a loop that may not call the allocator).  The pages that
+ * define the method have no counterpart to this call: it is an interface convenience, not part
+ * of the method.
  * Same arguments and results as ring_attn_bwd without the workspace: the scratch comes from a
  * file-scope device array of ring_attn_bwd_static_scratch_capacity() bytes (64 MiB) that every
  * GPU loading this library holds until the process exits.  Allocates nothing.
@@ -192,7 +193,8 @@ RA_API size_t ring_attn_bwd_workspace_size(int B, int H, int Hkv, int L, int d, 
  *     RA_ERR_INVALID_ARG before anything is enqueued (fp32 gradients need 4 bytes per query row,
  *     bf16 gradients 4 * (d + 1)).
  *   - The first call on a device looks the array's device address up (cudaGetSymbolAddress) with
- *     that device current; make that first call before any stream capture.
+ *     that device current; make that first call before any stream capture.  The address is kept
+ *     for the life of the process: cudaDeviceReset after the first call is not supported.
  *   - Every call on a device shares the array and leaves its contents behind; each call rewrites
  *     or zeroes what it reads.  Calls whose GPU work overlaps (other streams or threads) race.
  */
@@ -313,9 +315,30 @@ RA_API ra_status ring_attn_bwd_path(int B, int H, int Hkv, int L, int d, int n_s
 RA_API ra_status ring_attn_selftest_bounded_wait(unsigned long long limit_ns, unsigned int* returned,
                                                  void* stream);
 
-/* Reads the device status word of the current device into *status (HOST pointer; bits
- * RA_DEVICE_*), then clears it.  Synchronises `stream`. */
+/*
+ * The device status word.  There is one word per device, not one per stream or per call: it
+ * collects the RA_DEVICE_* bits of every kernel of this library that ran on the device since the
+ * word was last read, and reading it clears it for every caller.  A caller that shares the device
+ * with others (other threads, streams or libraries using this one) and needs to know whether ITS
+ * work timed out must read the word at a point where no other caller's work of this library is in
+ * flight on the device; otherwise a bit may belong to another caller, or another caller's read may
+ * have cleared a bit that this caller's kernel set.
+ *   The device address of the word is looked up once per device, on the first call that needs it,
+ * and kept for the life of the process: cudaDeviceReset after that first call is not supported
+ * (the module may be reloaded elsewhere).
+ *
+ * ring_attn_device_status -- reads the word of the current device into *status (HOST pointer; bits
+ * RA_DEVICE_*), then clears it.  Synchronises `stream`.
+ */
 RA_API ra_status ring_attn_device_status(unsigned int* status, void* stream);
+
+/*
+ * ring_attn_device_check -- ring_attn_device_status as a status code: synchronises `stream`, reads
+ * and clears the word, and returns RA_ERR_TIMEOUT if a bounded wait inside a kernel ran out (that
+ * kernel stopped early: its outputs are incomplete and must not be used), RA_ERR_CUDA if a kernel
+ * found its shared memory misaligned and did nothing, RA_OK if the word was clear.
+ */
+RA_API ra_status ring_attn_device_check(void* stream);
 
 /* Message for the calling thread's last non-OK status ("" if none).  Never NULL. */
 RA_API const char* ring_attn_last_error(void);

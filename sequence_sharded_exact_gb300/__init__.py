@@ -8,6 +8,7 @@ __graft_entry__ as g; g.build()"``).
 from .binding import (  # noqa: F401
     RingAttnError,
     bwd_workspace_size,
+    device_check,
     device_status,
     fwd,
     fwd_host,

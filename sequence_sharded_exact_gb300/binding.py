@@ -33,7 +33,7 @@ EXPORTS = (
     "ring_attn_rope", "ring_attn_ulysses_a2a", "ring_attn_ulysses_fwd", "ring_attn_ulysses_workspace_size",
     "ring_attn_ulysses_bwd", "ring_attn_ulysses_bwd_workspace_size", "ring_attn_fwd_host",
     "ring_attn_ring_step_fwd_accumulate",
-    "ring_attn_fwd_host_workspace_size", "ring_attn_selftest_bounded_wait",
+    "ring_attn_fwd_host_workspace_size", "ring_attn_selftest_bounded_wait", "ring_attn_device_check",
 )
 
 
@@ -68,6 +68,8 @@ def library():
         lib.ring_attn_fwd_path.argtypes = [I, I, I, I, I, I, I, I, I, P]
         lib.ring_attn_bwd_path.argtypes = [I, I, I, I, I, I, I, I, I, P]
         lib.ring_attn_device_status.argtypes = [P, P]
+        lib.ring_attn_device_check.argtypes = [P]
+        lib.ring_attn_device_check.restype = ctypes.c_int
         lib.ring_attn_last_error.argtypes = []
         lib.ring_attn_last_error.restype = ctypes.c_char_p
         lib.ring_attn_abi_version.argtypes = []
@@ -539,3 +541,10 @@ def device_status(stream=None, device=None):
     st = ctypes.c_uint(0)
     _check(library().ring_attn_device_status(ctypes.byref(st), _stream(stream, dev)))
     return int(st.value)
+
+
+def device_check(stream=None, device=None):
+    """ring_attn_device_check: synchronises the stream, reads and clears the device status word and
+    raises RingAttnError (status RA_ERR_TIMEOUT) if a bounded wait inside a kernel ran out."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check(library().ring_attn_device_check(_stream(stream, dev)))

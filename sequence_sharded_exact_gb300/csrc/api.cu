@@ -731,6 +731,20 @@ ra_status ring_attn_device_status(unsigned int* status, void* stream)
     return RA_OK;
 }
 
+ra_status ring_attn_device_check(void* stream)
+{
+    unsigned int st = 0;
+    ra_status r = ring_attn_device_status(&st, stream);
+    if (r != RA_OK) return r;
+    if (st & RA_DEVICE_TIMEOUT)
+        return fail(RA_ERR_TIMEOUT,
+                    "a bounded wait inside a kernel ran out: that kernel stopped early and its results are "
+                    "incomplete (status word 0x%x)", st);
+    if (st & RA_DEVICE_LAYOUT)
+        return fail(RA_ERR_CUDA, "a kernel found its shared memory misaligned and did nothing (status word 0x%x)", st);
+    return RA_OK;
+}
+
 // Host-side shard scheduler query.  Tiles are `tile` consecutive buffer rows from each shard's
 // first row; a (query tile, key tile) pair counts when the smallest natural key position of the
 // key tile does not exceed the largest natural query position of the query tile.  The per-tile

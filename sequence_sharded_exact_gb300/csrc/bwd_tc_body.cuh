@@ -48,6 +48,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "ra_internal.h"
 #include "ra_ptx.cuh"
 
@@ -853,16 +855,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
+    static std::once_flag once;
+    std::call_once(once, [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        tried = true;
-    }
+    });
     return fn;
 }
 
@@ -916,15 +917,21 @@ cudaError_t RA_BWD_LAUNCH(const Problem& p, const void* q, const void* k, const 
     a.visits = visits;
     a.scale = 1.0f / sqrtf((float)kHd);
     a.scale_log2 = a.scale * kLog2e;
+    // The shared-memory opt-in is set once per device; the lock makes concurrent first launches from
+    // several host threads safe.
+    static std::mutex attr_mu;
     static bool attr_done[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_done[dev]) {
-        e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+    {
+        std::lock_guard<std::mutex> lk(attr_mu);
+        if (!attr_done[dev]) {
+            e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+            if (e != cudaSuccess) return e;
+            attr_done[dev] = true;
+        }
     }
     const long long sms = device_sm_count();
     const unsigned grid = (unsigned)(a.items < sms ? a.items : sms);

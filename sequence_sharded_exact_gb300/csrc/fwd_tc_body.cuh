@@ -720,15 +720,21 @@ cudaError_t RA_FWD_LAUNCH(const Problem& p, const void* q, const void* k, const 
     a.visits = visits;
     a.scale_log2 = kLog2e / sqrtf((float)kHd);
 
+    // The shared-memory opt-in is set once per device; the lock makes concurrent first launches from
+    // several host threads safe.
+    static std::mutex attr_mu;
     static bool attr_done[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_done[dev]) {
-        e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+    {
+        std::lock_guard<std::mutex> lk(attr_mu);
+        if (!attr_done[dev]) {
+            e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+            if (e != cudaSuccess) return e;
+            attr_done[dev] = true;
+        }
     }
     const long long sms = device_sm_count();
     const unsigned grid = (unsigned)(a.items < sms ? a.items : sms);

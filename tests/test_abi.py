@@ -221,3 +221,15 @@ def test_selftest_bounded_wait_argument_errors(lib):
     assert lib.ring_attn_selftest_bounded_wait(10, P(256), None) == binding.RA_ERR_INVALID_ARG
     assert lib.ring_attn_selftest_bounded_wait(10**9, P(256), None) == binding.RA_ERR_INVALID_ARG
     assert lib.ring_attn_selftest_bounded_wait(10**6, None, None) == binding.RA_ERR_INVALID_ARG
+
+
+def test_device_check_reports_its_codes(lib):
+    """ring_attn_device_check turns the device status word into a status code (RA_ERR_TIMEOUT when
+    a bounded wait ran out; exercised on the GPU by test_gpu_failure_detection).  Without a device it
+    says so before touching the word."""
+    if torch.cuda.is_available():
+        pytest.skip("the GPU side is covered by test_gpu_failure_detection")
+    assert lib.ring_attn_device_check(None) == binding.RA_ERR_NO_DEVICE
+    st = ctypes.c_uint(7)
+    assert lib.ring_attn_device_status(ctypes.byref(st), None) == binding.RA_ERR_NO_DEVICE
+    assert st.value == 7  # untouched on failure

@@ -15,6 +15,12 @@ def test_bounded_wait_runs_out_and_reports():
     assert binding.selftest_bounded_wait(limit_ns=2_000_000) == 1       # the wait gave up after 2 ms
     assert ra.device_status() == binding.RA_DEVICE_TIMEOUT              # and said so
     assert ra.device_status() == 0                                      # reading clears the word
+    # the same report as a status code: ring_attn_device_check returns RA_ERR_TIMEOUT, then RA_OK
+    assert binding.selftest_bounded_wait(limit_ns=2_000_000) == 1
+    with pytest.raises(binding.RingAttnError) as err:
+        ra.device_check()
+    assert err.value.status == binding.RA_ERR_TIMEOUT and "bounded wait" in str(err.value)
+    ra.device_check()                                                   # the word was cleared
     # the context is intact: a forward still runs and the status stays clean
     x = synth.make_inputs(1, 2, 1, 1024, 128, dtype=torch.bfloat16, seed=5, device="cuda:0")
     out, lse = ra.fwd(x["q"], x["k"], x["v"], 4, True, "zigzag")
