@@ -206,6 +206,70 @@ RA_API ra_status ring_attn_bwd_static_scratch(const void* q, const void* k, cons
 RA_API size_t ring_attn_bwd_static_scratch_capacity(void);
 
 /*
+ * One device of the multi-device ring.  In the pages' setting each device i holds only its own
+ * shard -- Q_i, K_i, V_i -- and at ring step r = 0..n-1 computes the attention of Q_i against the
+ * K/V block it currently holds, that of shard j = (i - r) mod n, folds it into a running output,
+ * and passes the block on to device i + 1 while receiving the next from device i - 1
+ * (LLM-101-CN "distributed hands-on code", section 6.2, block_attention and forward; M4-051
+ * section 3; "Lecture 30: TP/PP/SP/CP", section 3.2).  These calls are that per-device data path;
+ * moving the blocks between devices is the caller's (NCCL or another transport).
+ *
+ * Local buffers: a device's tensors hold S = L / n_shards rows per head -- rows [i*S, (i+1)*S) of
+ * the whole-sequence buffers of the other calls, in the same order (shard i's rows of the layout):
+ *   q, dout: [B][H][S][d] (dtype);  k, v: [B][Hkv][S][d] (dtype) of the shard they came from;
+ *   o_acc, dq_acc: [B][H][S][d] float32;  lse_acc, lse, D: [B][H][S] float32;
+ *   dk, dv: [B][Hkv][S][d] float32, the gradients of the K/V block they travel with.
+ * L, n_shards, causal and layout describe the whole sequence: natural positions and the causal
+ * mask come from them, so shard_q and shard_kv (0 .. n_shards-1) must name the shards the local
+ * buffers hold.  Same requirements on L, n_shards, d and the pointers as ring_attn_fwd.
+ */
+
+/*
+ * ring_attn_block_fwd -- block attention of the query shard shard_q against the K/V block of shard
+ * shard_kv, written to (accumulate = 0) or folded into (accumulate = 1) the running state
+ * (o_acc, lse_acc): o_acc holds the output normalised by its own running sum, lse_acc the running
+ * log-sum-exp (natural log).  Folding uses the online-softmax merge of ring_attn_lse_merge; a row
+ * with lse_acc = -infinity holds nothing yet (its o_acc is not read).  A row that sees no key of
+ * this block gets o = 0, lse = -infinity (accumulate = 0) or is left unchanged (accumulate = 1);
+ * fully masked causal tiles are skipped.  After the n blocks of the ring, o_acc is the attention
+ * output (convert it with ring_attn_f32_convert) and lse_acc its log-sum-exp.
+ */
+RA_API ra_status ring_attn_block_fwd(const void* q, const void* k, const void* v, float* o_acc, float* lse_acc,
+                                     int B, int H, int Hkv, int L, int d, int n_shards, int shard_q, int shard_kv,
+                                     int accumulate, int causal, int layout, int dtype, void* stream);
+
+/*
+ * ring_attn_block_bwd -- the backward of one block: the contributions of the pairs (query of shard
+ * shard_q, key of shard shard_kv) to the gradients, with P = exp(s - lse) recomputed from the
+ * query rows' final lse and D = rowsum(dout * out) from ring_attn_bwd_preprocess:
+ *   dq_acc += dS k / sqrt(d)          (added to: zero it before the first block),
+ *   dk (+)= dS^T q / sqrt(d),  dv (+)= P^T dout,   dS = P (dout . v - D),
+ * dk and dv summed over the query heads that share a kv head, and added to (accumulate_kv = 1) or
+ * stored (accumulate_kv = 0; a key row that meets no query of this block gets 0).  The sum of
+ * the n blocks' contributions is ring_attn_bwd's result.
+ */
+RA_API ra_status ring_attn_block_bwd(const void* q, const void* k, const void* v, const void* dout,
+                                     const float* lse, const float* D, float* dq_acc, float* dk, float* dv, int B,
+                                     int H, int Hkv, int L, int d, int n_shards, int shard_q, int shard_kv,
+                                     int accumulate_kv, int causal, int layout, int dtype, void* stream);
+
+/*
+ * ring_attn_bwd_preprocess -- D[r] = sum_c out[r][c] * dout[r][c] for `rows` rows of d elements
+ * (dtype), D float32: the per-row term of the backward, computed once per device before its blocks.
+ * ring_attn_f32_zero -- x[0 .. count) = 0 (float32).
+ * ring_attn_f32_add -- acc[i] += part[i] for i < count (float32): a device adds its contribution
+ *   to the dK / dV accumulators that arrive with a block before passing them on.
+ * ring_attn_f32_convert -- dst[i] = src[i] converted to dtype (RA_F32 copies, RA_BF16 rounds to
+ *   nearest even): the running output or a gradient accumulator into the caller's dtype.
+ * Device pointers, 16-byte aligned; count >= 0 (0 enqueues nothing).
+ */
+RA_API ra_status ring_attn_bwd_preprocess(const void* out, const void* dout, float* D, long long rows, int d,
+                                          int dtype, void* stream);
+RA_API ra_status ring_attn_f32_zero(float* x, long long count, void* stream);
+RA_API ra_status ring_attn_f32_add(float* acc, const float* part, long long count, void* stream);
+RA_API ra_status ring_attn_f32_convert(const float* src, void* dst, long long count, int dtype, void* stream);
+
+/*
  * ring_attn_shard_tiles -- HOST ONLY, no CUDA call.  For each query shard, the number of
  * (query tile, key tile) pairs of `tile` x `tile` buffer rows (tiles start at each shard's first
  * row) that hold at least one visible (query, key) pair: the per-shard causal work that the

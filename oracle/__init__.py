@@ -57,12 +57,15 @@ def _load():
         lib.oracle_attn_bwd_dq_rows.argtypes = bcommon + [Lg, P, P]
         lib.oracle_attn_bwd_dkv_rows.argtypes = bcommon + [Lg, P, P, P]
         lib.oracle_attn_bwd.argtypes = bcommon + [P, P, P]
+        lib.oracle_block_fwd.argtypes = [P, P, P, I, I, I, Lg, I, I, I, I, I, I, P, P]
+        lib.oracle_block_bwd.argtypes = [P, P, P, P, P, P, I, I, I, Lg, I, I, I, I, I, I, P, P, P]
         lib.oracle_shard_tiles.argtypes = [Lg, I, I, I, I, P]
         lib.oracle_rope.argtypes = [P, Lg, Lg, I, I, I, ctypes.c_double, I, P]
         lib.oracle_num_threads.argtypes = []
         for f in ("oracle_attn_fwd_rows", "oracle_attn_fwd", "oracle_ring_fwd",
                   "oracle_attn_bwd_dq_rows", "oracle_attn_bwd_dkv_rows", "oracle_attn_bwd",
-                  "oracle_shard_tiles", "oracle_rope", "oracle_num_threads"):
+                  "oracle_shard_tiles", "oracle_rope", "oracle_num_threads", "oracle_block_fwd",
+                  "oracle_block_bwd"):
             getattr(lib, f).restype = I
         _lib = lib
         return lib
@@ -199,3 +202,41 @@ def rope(x, n, layout, base=10000.0, inverse=False):
     _check(_load().oracle_rope(_ptr(x), nheads, L, d, int(n), _layout(layout), float(base), int(bool(inverse)),
                                _ptr(y)), "rope")
     return y
+
+
+def _f64(a):
+    """Contiguous float64 numpy copy of a numpy array or torch tensor."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").double().contiguous().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def block_fwd(q_i, k_j, v_j, L, n, causal, layout, i, j):
+    """One device's block: attention of shard i's rows (q_i [B,H,S,d]) restricted to the keys of
+    shard j (k_j, v_j [B,Hkv,S,d]).  Returns (o_part [B,H,S,d] normalised by the block's own sum,
+    lse_part [B,H,S]; -inf where the row sees nothing of the block)."""
+    q_i, k_j, v_j = _f32(q_i), _f32(k_j), _f32(v_j)
+    B, H, S, d = q_i.shape
+    Hkv = k_j.shape[1]
+    o = np.empty((B, H, S, d), np.float64)
+    lse = np.empty((B, H, S), np.float64)
+    _check(_load().oracle_block_fwd(_ptr(q_i), _ptr(k_j), _ptr(v_j), B, H, Hkv, int(L), d, int(n), int(causal),
+                                    _layout(layout), int(i), int(j), _ptr(o), _ptr(lse)), "block_fwd")
+    return o, lse
+
+
+def block_bwd(q_i, k_j, v_j, dout_i, lse_i, D_i, L, n, causal, layout, i, j):
+    """The gradient contributions of the pairs (query of shard i, key of shard j), with P from the
+    query rows' full lse_i and D_i = <dO, O> ([B,H,S], float64).  Returns (dq_part [B,H,S,d],
+    dk_part [B,Hkv,S,d], dv_part [B,Hkv,S,d])."""
+    q_i, k_j, v_j, dout_i = _f32(q_i), _f32(k_j), _f32(v_j), _f32(dout_i)
+    lse_i, D_i = _f64(lse_i), _f64(D_i)
+    B, H, S, d = q_i.shape
+    Hkv = k_j.shape[1]
+    dq = np.empty((B, H, S, d), np.float64)
+    dk = np.empty((B, Hkv, S, d), np.float64)
+    dv = np.empty((B, Hkv, S, d), np.float64)
+    _check(_load().oracle_block_bwd(_ptr(q_i), _ptr(k_j), _ptr(v_j), _ptr(dout_i), _ptr(lse_i), _ptr(D_i), B, H,
+                                    Hkv, int(L), d, int(n), int(causal), _layout(layout), int(i), int(j), _ptr(dq),
+                                    _ptr(dk), _ptr(dv)), "block_bwd")
+    return dq, dk, dv

@@ -450,6 +450,153 @@ int oracle_attn_bwd(const float* q, const float* k, const float* v, const float*
     return st;
 }
 
+/* ---------------------------------------------------------------------------------------------
+ * One device of the multi-device ring ([LLM101] 6.2 block_attention; [M4-051] section 3): device i
+ * holds only shard i's rows; at ring step r it meets the K/V block of shard j = (i - r) mod n.
+ * Local buffers hold S = L/n rows per head: q_i, dout_i [B][H][S][d] and k_j, v_j [B][Hkv][S][d]
+ * are rows [i*S, (i+1)*S) (resp. [j*S, (j+1)*S)) of the whole-sequence buffers.  Positions and the
+ * causal mask come from the whole sequence (L, n, layout).
+ * ------------------------------------------------------------------------------------------- */
+
+/* The block attention by definition: for every local row of shard i, attention restricted to the
+ * keys of shard j it may see (two passes, float64).  o_part [B][H][S][d] is normalised by the
+ * block's own sum, lse_part [B][H][S] is the log-sum-exp over those keys; a row that sees no key
+ * of the block gets o_part = 0 and lse_part = -inf.  The n blocks of a row together are the row's
+ * full key set, so their (o_part, lse_part) recombine into full attention. */
+int oracle_block_fwd(const float* q_i, const float* k_j, const float* v_j, int B, int H, int Hkv, long L, int d,
+                     int n, int causal, int layout, int i, int j, double* o_part, double* lse_part)
+{
+    if (!check_args(B, H, Hkv, L, d, n, layout) || i < 0 || i >= n || j < 0 || j >= n) return ORACLE_BAD_ARGS;
+    const long S = L / n;
+    const double scale = 1.0 / sqrt((double)d);
+    int status = ORACLE_OK;
+#pragma omp parallel
+    {
+        double* sc = (double*)malloc(sizeof(double) * S);
+        if (!sc) {
+#pragma omp atomic write
+            status = ORACLE_NO_MEMORY;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (long idx = 0; idx < (long)B * H * S; ++idx) {
+                const long u = idx % S; /* local row */
+                const int h = (int)((idx / S) % H);
+                const int b = (int)(idx / ((long)H * S));
+                const int g = h / (H / Hkv);
+                const long p = oracle_natural_position((long)i * S + u, L, n, layout);
+                const float* qrow = q_i + idx * d;
+                const float* kh = k_j + ((long)b * Hkv + g) * S * d;
+                const float* vh = v_j + ((long)b * Hkv + g) * S * d;
+                double mx = -INFINITY;
+                for (long t = 0; t < S; ++t) {
+                    if (causal && oracle_natural_position((long)j * S + t, L, n, layout) > p) {
+                        sc[t] = -INFINITY;
+                        continue;
+                    }
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c) acc += (double)qrow[c] * (double)kh[t * d + c];
+                    sc[t] = acc * scale;
+                    if (sc[t] > mx) mx = sc[t];
+                }
+                double* o = o_part + idx * d;
+                for (int c = 0; c < d; ++c) o[c] = 0.0;
+                if (mx == -INFINITY) { /* nothing of this block is visible */
+                    lse_part[idx] = -INFINITY;
+                    continue;
+                }
+                double sum = 0.0;
+                for (long t = 0; t < S; ++t) {
+                    if (sc[t] == -INFINITY) continue;
+                    const double e = exp(sc[t] - mx);
+                    sum += e;
+                    for (int c = 0; c < d; ++c) o[c] += e * (double)vh[t * d + c];
+                }
+                for (int c = 0; c < d; ++c) o[c] /= sum;
+                lse_part[idx] = mx + log(sum);
+            }
+        }
+        free(sc);
+    }
+    return status;
+}
+
+/* The backward contributions of one block by definition: only the pairs (query p of shard i, key t
+ * of shard j) with t visible to p, with P = exp(s - lse_p) from the query row's FULL log-sum-exp and
+ * D_p = <dO_p, O_p> of the full output (both given, [B][H][S], float64):
+ *   dq_part_p = scale sum_t dS_pt k_t,  dk_part_t = scale sum_{p, h in group} dS_pt q_p,
+ *   dv_part_t = sum_{p, h in group} P_pt dO_p,   dS_pt = P_pt (<dO_p, v_t> - D_p).
+ * dq_part [B][H][S][d], dk_part and dv_part [B][Hkv][S][d].  Summed over the n blocks these are
+ * the full gradients (oracle_attn_bwd). */
+int oracle_block_bwd(const float* q_i, const float* k_j, const float* v_j, const float* dout_i, const double* lse_i,
+                     const double* D_i, int B, int H, int Hkv, long L, int d, int n, int causal, int layout, int i,
+                     int j, double* dq_part, double* dk_part, double* dv_part)
+{
+    if (!check_args(B, H, Hkv, L, d, n, layout) || i < 0 || i >= n || j < 0 || j >= n) return ORACLE_BAD_ARGS;
+    const long S = L / n;
+    const int G = H / Hkv;
+    const double scale = 1.0 / sqrt((double)d);
+    /* dQ: one query row at a time */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long idx = 0; idx < (long)B * H * S; ++idx) {
+        const long u = idx % S;
+        const int h = (int)((idx / S) % H);
+        const int b = (int)(idx / ((long)H * S));
+        const int g = h / G;
+        const long p = oracle_natural_position((long)i * S + u, L, n, layout);
+        const float* qrow = q_i + idx * d;
+        const float* dorow = dout_i + idx * d;
+        const float* kh = k_j + ((long)b * Hkv + g) * S * d;
+        const float* vh = v_j + ((long)b * Hkv + g) * S * d;
+        double* out = dq_part + idx * d;
+        for (int c = 0; c < d; ++c) out[c] = 0.0;
+        for (long t = 0; t < S; ++t) {
+            if (causal && oracle_natural_position((long)j * S + t, L, n, layout) > p) continue;
+            double s = 0.0, dP = 0.0;
+            for (int c = 0; c < d; ++c) {
+                s += (double)qrow[c] * (double)kh[t * d + c];
+                dP += (double)dorow[c] * (double)vh[t * d + c];
+            }
+            const double P = exp(s * scale - lse_i[idx]);
+            const double dS = P * (dP - D_i[idx]);
+            for (int c = 0; c < d; ++c) out[c] += scale * dS * (double)kh[t * d + c];
+        }
+    }
+    /* dK, dV: one key row at a time, summed over the query heads of its group */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long kidx = 0; kidx < (long)B * Hkv * S; ++kidx) {
+        const long t = kidx % S;
+        const int g = (int)((kidx / S) % Hkv);
+        const int b = (int)(kidx / ((long)Hkv * S));
+        const long pt = oracle_natural_position((long)j * S + t, L, n, layout);
+        const float* krow = k_j + kidx * d;
+        const float* vrow = v_j + kidx * d;
+        double* dkx = dk_part + kidx * d;
+        double* dvx = dv_part + kidx * d;
+        for (int c = 0; c < d; ++c) { dkx[c] = 0.0; dvx[c] = 0.0; }
+        for (int hh = 0; hh < G; ++hh) {
+            const long hbase = ((long)b * H + (long)g * G + hh) * S;
+            for (long u = 0; u < S; ++u) {
+                if (causal && oracle_natural_position((long)i * S + u, L, n, layout) < pt) continue;
+                const long idx = hbase + u;
+                const float* qrow = q_i + idx * d;
+                const float* dorow = dout_i + idx * d;
+                double s = 0.0, dP = 0.0;
+                for (int c = 0; c < d; ++c) {
+                    s += (double)qrow[c] * (double)krow[c];
+                    dP += (double)dorow[c] * (double)vrow[c];
+                }
+                const double P = exp(s * scale - lse_i[idx]);
+                const double dS = P * (dP - D_i[idx]);
+                for (int c = 0; c < d; ++c) {
+                    dvx[c] += P * (double)dorow[c];
+                    dkx[c] += scale * dS * (double)qrow[c];
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* Rotary position embedding with natural positions.  [LLM101] section 6 (the questions after 6.2)
  * asks how position information must be treated once K/V blocks travel round the ring; reading C17: every row is rotated by the angle of
  * its NATURAL position p (its place in the whole sequence, from the layout), never by its buffer

@@ -20,6 +20,12 @@ from .binding import (  # noqa: F401
     bwd_static_scratch_capacity,
     fwd_path,
     bwd_path,
+    bwd_preprocess,
+    block_bwd,
+    block_fwd,
+    f32_add,
+    f32_convert,
+    f32_zero,
     library,
     lse_merge,
     ring_step_fwd,

@@ -34,6 +34,8 @@ EXPORTS = (
     "ring_attn_ulysses_bwd", "ring_attn_ulysses_bwd_workspace_size", "ring_attn_fwd_host",
     "ring_attn_ring_step_fwd_accumulate",
     "ring_attn_fwd_host_workspace_size", "ring_attn_selftest_bounded_wait", "ring_attn_device_check",
+    "ring_attn_block_fwd", "ring_attn_block_bwd", "ring_attn_bwd_preprocess", "ring_attn_f32_zero",
+    "ring_attn_f32_add", "ring_attn_f32_convert",
 )
 
 
@@ -70,6 +72,18 @@ def library():
         lib.ring_attn_device_status.argtypes = [P, P]
         lib.ring_attn_device_check.argtypes = [P]
         lib.ring_attn_device_check.restype = ctypes.c_int
+        lib.ring_attn_block_fwd.argtypes = [P, P, P, P, P] + [I] * 12 + [P]
+        lib.ring_attn_block_fwd.restype = ctypes.c_int
+        lib.ring_attn_block_bwd.argtypes = [P] * 9 + [I] * 12 + [P]
+        lib.ring_attn_block_bwd.restype = ctypes.c_int
+        lib.ring_attn_bwd_preprocess.argtypes = [P, P, P, LL, I, I, P]
+        lib.ring_attn_bwd_preprocess.restype = ctypes.c_int
+        lib.ring_attn_f32_zero.argtypes = [P, LL, P]
+        lib.ring_attn_f32_zero.restype = ctypes.c_int
+        lib.ring_attn_f32_add.argtypes = [P, P, LL, P]
+        lib.ring_attn_f32_add.restype = ctypes.c_int
+        lib.ring_attn_f32_convert.argtypes = [P, P, LL, I, P]
+        lib.ring_attn_f32_convert.restype = ctypes.c_int
         lib.ring_attn_last_error.argtypes = []
         lib.ring_attn_last_error.restype = ctypes.c_char_p
         lib.ring_attn_abi_version.argtypes = []
@@ -548,3 +562,91 @@ def device_check(stream=None, device=None):
     raises RingAttnError (status RA_ERR_TIMEOUT) if a bounded wait inside a kernel ran out."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     _check(library().ring_attn_device_check(_stream(stream, dev)))
+
+
+# ------------------------------------------------------------------------------------------------
+# One device of the multi-device ring: local shard buffers of S = L / n_shards rows per head
+# ------------------------------------------------------------------------------------------------
+def _need_block(q, k, v, n_shards, shard_q, shard_kv):
+    """q [B,H,S,d] (shard shard_q's rows), k and v [B,Hkv,S,d] (shard shard_kv's rows), same dtype and
+    device; returns (B, H, Hkv, S, d, L = n_shards * S)."""
+    B, H, Hkv, S, d = _need_qkv(q, k, v)
+    n = int(n_shards)
+    if n < 1 or not (0 <= int(shard_q) < n and 0 <= int(shard_kv) < n):
+        raise ValueError("shard indices must lie in [0, n_shards)")
+    return B, H, Hkv, S, d, n * S
+
+
+def block_fwd(q, k, v, o_acc, lse_acc, n_shards, shard_q, shard_kv, accumulate, causal=True, layout="zigzag",
+              stream=None):
+    """ring_attn_block_fwd: block attention of the local query shard shard_q against the K/V block of
+    shard shard_kv, written to (accumulate=False) or folded into (accumulate=True) the running state
+    o_acc [B,H,S,d] float32 (normalised output) and lse_acc [B,H,S] float32.  Returns (o_acc, lse_acc)."""
+    B, H, Hkv, S, d, L = _need_block(q, k, v, n_shards, shard_q, shard_kv)
+    _need(o_acc, "o_acc", q.device, (B, H, S, d), torch.float32)
+    _need(lse_acc, "lse_acc", q.device, (B, H, S), torch.float32)
+    _check(library().ring_attn_block_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o_acc), _ptr(lse_acc), B, H, Hkv, L, d,
+                                         int(n_shards), int(shard_q), int(shard_kv), int(bool(accumulate)),
+                                         int(causal), _layout(layout), _dtype_code(q.dtype),
+                                         _stream(stream, q.device)))
+    return o_acc, lse_acc
+
+
+def block_bwd(q, k, v, dout, lse, D, dq_acc, dk, dv, n_shards, shard_q, shard_kv, accumulate_kv, causal=True,
+              layout="zigzag", stream=None):
+    """ring_attn_block_bwd: the gradient contributions of the pairs (query of shard shard_q, key of shard
+    shard_kv): added into dq_acc [B,H,S,d] float32; added into (accumulate_kv=True) or stored to dk, dv
+    [B,Hkv,S,d] float32.  lse and D [B,H,S] float32 are the query rows' full log-sum-exp and
+    rowsum(dout * out).  Returns (dq_acc, dk, dv)."""
+    B, H, Hkv, S, d, L = _need_block(q, k, v, n_shards, shard_q, shard_kv)
+    _need(dout, "dout", q.device, q.shape, q.dtype)
+    _need(lse, "lse", q.device, (B, H, S), torch.float32)
+    _need(D, "D", q.device, (B, H, S), torch.float32)
+    _need(dq_acc, "dq_acc", q.device, (B, H, S, d), torch.float32)
+    _need(dk, "dk", q.device, (B, Hkv, S, d), torch.float32)
+    _need(dv, "dv", q.device, (B, Hkv, S, d), torch.float32)
+    _check(library().ring_attn_block_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(D), _ptr(dq_acc),
+                                         _ptr(dk), _ptr(dv), B, H, Hkv, L, d, int(n_shards), int(shard_q),
+                                         int(shard_kv), int(bool(accumulate_kv)), int(causal), _layout(layout),
+                                         _dtype_code(q.dtype), _stream(stream, q.device)))
+    return dq_acc, dk, dv
+
+
+def bwd_preprocess(out, dout, D=None, stream=None):
+    """ring_attn_bwd_preprocess: D = rowsum(out * dout) over the last dimension, float32."""
+    _need(out, "out", out.device)
+    _dtype_code(out.dtype)
+    _need(dout, "dout", out.device, out.shape, out.dtype)
+    if D is None:
+        D = torch.empty(out.shape[:-1], dtype=torch.float32, device=out.device)
+    _need(D, "D", out.device, out.shape[:-1], torch.float32)
+    d = int(out.shape[-1])
+    _check(library().ring_attn_bwd_preprocess(_ptr(out), _ptr(dout), _ptr(D), int(D.numel()), d,
+                                              _dtype_code(out.dtype), _stream(stream, out.device)))
+    return D
+
+
+def f32_zero(x, stream=None):
+    """ring_attn_f32_zero: x (float32) = 0.  Returns x."""
+    _need(x, "x", x.device, None, torch.float32)
+    _check(library().ring_attn_f32_zero(_ptr(x), int(x.numel()), _stream(stream, x.device)))
+    return x
+
+
+def f32_add(acc, part, stream=None):
+    """ring_attn_f32_add: acc += part (float32, same shape).  Returns acc."""
+    _need(acc, "acc", acc.device, None, torch.float32)
+    _need(part, "part", acc.device, acc.shape, torch.float32)
+    _check(library().ring_attn_f32_add(_ptr(acc), _ptr(part), int(acc.numel()), _stream(stream, acc.device)))
+    return acc
+
+
+def f32_convert(src, dtype, dst=None, stream=None):
+    """ring_attn_f32_convert: src (float32) converted to dtype (float32 or bfloat16).  Returns dst."""
+    _need(src, "src", src.device, None, torch.float32)
+    if dst is None:
+        dst = torch.empty(src.shape, dtype=dtype, device=src.device)
+    _need(dst, "dst", src.device, src.shape, dtype)
+    _check(library().ring_attn_f32_convert(_ptr(src), _ptr(dst), int(src.numel()), _dtype_code(dtype),
+                                           _stream(stream, src.device)))
+    return dst

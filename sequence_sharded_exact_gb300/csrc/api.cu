@@ -405,6 +405,128 @@ ra_status ring_attn_bwd_tile_visits(const void* q, const void* k, const void* v,
                     Problem{B, H, Hkv, L, d, n_shards, causal, layout, dtype}, visits, stream);
 }
 
+// ---------------------------------------------------------------------------------------------
+// One device's data path of the multi-device ring (block calls and their helpers)
+// ---------------------------------------------------------------------------------------------
+namespace {
+
+ra_status check_block(const Problem& p, int shard_q, int shard_kv, int flag, const char* flag_name)
+{
+    ra_status st = check_problem(p);
+    if (st != RA_OK) return st;
+    if (shard_q < 0 || shard_q >= p.n || shard_kv < 0 || shard_kv >= p.n)
+        return fail(RA_ERR_INVALID_ARG, "shard indices (%d, %d) outside [0, n_shards = %d)", shard_q, shard_kv, p.n);
+    if (flag != 0 && flag != 1) return fail(RA_ERR_INVALID_ARG, "%s must be 0 or 1 (got %d)", flag_name, flag);
+    return RA_OK;
+}
+
+ra_status check_count(long long count)
+{
+    if (count < 0) return fail(RA_ERR_INVALID_ARG, "count must be >= 0 (got %lld)", count);
+    return RA_OK;
+}
+
+}  // namespace
+
+ra_status ring_attn_block_fwd(const void* q, const void* k, const void* v, float* o_acc, float* lse_acc, int B,
+                              int H, int Hkv, int L, int d, int n_shards, int shard_q, int shard_kv, int accumulate,
+                              int causal, int layout, int dtype, void* stream)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_block(p, shard_q, shard_kv, accumulate, "accumulate");
+    if (st != RA_OK) return st;
+    if ((st = check_ptrs({q, k, v, o_acc, lse_acc})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const BlockView blk{shard_q, shard_kv, 0};
+    const int step = (shard_q - shard_kv + n_shards) % n_shards;
+    const int mode = accumulate ? kFwdRingStepAcc : kFwdRingStep;
+    cudaError_t e;
+    if (tc_fwd_supported(p)) {
+        unsigned int* sw = status_word(&e);
+        if (!sw) return cuda_fail(e, "status word");
+        e = launch_fwd_tc(p, q, k, v, o_acc, lse_acc, mode, step, sw, s, nullptr, &blk);
+    } else {
+        e = launch_fwd_simt(p, q, k, v, o_acc, lse_acc, mode, step, s, &blk);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_block_fwd launch");
+    return RA_OK;
+}
+
+ra_status ring_attn_block_bwd(const void* q, const void* k, const void* v, const void* dout, const float* lse,
+                              const float* D, float* dq_acc, float* dk, float* dv, int B, int H, int Hkv, int L,
+                              int d, int n_shards, int shard_q, int shard_kv, int accumulate_kv, int causal,
+                              int layout, int dtype, void* stream)
+{
+    Problem p{B, H, Hkv, L, d, n_shards, causal, layout, dtype};
+    ra_status st = check_block(p, shard_q, shard_kv, accumulate_kv, "accumulate_kv");
+    if (st != RA_OK) return st;
+    if ((st = check_ptrs({q, k, v, dout, lse, D, dq_acc, dk, dv})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const BlockView blk{shard_q, shard_kv, accumulate_kv};
+    cudaError_t e;
+    if (tc_bwd_supported(p)) {
+        unsigned int* sw = status_word(&e);
+        if (!sw) return cuda_fail(e, "status word");
+        e = launch_bwd_tc(p, q, k, v, dout, D, lse, dq_acc, dk, dv, RA_F32, sw, s, nullptr, &blk);
+    } else {
+        e = launch_bwd_simt(p, q, k, v, dout, D, lse, dq_acc, dk, dv, RA_F32, s, &blk);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_block_bwd launch");
+    return RA_OK;
+}
+
+ra_status ring_attn_bwd_preprocess(const void* out, const void* dout, float* D, long long rows, int d, int dtype,
+                                   void* stream)
+{
+    ra_status st = check_count(rows);
+    if (st != RA_OK) return st;
+    if (d < 1) return fail(RA_ERR_INVALID_ARG, "d must be >= 1");
+    if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (rows == 0) return RA_OK;
+    if ((st = check_ptrs({out, dout, D})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaError_t e = launch_bwd_preprocess(out, dout, dtype, rows, d, D, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_bwd_preprocess launch");
+    return RA_OK;
+}
+
+ra_status ring_attn_f32_zero(float* x, long long count, void* stream)
+{
+    ra_status st = check_count(count);
+    if (st != RA_OK || count == 0) return st;
+    if ((st = check_ptrs({x})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaError_t e = launch_zero(x, count, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_f32_zero launch");
+    return RA_OK;
+}
+
+ra_status ring_attn_f32_add(float* acc, const float* part, long long count, void* stream)
+{
+    ra_status st = check_count(count);
+    if (st != RA_OK || count == 0) return st;
+    if ((st = check_ptrs({acc, part})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaError_t e = launch_add(acc, part, count, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_f32_add launch");
+    return RA_OK;
+}
+
+ra_status ring_attn_f32_convert(const float* src, void* dst, long long count, int dtype, void* stream)
+{
+    ra_status st = check_count(count);
+    if (st != RA_OK) return st;
+    if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (count == 0) return RA_OK;
+    if ((st = check_ptrs({src, dst})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaError_t e = launch_convert(src, dst, dtype, count, 1.0f, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_f32_convert launch");
+    return RA_OK;
+}
+
 ra_status ring_attn_rope(void* x, int B, int H, int L, int d, int n_shards, int layout, int dtype,
                          double base, int inverse, void* stream)
 {

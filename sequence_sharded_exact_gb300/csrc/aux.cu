@@ -177,6 +177,21 @@ __global__ void __launch_bounds__(256) zero_kernel(float* __restrict__ dst, long
         dst[i] = 0.f;
 }
 
+__global__ void __launch_bounds__(256)
+add_kernel(float* __restrict__ acc, const float* __restrict__ part, long long count)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long n4 = count >> 2;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const float4 a = reinterpret_cast<const float4*>(acc)[i];
+        const float4 b = reinterpret_cast<const float4*>(part)[i];
+        reinterpret_cast<float4*>(acc)[i] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    }
+    for (long long i = (n4 << 2) + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+         i += stride)
+        acc[i] += part[i];
+}
+
 unsigned grid_for(long long work_items, int per_block)
 {
     const long long want = (work_items + per_block - 1) / per_block;
@@ -222,6 +237,13 @@ cudaError_t launch_zero(float* dst, long long count, cudaStream_t s)
 {
     if (count == 0) return cudaSuccess;
     zero_kernel<<<grid_for((count + 3) / 4, 256), 256, 0, s>>>(dst, count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_add(float* acc, const float* part, long long count, cudaStream_t s)
+{
+    if (count == 0) return cudaSuccess;
+    add_kernel<<<grid_for((count + 3) / 4, 256), 256, 0, s>>>(acc, part, count);
     return cudaGetLastError();
 }
 

@@ -10,7 +10,8 @@ namespace ra {
 bool tc_bwd_supported_d64(const Problem& p);
 cudaError_t launch_bwd_tc_d64(const Problem& p, const void* q, const void* k, const void* v, const void* dout,
                               const float* D, const float* lse, float* dq_acc, void* dk, void* dv, int grad_dtype,
-                              unsigned int* status, cudaStream_t s, unsigned long long* visits);
+                              unsigned int* status, cudaStream_t s, unsigned long long* visits,
+                              const BlockView* blk);
 
 bool tc_bwd_supported(const Problem& p)
 {
@@ -19,10 +20,11 @@ bool tc_bwd_supported(const Problem& p)
 
 cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const void* v, const void* dout,
                           const float* D, const float* lse, float* dq_acc, void* dk, void* dv, int grad_dtype,
-                          unsigned int* status, cudaStream_t s, unsigned long long* visits)
+                          unsigned int* status, cudaStream_t s, unsigned long long* visits, const BlockView* blk)
 {
-    return p.d == 64 ? launch_bwd_tc_d64(p, q, k, v, dout, D, lse, dq_acc, dk, dv, grad_dtype, status, s, visits)
-                     : launch_bwd_tc_d128(p, q, k, v, dout, D, lse, dq_acc, dk, dv, grad_dtype, status, s, visits);
+    return p.d == 64
+               ? launch_bwd_tc_d64(p, q, k, v, dout, D, lse, dq_acc, dk, dv, grad_dtype, status, s, visits, blk)
+               : launch_bwd_tc_d128(p, q, k, v, dout, D, lse, dq_acc, dk, dv, grad_dtype, status, s, visits, blk);
 }
 
 }  // namespace ra

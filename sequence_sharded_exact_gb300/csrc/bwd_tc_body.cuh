@@ -117,9 +117,16 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;
 struct BwdArgs {
     Geometry geo;
     int B, H, Hkv, G;
-    int T;            // 128-row K/V tiles per head (striped: per shard)
-    int pairs;        // mirrored tile pairs per kv head (striped: per shard)
+    int T;            // 128-row K/V tiles per head (striped, block call: per shard)
+    int pairs;        // mirrored tile pairs per kv head (striped, block call: per shard)
     long long items;  // B * Hkv * pairs (striped: B * Hkv * n * pairs)
+    // One device's block call: only the K/V tiles of shard kv_shard, met by the queries of shard
+    // (kv_shard + step) mod n at ring step `step` alone, with q / dout / lse / D / dq in local
+    // buffers of qL = S rows per head and k / v / dk / dv in local buffers of S rows: a
+    // whole-sequence row r is local row r - q_off (queries) or r - kv_off (keys).  dK and dV are then
+    // float32 and added to (acc_kv = 1) or stored (acc_kv = 0; a tile that meets no query gets zeros).
+    // Otherwise blk = 0, every step is walked, the offsets are 0 and qL = L.
+    int blk, kv_shard, step, q_off, kv_off, qL, acc_kv;
     const float* lse;
     const float* Dv;
     float* dq_acc;
@@ -159,7 +166,8 @@ __device__ __forceinline__ KvRange q_tile_range(const Geometry& g, int shard, in
 __device__ __forceinline__ int q_tiles_per_head(const BwdArgs& a, int shard, int pk)
 {
     int nt = 0;
-    for (int st = 0; st < a.geo.n; ++st)
+    const int s0 = a.blk ? a.step : 0, s1 = a.blk ? a.step + 1 : a.geo.n;
+    for (int st = s0; st < s1; ++st)
         for (int c = 0; c < a.geo.cps; ++c) nt += q_tile_range(a.geo, shard, st, c, pk).count / kQT;
     return nt;
 }
@@ -168,8 +176,10 @@ __device__ __forceinline__ bool unit_of(const BwdArgs& a, long long item, int me
 {
     const int pair = (int)(item % a.pairs);
     long long rest = item / a.pairs;
-    int shard = 0;
-    if (a.geo.layout == 2) {  // striped: tiles of consecutive rows inside one shard
+    // striped and block calls: tiles of consecutive rows inside one shard
+    const bool rowwise = a.geo.layout == 2 || a.blk;
+    int shard = a.blk ? a.kv_shard : 0;
+    if (a.geo.layout == 2 && !a.blk) {
         shard = (int)(rest % a.geo.n);
         rest /= a.geo.n;
     }
@@ -177,7 +187,7 @@ __device__ __forceinline__ bool unit_of(const BwdArgs& a, long long item, int me
     u.b = (int)(rest / a.Hkv);
     const int tile = member == 0 ? pair : a.T - 1 - pair;
     if (member == 1 && tile == pair) return false;
-    if (a.geo.layout == 2) {
+    if (rowwise) {
         u.rk = shard * a.geo.S + tile * kKT;
         u.pk = natural_position(a.geo, u.rk);
     } else {
@@ -224,12 +234,12 @@ __device__ __forceinline__ bool unit_in_slot(const BwdArgs& a, int s, KvUnit& u)
 // Query tiles of a unit: heads of the group in turn, each walking the query shards in ring order.
 struct QWalk {
     Geometry geo;
-    int shard, pk, st, c, t, nt, hh;
+    int shard, pk, st, st0, st1, c, t, nt, hh;
     KvRange qr;
     __device__ __forceinline__ void settle()
     {
         while (true) {
-            while (st < geo.n) {
+            while (st < st1) {
                 qr = q_tile_range(geo, shard, st, c, pk);
                 nt = qr.count / kQT;
                 if (nt > 0) return;
@@ -239,7 +249,7 @@ struct QWalk {
                 }
             }
             ++hh;
-            st = 0;
+            st = st0;
             c = 0;
             if (hh > 1 << 20) return;  // callers never walk past the unit's tile count
         }
@@ -249,7 +259,9 @@ struct QWalk {
         geo = a.geo;
         shard = u.shard;
         pk = u.pk;
-        st = 0;
+        st0 = a.blk ? a.step : 0;  // a block call walks its one ring step
+        st1 = a.blk ? a.step + 1 : a.geo.n;
+        st = st0;
         c = 0;
         t = 0;
         hh = 0;
@@ -387,7 +399,21 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
     for (int slot = 0; slot < slots; ++slot) {
         {
             KvUnit u;
-            if (!unit_in_slot(a, slot, u) || u.ntiles == 0) continue;
+            if (!unit_in_slot(a, slot, u)) continue;
+            if (u.ntiles == 0) {
+                // a block call's tile that meets no query in this block: stored gradients are zero
+                if (a.blk && !a.acc_kv) {
+                    const long long krow = ((long long)u.b * a.Hkv + u.g) * a.qL + (u.rk - a.kv_off) + r;
+#pragma unroll 1
+                    for (int which = 0; which < 2; ++which) {
+                        float4* d = reinterpret_cast<float4*>(static_cast<float*>(which == 0 ? a.dk : a.dv) +
+                                                              krow * kHd + w * (kHd / 2));
+#pragma unroll
+                        for (int e = 0; e < kHd / 8; ++e) d[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                continue;
+            }
             QWalk walk;
             walk.begin(a, u);
             for (int t = 0; t < u.ntiles; ++t, ++gt) {
@@ -433,7 +459,7 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
             if (!mbar_wait(bar(BAR_ACC_FULL), uc & 1, ctl)) goto done;
             tc_fence_after_sync();
             __syncwarp();
-            const long long krow = ((long long)u.b * a.Hkv + u.g) * a.geo.L + u.rk + r;
+            const long long krow = ((long long)u.b * a.Hkv + u.g) * a.qL + (u.rk - a.kv_off) + r;
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 const uint32_t col = (which == 0 ? kColDK : kColDV) + (uint32_t)w * (kHd / 2);
@@ -444,7 +470,15 @@ __device__ __forceinline__ void math_role(const BwdArgs& a, uint32_t sbase, uint
                     tmem_ld_32x32b_x32(tmem + lane_off + col + c * 32, x);
                     tmem_ld_wait(x);
                     const long long off = krow * kHd + w * (kHd / 2) + c * 32;
-                    if (a.grad_bf16) {
+                    if (a.acc_kv) {  // block call: add into the float32 gradients that travel with the block
+                        float4* d = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float4 y = d[e];
+                            d[e] = make_float4(y.x + __uint_as_float(x[4 * e]), y.y + __uint_as_float(x[4 * e + 1]),
+                                               y.z + __uint_as_float(x[4 * e + 2]), y.w + __uint_as_float(x[4 * e + 3]));
+                        }
+                    } else if (a.grad_bf16) {
                         uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
@@ -533,7 +567,7 @@ __device__ __forceinline__ void dq_role(const BwdArgs& a, uint32_t sbase, uint32
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(BAR_DQ_FREE));
                     const int zq = u.b * a.H + u.g * a.G + hh;
-                    float* dst = a.dq_acc + ((long long)zq * a.geo.L + qrow) * kHd + (dcol & 63);
+                    float* dst = a.dq_acc + ((long long)zq * a.qL + qrow - a.q_off) * kHd + (dcol & 63);
                     if (dq_c0 == 0)
                         red_group(dst, xa, 0, gap_ns);
                     else
@@ -548,7 +582,7 @@ __device__ __forceinline__ void dq_role(const BwdArgs& a, uint32_t sbase, uint32
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(BAR_DQ_FREE));
                     const int zq = u.b * a.H + u.g * a.G + hh;
-                    float* dst = a.dq_acc + ((long long)zq * a.geo.L + qrow) * kHd + dcol;
+                    float* dst = a.dq_acc + ((long long)zq * a.qL + qrow - a.q_off) * kHd + dcol;
                     red_group(dst, xa, 0, gap_ns);
                     red_group(dst, xb, 64, gap_ns);
                 }
@@ -581,11 +615,11 @@ __device__ __forceinline__ void producer_role(const BwdArgs& a, uint32_t sbase, 
             mbar_arrive_expect_tx(bar(BAR_KV_FULL), (kD64 ? 3 : 2) * kTileBytes);
 #pragma unroll
             for (int half = 0; half < kHalves; ++half) {
-                tma_load_3d(sbase + kSmemK + (uint32_t)half * kHalf, tmK, bar(BAR_KV_FULL), half * 64, u.rk, zkv);
-                tma_load_3d(sbase + kSmemV + (uint32_t)half * kHalf, tmV, bar(BAR_KV_FULL), half * 64, u.rk, zkv);
+                tma_load_3d(sbase + kSmemK + (uint32_t)half * kHalf, tmK, bar(BAR_KV_FULL), half * 64, u.rk - a.kv_off, zkv);
+                tma_load_3d(sbase + kSmemV + (uint32_t)half * kHalf, tmV, bar(BAR_KV_FULL), half * 64, u.rk - a.kv_off, zkv);
             }
             if constexpr (kD64)
-                tma_load_3d(sbase + kSmemK + kTileBytes, tmK, bar(BAR_KV_FULL), 0, u.rk, zkv);
+                tma_load_3d(sbase + kSmemK + kTileBytes, tmK, bar(BAR_KV_FULL), 0, u.rk - a.kv_off, zkv);
             ++uc;
             QWalk walk;
             walk.begin(a, u);
@@ -595,21 +629,21 @@ __device__ __forceinline__ void producer_role(const BwdArgs& a, uint32_t sbase, 
                 if (a.visits) atomicAdd(a.visits + (long long)(qrow / a.geo.S) * a.geo.n + u.shard, 1ull);
                 const uint32_t st = stage_of(qc), use = qc / kStages;
                 const int zq = u.b * a.H + u.g * a.G + hh;
-                const long long qbase = (long long)zq * a.geo.L + qrow;  // first row's index in lse / D
+                const long long qbase = (long long)zq * a.qL + qrow - a.q_off;  // first row's index in lse / D
                 // Q with its lse first: S^T and phase A need them; dO and D follow
                 if (use > 0 && !mbar_wait(bar(BAR_Q_EMPTY + (int)st), (use - 1) & 1, ctl)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(BAR_Q_FULL + (int)st), kTileBytes + kVecBytes);
 #pragma unroll
                 for (int half = 0; half < kHalves; ++half)
                     tma_load_3d(sbase + kSmemQ + st * kTileBytes + (uint32_t)half * kHalf, tmQ,
-                                bar(BAR_Q_FULL + (int)st), half * 64, qrow, zq);
+                                bar(BAR_Q_FULL + (int)st), half * 64, qrow - a.q_off, zq);
                 bulk_load_1d(sbase + kSmemLse + st * kVecBytes, a.lse + qbase, kVecBytes, bar(BAR_Q_FULL + (int)st));
                 if (use > 0 && !mbar_wait(bar(BAR_DO_EMPTY + (int)st), (use - 1) & 1, ctl)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(BAR_DO_FULL + (int)st), kTileBytes + kVecBytes);
 #pragma unroll
                 for (int half = 0; half < kHalves; ++half)
                     tma_load_3d(sbase + kSmemDO + st * kTileBytes + (uint32_t)half * kHalf, tmDO,
-                                bar(BAR_DO_FULL + (int)st), half * 64, qrow, zq);
+                                bar(BAR_DO_FULL + (int)st), half * 64, qrow - a.q_off, zq);
                 bulk_load_1d(sbase + kSmemD + st * kVecBytes, a.Dv + qbase, kVecBytes, bar(BAR_DO_FULL + (int)st));
             }
         }
@@ -892,27 +926,34 @@ bool RA_BWD_SUPPORTED(const Problem& p)
 
 cudaError_t RA_BWD_LAUNCH(const Problem& p, const void* q, const void* k, const void* v, const void* dout,
                           const float* D, const float* lse, float* dq_acc, void* dk, void* dv, int grad_dtype,
-                          unsigned int* status, cudaStream_t s, unsigned long long* visits)
+                          unsigned int* status, cudaStream_t s, unsigned long long* visits, const BlockView* blk)
 {
-    CUtensorMap tq, tk, tv, tdo;
-    if (!make_map(&tq, q, p.L, (long long)p.B * p.H, kQT) || !make_map(&tk, k, p.L, (long long)p.B * p.Hkv, kKT) ||
-        !make_map(&tv, v, p.L, (long long)p.B * p.Hkv, kKT) || !make_map(&tdo, dout, p.L, (long long)p.B * p.H, kQT))
-        return cudaErrorInvalidValue;
     BwdArgs a;
     a.geo = p.geo();
+    a.blk = blk ? 1 : 0;
+    a.kv_shard = blk ? blk->kv_shard : 0;
+    a.step = blk ? (blk->q_shard - blk->kv_shard + p.n) % p.n : 0;
+    a.q_off = blk ? blk->q_shard * a.geo.S : 0;
+    a.kv_off = blk ? blk->kv_shard * a.geo.S : 0;
+    a.qL = blk ? a.geo.S : p.L;  // rows per head of every buffer (local shard buffers in a block call)
+    a.acc_kv = blk ? blk->acc_kv : 0;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_map(&tq, q, a.qL, (long long)p.B * p.H, kQT) || !make_map(&tk, k, a.qL, (long long)p.B * p.Hkv, kKT) ||
+        !make_map(&tv, v, a.qL, (long long)p.B * p.Hkv, kKT) || !make_map(&tdo, dout, a.qL, (long long)p.B * p.H, kQT))
+        return cudaErrorInvalidValue;
     a.B = p.B;
     a.H = p.H;
     a.Hkv = p.Hkv;
     a.G = p.H / p.Hkv;
-    a.T = (p.layout == 2 ? p.L / p.n : p.L) / kKT;
+    a.T = (p.layout == 2 || blk ? p.L / p.n : p.L) / kKT;
     a.pairs = (a.T + 1) / 2;
-    a.items = (long long)p.B * p.Hkv * a.pairs * (p.layout == 2 ? p.n : 1);
+    a.items = (long long)p.B * p.Hkv * a.pairs * (p.layout == 2 && !blk ? p.n : 1);
     a.lse = lse;
     a.Dv = D;
     a.dq_acc = dq_acc;
     a.dk = dk;
     a.dv = dv;
-    a.grad_bf16 = grad_dtype == 1;
+    a.grad_bf16 = !blk && grad_dtype == 1;  // a block call's gradients are float32
     a.status = status;
     a.visits = visits;
     a.scale = 1.0f / sqrtf((float)kHd);

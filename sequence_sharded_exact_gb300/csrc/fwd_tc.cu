@@ -10,7 +10,7 @@ namespace ra {
 bool tc_fwd_supported_d64(const Problem& p);
 cudaError_t launch_fwd_tc_d64(const Problem& p, const void* q, const void* k, const void* v, void* out, float* lse,
                               int mode, int step, unsigned int* status, cudaStream_t s,
-                              unsigned long long* visits);
+                              unsigned long long* visits, const BlockView* blk);
 
 bool tc_fwd_supported(const Problem& p)
 {
@@ -18,10 +18,11 @@ bool tc_fwd_supported(const Problem& p)
 }
 
 cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v, void* out, float* lse,
-                          int mode, int step, unsigned int* status, cudaStream_t s, unsigned long long* visits)
+                          int mode, int step, unsigned int* status, cudaStream_t s, unsigned long long* visits,
+                          const BlockView* blk)
 {
-    return p.d == 64 ? launch_fwd_tc_d64(p, q, k, v, out, lse, mode, step, status, s, visits)
-                     : launch_fwd_tc_d128(p, q, k, v, out, lse, mode, step, status, s, visits);
+    return p.d == 64 ? launch_fwd_tc_d64(p, q, k, v, out, lse, mode, step, status, s, visits, blk)
+                     : launch_fwd_tc_d128(p, q, k, v, out, lse, mode, step, status, s, visits, blk);
 }
 
 }  // namespace ra

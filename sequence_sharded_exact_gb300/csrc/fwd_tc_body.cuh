@@ -86,9 +86,14 @@ struct FwdArgs {
     Geometry geo;
     int B, H, Hkv, G;
     int mode, step;
-    int U;           // 256-row blocks per head (striped: per shard)
-    int pairs;       // mirrored block pairs per head (striped: per shard)
+    int U;           // 256-row blocks per head (striped, block call: per shard)
+    int pairs;       // mirrored block pairs per head (striped, block call: per shard)
     long long items; // B * H * pairs (striped: B * H * n * pairs)
+    // One device's block call: only the rows of query shard q_shard, against one K/V block, with
+    // q / out / lse and k / v in local buffers of qL = S rows per head.  A whole-sequence buffer row
+    // r is local row r - q_off (queries) or r - kv_off (keys).  Otherwise blk = 0, the offsets are 0
+    // and qL = L.
+    int blk, q_shard, q_off, kv_off, qL;
     void* out;
     float* lse;
     unsigned int* status;
@@ -154,8 +159,10 @@ __device__ __forceinline__ bool unit_of(const FwdArgs& a, long long item, int me
 {
     const int pair = (int)(item % a.pairs);
     long long rest = item / a.pairs;
-    int shard = 0;
-    if (a.geo.layout == 2) {  // striped: blocks of consecutive rows inside one shard
+    // striped and block calls: blocks of consecutive rows inside one shard
+    const bool rowwise = a.geo.layout == 2 || a.blk;
+    int shard = a.blk ? a.q_shard : 0;
+    if (a.geo.layout == 2 && !a.blk) {
         shard = (int)(rest % a.geo.n);
         rest /= a.geo.n;
     }
@@ -166,7 +173,7 @@ __device__ __forceinline__ bool unit_of(const FwdArgs& a, long long item, int me
     u.h = u.g * a.G + hg;
     const int blk = member == 0 ? pair : a.U - 1 - pair;
     if (member == 1 && blk == pair) return false;
-    if (a.geo.layout == 2) {
+    if (rowwise) {
         u.r0 = shard * a.geo.S + blk * kBlock;
         u.p0 = natural_position(a.geo, u.r0);
     } else {
@@ -215,7 +222,7 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
         for (int member = 0; member < 2; ++member) {
             Unit u;
             if (!unit_of(a, item, member, u)) continue;
-            const long long row_g = ((long long)u.b * a.H + u.h) * a.geo.L + u.r0 + w * kTile + rw;
+            const long long row_g = ((long long)u.b * a.H + u.h) * a.qL + (u.r0 - a.q_off) + w * kTile + rw;
             if (u.ntiles == 0) {  // ring-step modes only: nothing visible from this block
                 if (a.mode == kFwdRingStepAcc) continue;  // the running result stays as it is
                 float* orow = static_cast<float*>(a.out) + row_g * kHd;
@@ -306,7 +313,13 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                     tmem_st_32x32b_x32(tS + half * 32, pk);
                 }
                 const float2 s2 = add2(add2(s4[0], s4[1]), add2(s4[2], s4[3]));
-                const float rsum = s2.x + s2.y;
+                // P V multiplies V by the weights rounded to bf16, while the sum above adds them
+                // unrounded.  For the tile's largest weight the difference is added to the sum, so that
+                // a row dominated by one key is normalised by exactly the weight its V row received
+                // (the same fma and ex2 as that element: the same value bit for bit).
+                const float p_max = ex2_approx(fmaf(mx, sl2, -ref));
+                const float p_max_bf16 = __uint_as_float(pack_bf16x2(p_max, 0.f) << 16);
+                const float rsum = s2.x + s2.y + (p_max_bf16 - p_max);
                 l_run = l_run * alpha + rsum;
                 tmem_st_wait();
                 const bool need = jj > 0 && alpha != 1.0f;
@@ -379,7 +392,8 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                     float4* dst = reinterpret_cast<float4*>(orow + c4 * 32);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float4 x = dst[e];
+                        // a running row with lse = -inf holds nothing yet: its o_acc is not read
+                        const float4 x = wa != 0.f ? dst[e] : make_float4(0.f, 0.f, 0.f, 0.f);
                         dst[e] = make_float4(wa * x.x + wb * __uint_as_float(o[4 * e]), wa * x.y + wb * __uint_as_float(o[4 * e + 1]),
                                              wa * x.z + wb * __uint_as_float(o[4 * e + 2]),
                                              wa * x.w + wb * __uint_as_float(o[4 * e + 3]));
@@ -431,7 +445,7 @@ __device__ __forceinline__ void producer_role(const FwdArgs& a, uint32_t sbase, 
 #pragma unroll
                 for (int half = 0; half < kHalves; ++half)
                     tma_load_3d(sbase + kSmemQ + (uint32_t)(w * kHalves + half) * kHalfBytes, tmQ, bar(BAR_Q_FULL),
-                                half * 64, u.r0 + w * kTile, zq);
+                                half * 64, u.r0 - a.q_off + w * kTile, zq);
             ++qc;
             const int zkv = u.b * a.Hkv + u.g;
             KvWalk walk;
@@ -449,13 +463,13 @@ __device__ __forceinline__ void producer_role(const FwdArgs& a, uint32_t sbase, 
 #pragma unroll
                 for (int half = 0; half < kHalves; ++half)
                     tma_load_3d(sbase + kSmemK + (uint32_t)stage * kTileBytes + (uint32_t)half * kHalfBytes, tmK,
-                                bar(BAR_K_FULL + stage), half * 64, kv_row, zkv);
+                                bar(BAR_K_FULL + stage), half * 64, kv_row - a.kv_off, zkv);
                 if (use > 0 && !mbar_wait(bar(BAR_V_EMPTY + stage), (use - 1) & 1, ctl)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(BAR_V_FULL + stage), kTileBytes);
 #pragma unroll
                 for (int half = 0; half < kHalves; ++half)
                     tma_load_3d(sbase + kSmemV + (uint32_t)stage * kTileBytes + (uint32_t)half * kHalfBytes, tmV,
-                                bar(BAR_V_FULL + stage), half * 64, kv_row, zkv);
+                                bar(BAR_V_FULL + stage), half * 64, kv_row - a.kv_off, zkv);
             }
         }
     }
@@ -697,23 +711,28 @@ bool RA_FWD_SUPPORTED(const Problem& p)
 
 cudaError_t RA_FWD_LAUNCH(const Problem& p, const void* q, const void* k, const void* v, void* out,
                           float* lse, int mode, int step, unsigned int* status, cudaStream_t s,
-                          unsigned long long* visits)
+                          unsigned long long* visits, const BlockView* blk)
 {
-    CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, q, p.L, (long long)p.B * p.H) || !make_map(&tk, k, p.L, (long long)p.B * p.Hkv) ||
-        !make_map(&tv, v, p.L, (long long)p.B * p.Hkv))
-        return cudaErrorInvalidValue;
     FwdArgs a;
     a.geo = p.geo();
+    a.blk = blk ? 1 : 0;
+    a.q_shard = blk ? blk->q_shard : 0;
+    a.q_off = blk ? blk->q_shard * a.geo.S : 0;
+    a.kv_off = blk ? blk->kv_shard * a.geo.S : 0;
+    a.qL = blk ? a.geo.S : p.L;  // rows per head of every buffer (local shard buffers in a block call)
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, q, a.qL, (long long)p.B * p.H) || !make_map(&tk, k, a.qL, (long long)p.B * p.Hkv) ||
+        !make_map(&tv, v, a.qL, (long long)p.B * p.Hkv))
+        return cudaErrorInvalidValue;
     a.B = p.B;
     a.H = p.H;
     a.Hkv = p.Hkv;
     a.G = p.H / p.Hkv;
     a.mode = mode;
     a.step = step;
-    a.U = (p.layout == 2 ? p.L / p.n : p.L) / kBlock;
+    a.U = (p.layout == 2 || blk ? p.L / p.n : p.L) / kBlock;
     a.pairs = (a.U + 1) / 2;
-    a.items = (long long)p.B * p.H * a.pairs * (p.layout == 2 ? p.n : 1);
+    a.items = (long long)p.B * p.H * a.pairs * (p.layout == 2 && !blk ? p.n : 1);
     a.out = out;
     a.lse = lse;
     a.status = status;

@@ -8,6 +8,10 @@
 // the row's natural position are never visited (airsota M4-051 section 3).
 // Backward: one warp per query row for dQ and one warp per key row for dK/dV, recomputing
 // P = exp(s - lse) from the saved lse.
+// Block calls (one device of the multi-device ring): the rows are those of one query shard and the
+// keys those of one K/V shard, in local buffers of qL = S rows per head; a whole-sequence buffer
+// row r is local row r - q_off (queries) or r - kv_off (keys).  Whole-sequence calls have zero
+// offsets and qL = L.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -59,21 +63,21 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                 void* __restrict__ out, float* __restrict__ lse, Geometry geo, int B, int H,
-                int Hkv, int mode, int step, float scale_log2)
+                int Hkv, int mode, int step, float scale_log2, int q_off, int kv_off, int qL)
 {
     constexpr int EPL = D / 32;
     __shared__ float qs[kWarps][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * kWarps + warp;
-    if (row >= (long long)B * H * geo.L) return;
-    const int r = (int)(row % geo.L);
-    const int h = (int)((row / geo.L) % H);
-    const int b = (int)(row / ((long long)geo.L * H));
+    if (row >= (long long)B * H * qL) return;
+    const int r = (int)(row % qL) + q_off;  // whole-sequence buffer row
+    const int h = (int)((row / qL) % H);
+    const int b = (int)(row / ((long long)qL * H));
     const int g = h / (H / Hkv);
     for (int c = lane; c < D; c += 32) qs[warp][c] = to_f(q[row * D + c]);
     __syncwarp();
-    const T* kh = k + ((long long)b * Hkv + g) * geo.L * D;
-    const T* vh = v + ((long long)b * Hkv + g) * geo.L * D;
+    const T* kh = k + ((long long)b * Hkv + g) * qL * D;  // key row t (whole sequence) is local row t - kv_off
+    const T* vh = v + ((long long)b * Hkv + g) * qL * D;
     const int i = r / geo.S;
     const int p = natural_position(geo, r);
 
@@ -88,7 +92,7 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
             for (int base = 0; base < kr.count; base += 32) {
                 const int t = base + lane;
                 float s = -INFINITY;
-                if (t < kr.count) s = dot_row<T, D>(qs[warp], kh + (long long)(kr.row0 + t) * D) * scale_log2;
+                if (t < kr.count) s = dot_row<T, D>(qs[warp], kh + (long long)(kr.row0 - kv_off + t) * D) * scale_log2;
                 const float m_new = fmaxf(m, warp_max(s));
                 const float ref = m_new == -INFINITY ? 0.f : m_new;
                 const float alpha = exp2f(m - ref);
@@ -99,7 +103,7 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
                 const int nvalid = min(32, kr.count - base);
                 for (int tt = 0; tt < nvalid; ++tt) {
                     const float pt = __shfl_sync(kFull, pr, tt);
-                    const T* vrow = vh + (long long)(kr.row0 + base + tt) * D;
+                    const T* vrow = vh + (long long)(kr.row0 - kv_off + base + tt) * D;
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) o[e] = fmaf(pt, to_f(vrow[lane + 32 * e]), o[e]);
                 }
@@ -124,8 +128,9 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
         const float wa = acc == -INFINITY ? 0.f : expf(acc - nl);
         const float wb = expf(b - nl) / l;
         float* orow = static_cast<float*>(out) + row * D;
+        // a running row with lse = -inf holds nothing yet: its o_acc is not read
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) orow[lane + 32 * e] = wa * orow[lane + 32 * e] + wb * o[e];
+        for (int e = 0; e < EPL; ++e) orow[lane + 32 * e] = (wa != 0.f ? wa * orow[lane + 32 * e] : 0.f) + wb * o[e];
         if (lane == 0) lse[row] = nl;
     } else {
         float* orow = static_cast<float*>(out) + row * D;
@@ -145,25 +150,26 @@ __global__ void __launch_bounds__(kWarps * 32)
 bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    const T* __restrict__ dout, const float* __restrict__ Dv,
                    const float* __restrict__ lse, G* __restrict__ dq, Geometry geo, int B, int H,
-                   int Hkv, float scale, float scale_log2)
+                   int Hkv, float scale, float scale_log2, int s0, int s1, int q_off, int kv_off, int qL,
+                   int acc_dq)
 {
     constexpr int EPL = D / 32;
     __shared__ float qs[kWarps][D];
     __shared__ float ds[kWarps][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * kWarps + warp;
-    if (row >= (long long)B * H * geo.L) return;
-    const int r = (int)(row % geo.L);
-    const int h = (int)((row / geo.L) % H);
-    const int b = (int)(row / ((long long)geo.L * H));
+    if (row >= (long long)B * H * qL) return;
+    const int r = (int)(row % qL) + q_off;  // whole-sequence buffer row
+    const int h = (int)((row / qL) % H);
+    const int b = (int)(row / ((long long)qL * H));
     const int g = h / (H / Hkv);
     for (int c = lane; c < D; c += 32) {
         qs[warp][c] = to_f(q[row * D + c]);
         ds[warp][c] = to_f(dout[row * D + c]);
     }
     __syncwarp();
-    const T* kh = k + ((long long)b * Hkv + g) * geo.L * D;
-    const T* vh = v + ((long long)b * Hkv + g) * geo.L * D;
+    const T* kh = k + ((long long)b * Hkv + g) * qL * D;  // key row t (whole sequence) is local row t - kv_off
+    const T* vh = v + ((long long)b * Hkv + g) * qL * D;
     const int i = r / geo.S;
     const int p = natural_position(geo, r);
     const float lse2 = lse[row] * kLog2e;
@@ -171,14 +177,14 @@ bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     float acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-    for (int st = 0; st < geo.n; ++st) {
+    for (int st = s0; st < s1; ++st) {
         for (int c = 0; c < geo.cps; ++c) {
             const KvRange kr = kv_range(geo, i, st, c, p);
             for (int base = 0; base < kr.count; base += 32) {
                 const int t = base + lane;
                 float dS = 0.f;
                 if (t < kr.count) {
-                    const long long kv = (long long)(kr.row0 + t) * D;
+                    const long long kv = (long long)(kr.row0 - kv_off + t) * D;
                     const float s = dot_row<T, D>(qs[warp], kh + kv) * scale_log2;
                     const float dP = dot_row<T, D>(ds[warp], vh + kv);
                     dS = exp2f(s - lse2) * (dP - Drow);
@@ -186,7 +192,7 @@ bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
                 const int nvalid = min(32, kr.count - base);
                 for (int tt = 0; tt < nvalid; ++tt) {
                     const float w = __shfl_sync(kFull, dS, tt);
-                    const T* krow = kh + (long long)(kr.row0 + base + tt) * D;
+                    const T* krow = kh + (long long)(kr.row0 - kv_off + base + tt) * D;
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, to_f(krow[lane + 32 * e]), acc[e]);
                 }
@@ -194,7 +200,10 @@ bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
         }
     }
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) dq[row * D + lane + 32 * e] = from_f<G>(acc[e] * scale);
+    for (int e = 0; e < EPL; ++e) {
+        const long long x = row * D + lane + 32 * e;
+        dq[x] = from_f<G>(acc_dq ? to_f(dq[x]) + acc[e] * scale : acc[e] * scale);
+    }
 }
 
 // One warp per key row t of kv head (b, g): the query rows that see it are visited shard by shard
@@ -204,17 +213,18 @@ __global__ void __launch_bounds__(kWarps * 32)
 bwd_dkv_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                     const T* __restrict__ dout, const float* __restrict__ Dv,
                     const float* __restrict__ lse, G* __restrict__ dk, G* __restrict__ dv,
-                    Geometry geo, int B, int H, int Hkv, float scale, float scale_log2)
+                    Geometry geo, int B, int H, int Hkv, float scale, float scale_log2, int s0, int s1,
+                    int q_off, int kv_off, int qL, int acc_kv)
 {
     constexpr int EPL = D / 32;
     __shared__ float ks[kWarps][D];
     __shared__ float vs[kWarps][D];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long krow = (long long)blockIdx.x * kWarps + warp;
-    if (krow >= (long long)B * Hkv * geo.L) return;
-    const int t = (int)(krow % geo.L);
-    const int g = (int)((krow / geo.L) % Hkv);
-    const int b = (int)(krow / ((long long)geo.L * Hkv));
+    if (krow >= (long long)B * Hkv * qL) return;
+    const int t = (int)(krow % qL) + kv_off;  // whole-sequence buffer row
+    const int g = (int)((krow / qL) % Hkv);
+    const int b = (int)(krow / ((long long)qL * Hkv));
     const int G_ = H / Hkv;
     for (int c = lane; c < D; c += 32) {
         ks[warp][c] = to_f(k[krow * D + c]);
@@ -227,8 +237,9 @@ bwd_dkv_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
 #pragma unroll
     for (int e = 0; e < EPL; ++e) ak[e] = av[e] = 0.f;
     for (int hh = 0; hh < G_; ++hh) {
-        const long long hb = ((long long)b * H + (long long)g * G_ + hh) * geo.L;
-        for (int st = 0; st < geo.n; ++st) {
+        // local query row = whole-sequence row - q_off
+        const long long hb = ((long long)b * H + (long long)g * G_ + hh) * qL - q_off;
+        for (int st = s0; st < s1; ++st) {
             for (int c = 0; c < geo.cps; ++c) {
                 const KvRange qr = q_range(geo, j, st, c, pt);
                 for (int base = 0; base < qr.count; base += 32) {
@@ -258,80 +269,97 @@ bwd_dkv_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
     }
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
-        dk[krow * D + lane + 32 * e] = from_f<G>(ak[e] * scale);
-        dv[krow * D + lane + 32 * e] = from_f<G>(av[e]);
+        const long long x = krow * D + lane + 32 * e;
+        dk[x] = from_f<G>(acc_kv ? to_f(dk[x]) + ak[e] * scale : ak[e] * scale);
+        dv[x] = from_f<G>(acc_kv ? to_f(dv[x]) + av[e] : av[e]);
     }
+}
+
+// Row addressing of a call: whole-sequence buffers, or one device's block call (local shard buffers).
+struct Rows {
+    int q_off, kv_off, qL;
+};
+
+Rows rows_of(const Problem& p, const BlockView* blk)
+{
+    const int S = p.L / p.n;
+    return blk ? Rows{blk->q_shard * S, blk->kv_shard * S, S} : Rows{0, 0, p.L};
 }
 
 template <typename T, int D>
 cudaError_t fwd_simt_typed(const Problem& p, const void* q, const void* k, const void* v,
-                           void* out, float* lse, int mode, int step, cudaStream_t s)
+                           void* out, float* lse, int mode, int step, cudaStream_t s, const BlockView* blk)
 {
-    const long long rows = p.q_rows();
+    const Rows rw = rows_of(p, blk);
+    const long long rows = (long long)p.B * p.H * rw.qL;
     const unsigned grid = (unsigned)((rows + kWarps - 1) / kWarps);
     const float scale_log2 = kLog2e / sqrtf((float)D);
     fwd_simt_kernel<T, D><<<grid, kWarps * 32, 0, s>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), out, lse,
-        p.geo(), p.B, p.H, p.Hkv, mode, step, scale_log2);
+        p.geo(), p.B, p.H, p.Hkv, mode, step, scale_log2, rw.q_off, rw.kv_off, rw.qL);
     return cudaGetLastError();
 }
 
 template <typename T, typename G, int D>
 cudaError_t bwd_simt_typed(const Problem& p, const void* q, const void* k, const void* v,
                            const void* dout, const float* Dv, const float* lse, void* dq,
-                           void* dk, void* dv, cudaStream_t s)
+                           void* dk, void* dv, cudaStream_t s, const BlockView* blk)
 {
     const float scale = 1.f / sqrtf((float)D);
     const float scale_log2 = kLog2e * scale;
-    const unsigned gq = (unsigned)((p.q_rows() + kWarps - 1) / kWarps);
+    const Rows rw = rows_of(p, blk);
+    // a block call walks its one ring step and adds dQ (and, if asked, dK, dV) into float32 outputs
+    const int s0 = blk ? (blk->q_shard - blk->kv_shard + p.n) % p.n : 0;
+    const int s1 = blk ? s0 + 1 : p.n;
+    const unsigned gq = (unsigned)(((long long)p.B * p.H * rw.qL + kWarps - 1) / kWarps);
     bwd_dq_simt_kernel<T, G, D><<<gq, kWarps * 32, 0, s>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
         static_cast<const T*>(dout), Dv, lse, static_cast<G*>(dq), p.geo(), p.B, p.H, p.Hkv, scale,
-        scale_log2);
+        scale_log2, s0, s1, rw.q_off, rw.kv_off, rw.qL, blk ? 1 : 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const unsigned gk = (unsigned)((p.kv_rows() + kWarps - 1) / kWarps);
+    const unsigned gk = (unsigned)(((long long)p.B * p.Hkv * rw.qL + kWarps - 1) / kWarps);
     bwd_dkv_simt_kernel<T, G, D><<<gk, kWarps * 32, 0, s>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
         static_cast<const T*>(dout), Dv, lse, static_cast<G*>(dk), static_cast<G*>(dv), p.geo(),
-        p.B, p.H, p.Hkv, scale, scale_log2);
+        p.B, p.H, p.Hkv, scale, scale_log2, s0, s1, rw.q_off, rw.kv_off, rw.qL, blk ? blk->acc_kv : 0);
     return cudaGetLastError();
 }
 
 template <typename T, int D>
 cudaError_t bwd_simt_grad(const Problem& p, const void* q, const void* k, const void* v,
                           const void* dout, const float* Dv, const float* lse, void* dq, void* dk,
-                          void* dv, int grad_dtype, cudaStream_t s)
+                          void* dv, int grad_dtype, cudaStream_t s, const BlockView* blk)
 {
-    if (grad_dtype == 0)
-        return bwd_simt_typed<T, float, D>(p, q, k, v, dout, Dv, lse, dq, dk, dv, s);
-    return bwd_simt_typed<T, __nv_bfloat16, D>(p, q, k, v, dout, Dv, lse, dq, dk, dv, s);
+    if (grad_dtype == 0 || blk)  // a block call's gradients are float32
+        return bwd_simt_typed<T, float, D>(p, q, k, v, dout, Dv, lse, dq, dk, dv, s, blk);
+    return bwd_simt_typed<T, __nv_bfloat16, D>(p, q, k, v, dout, Dv, lse, dq, dk, dv, s, blk);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_simt(const Problem& p, const void* q, const void* k, const void* v,
-                            void* out, float* lse, int mode, int step, cudaStream_t s)
+                            void* out, float* lse, int mode, int step, cudaStream_t s, const BlockView* blk)
 {
     if (p.dtype == 0)
-        return p.d == 64 ? fwd_simt_typed<float, 64>(p, q, k, v, out, lse, mode, step, s)
-                         : fwd_simt_typed<float, 128>(p, q, k, v, out, lse, mode, step, s);
-    return p.d == 64 ? fwd_simt_typed<__nv_bfloat16, 64>(p, q, k, v, out, lse, mode, step, s)
-                     : fwd_simt_typed<__nv_bfloat16, 128>(p, q, k, v, out, lse, mode, step, s);
+        return p.d == 64 ? fwd_simt_typed<float, 64>(p, q, k, v, out, lse, mode, step, s, blk)
+                         : fwd_simt_typed<float, 128>(p, q, k, v, out, lse, mode, step, s, blk);
+    return p.d == 64 ? fwd_simt_typed<__nv_bfloat16, 64>(p, q, k, v, out, lse, mode, step, s, blk)
+                     : fwd_simt_typed<__nv_bfloat16, 128>(p, q, k, v, out, lse, mode, step, s, blk);
 }
 
 cudaError_t launch_bwd_simt(const Problem& p, const void* q, const void* k, const void* v,
                             const void* dout, const float* Dv, const float* lse, void* dq,
-                            void* dk, void* dv, int grad_dtype, cudaStream_t s)
+                            void* dk, void* dv, int grad_dtype, cudaStream_t s, const BlockView* blk)
 {
     if (p.dtype == 0)
         return p.d == 64
-                   ? bwd_simt_grad<float, 64>(p, q, k, v, dout, Dv, lse, dq, dk, dv, grad_dtype, s)
-                   : bwd_simt_grad<float, 128>(p, q, k, v, dout, Dv, lse, dq, dk, dv, grad_dtype, s);
+                   ? bwd_simt_grad<float, 64>(p, q, k, v, dout, Dv, lse, dq, dk, dv, grad_dtype, s, blk)
+                   : bwd_simt_grad<float, 128>(p, q, k, v, dout, Dv, lse, dq, dk, dv, grad_dtype, s, blk);
     return p.d == 64 ? bwd_simt_grad<__nv_bfloat16, 64>(p, q, k, v, dout, Dv, lse, dq, dk, dv,
-                                                        grad_dtype, s)
+                                                        grad_dtype, s, blk)
                      : bwd_simt_grad<__nv_bfloat16, 128>(p, q, k, v, dout, Dv, lse, dq, dk, dv,
-                                                         grad_dtype, s);
+                                                         grad_dtype, s, blk);
 }
 
 }  // namespace ra

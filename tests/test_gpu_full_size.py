@@ -1,5 +1,18 @@
-"""Full-size workloads (the sizes the benchmark times), checked on sampled rows the oracle computes
-one by one, plus properties that hold at any size."""
+"""Full-size workloads (the sizes the benchmark times) against the float64 oracle.
+
+Depth of the element-by-element checks, per workload:
+  * causal_contig_8k (B2 H8 L8192, contiguous): every element of out and lse;
+  * zigzag_gqa_32k (H32 Hkv8 L32768): the first and the last kv-head group in full (4 query heads x
+    32768 rows each) plus 4096 seeded rows of the other heads;
+  * zigzag_gqa_128k (H32 Hkv8 L131072, 1% of keys x8): one whole query head (131072 rows) plus 4096
+    seeded rows over all heads;
+  * zigzag_gqa_64k_train (L65536, n16): dQ on 4096 seeded rows; dK and dV on keys of one kv head
+    spread over the whole natural range -- natural positions 0-127 (every query of the group sees
+    them: the longest accumulations), the first and last key of every chunk, and seeded random keys;
+  * the striped workloads and a 262144-token sequence: sampled rows plus chunk edges.
+Every check reports max-abs and relative L2 error per tensor; the bound is the bf16 one (max-abs 2e-2
+and relative L2 5e-3, both).  Properties that hold at any size (finite outputs, sum identities of
+the gradients) are checked as well."""
 import numpy as np
 import pytest
 import torch
@@ -36,8 +49,111 @@ def sampled_rows(w, count, seed):
     return np.array(sorted(rows), dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", ["causal_contig_8k", "zigzag_gqa_32k", "zigzag_gqa_128k",
-                                  "zigzag_gqa_64k_train", "striped_gqa_128k"])
+def report(capsys, name, what, got, ref):
+    """Max-abs and relative L2 error of one tensor, printed to the terminal and checked."""
+    ma, rl = errors(got, ref)
+    with capsys.disabled():
+        print(f"\n[parity] {name} {what}: {np.asarray(ref).size} values, max-abs {ma:.3e}, rel-L2 {rl:.3e}")
+    assert ma <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"{name} {what}: max-abs {ma:.3e}, rel-L2 {rl:.3e}"
+
+
+def head_rows(w, heads):
+    """Flat row indices (b*H + h)*L + r of every row of the given query heads (all batches)."""
+    B, H, L = w["B"], w["H"], w["L"]
+    return np.concatenate([np.arange(((b * H + h) * L), ((b * H + h) * L) + L, dtype=np.int64)
+                           for b in range(B) for h in heads])
+
+
+def test_causal_contig_8k_every_element(capsys):
+    name = "causal_contig_8k"
+    w = synth.WORKLOADS[name]
+    B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
+    x = synth.make_workload(name, device=DEV, gen_device=DEV, with_dout=False)
+    assert ra.fwd_path(B, H, Hkv, L, d, n, w["causal"], w["layout"], w["dtype"]) == "tcgen05"
+    out, lse = ra.fwd(x["q"], x["k"], x["v"], n, w["causal"], w["layout"])
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.attn_fwd(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), n, w["causal"], w["layout"])
+    report(capsys, name, "out (every element)", to_np(out), ref_o)
+    report(capsys, name, "lse (every element)", to_np(lse), ref_l)
+
+
+def test_zigzag_gqa_32k_full_kv_groups(capsys):
+    name = "zigzag_gqa_32k"
+    w = synth.WORKLOADS[name]
+    B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
+    G = H // Hkv
+    x = synth.make_workload(name, device=DEV, gen_device=DEV, with_dout=False)
+    out, lse = ra.fwd(x["q"], x["k"], x["v"], n, w["causal"], w["layout"])
+    torch.cuda.synchronize()
+    host = {t: x[t].cpu() for t in ("q", "k", "v")}
+    first, last = list(range(G)), list(range(H - G, H))
+    rng = np.random.default_rng(32768)
+    others = np.sort(rng.choice(np.arange(G * L, (H - G) * L), size=4096, replace=False))
+    for what, rows in (("kv group 0 (heads 0-3, every row)", head_rows(w, first)),
+                       (f"kv group {Hkv - 1} (heads {H - G}-{H - 1}, every row)", head_rows(w, last)),
+                       ("4096 seeded rows of heads 4-27", others)):
+        ref_o, ref_l = oracle.attn_fwd_rows(host["q"], host["k"], host["v"], n, w["causal"], w["layout"], rows)
+        idx = torch.from_numpy(rows).to(DEV)
+        report(capsys, name, "out, " + what, to_np(out.view(-1, d)[idx]), ref_o)
+        report(capsys, name, "lse, " + what, to_np(lse.view(-1)[idx]), ref_l)
+
+
+def test_zigzag_gqa_128k_full_head_and_rows(capsys):
+    name = "zigzag_gqa_128k"
+    w = synth.WORKLOADS[name]
+    B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
+    x = synth.make_workload(name, device=DEV, gen_device=DEV, with_dout=False)
+    out, lse = ra.fwd(x["q"], x["k"], x["v"], n, w["causal"], w["layout"])
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all().item() and torch.isfinite(lse).all().item()
+    host = {t: x[t].cpu() for t in ("q", "k", "v")}
+    rng = np.random.default_rng(131072)
+    for what, rows in ((f"head {H - 1} (every row)", head_rows(w, [H - 1])),
+                       ("4096 seeded rows of all heads", np.sort(rng.choice(B * H * L, size=4096, replace=False)))):
+        ref_o, ref_l = oracle.attn_fwd_rows(host["q"], host["k"], host["v"], n, w["causal"], w["layout"], rows)
+        idx = torch.from_numpy(rows).to(DEV)
+        report(capsys, name, "out, " + what, to_np(out.view(-1, d)[idx]), ref_o)
+        report(capsys, name, "lse, " + what, to_np(lse.view(-1)[idx]), ref_l)
+
+
+def test_training_backward_over_the_whole_range(capsys):
+    """dQ on 4096 seeded rows; dK and dV on keys of the last kv head at natural positions 0-127, at
+    the first and last position of every chunk (the first keys of every shard), and at 64 seeded
+    random positions."""
+    name = "zigzag_gqa_64k_train"
+    w = synth.WORKLOADS[name]
+    B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
+    x = synth.make_workload(name, device=DEV, gen_device=DEV, with_dout=True)
+    assert ra.bwd_path(B, H, Hkv, L, d, n, w["causal"], w["layout"], w["dtype"]) == "tcgen05"
+    out, lse = ra.fwd(x["q"], x["k"], x["v"], n, w["causal"], w["layout"])
+    dq, dk, dv = ra.bwd(x["q"], x["k"], x["v"], out, lse, x["dout"], n, w["causal"], w["layout"])
+    torch.cuda.synchronize()
+    host = {t: x[t].cpu() for t in ("q", "k", "v", "dout")}
+    rng = np.random.default_rng(65536)
+    rows = np.sort(rng.choice(B * H * L, size=4096, replace=False))
+    ref_dq = oracle.attn_bwd_dq_rows(host["q"], host["k"], host["v"], host["dout"], n, w["causal"], w["layout"], rows)
+    report(capsys, name, "dq, 4096 seeded rows", to_np(dq.view(-1, d)[torch.from_numpy(rows).to(DEV)]), ref_dq)
+    # natural position -> buffer row of the layout, from the oracle's own position map
+    nat = np.array([oracle.natural_position(r, L, n, w["layout"]) for r in range(L)], dtype=np.int64)
+    row_of = np.empty(L, dtype=np.int64)
+    row_of[nat] = np.arange(L)
+    chunk = L // (2 * n)
+    positions = set(range(128))
+    for c in range(L // chunk):
+        positions.update((c * chunk, c * chunk + chunk - 1))
+    positions.update(rng.choice(L, size=64, replace=False).tolist())
+    g = Hkv - 1
+    keys = np.array(sorted(((B - 1) * Hkv + g) * L + int(row_of[p]) for p in positions), dtype=np.int64)
+    assert keys.size >= 64
+    ref_dk, ref_dv = oracle.attn_bwd_dkv_rows(host["q"], host["k"], host["v"], host["dout"], n, w["causal"],
+                                              w["layout"], keys)
+    idx = torch.from_numpy(keys).to(DEV)
+    what = f"{keys.size} keys of kv head {g} (positions 0-127, every chunk edge, 64 seeded)"
+    report(capsys, name, "dk, " + what, to_np(dk.view(-1, d)[idx]), ref_dk)
+    report(capsys, name, "dv, " + what, to_np(dv.view(-1, d)[idx]), ref_dv)
+
+
+@pytest.mark.parametrize("name", ["zigzag_gqa_64k_train", "striped_gqa_128k"])
 def test_full_size_forward_sampled_rows(name):
     w = synth.WORKLOADS[name]
     B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
