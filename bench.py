@@ -10,8 +10,12 @@ kernel + LSE merge per step) on the long-context workload, and the merge kernel'
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}] [--no-extra]
 
 --impl reference times the float64 CPU oracle on a bounded sample of the same workload.
-For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of the workload (the
-sharded multi-device ring is not exercised on one-GPU machines); value = all ranks' work / max time.
+For N > 1 (torchrun, one rank per GPU) the workload is split over the N devices as the pages
+describe: n = N shards of L / N tokens, one per device, each device computing its shard's block
+attention against the K/V block it holds and passing the block round the ring over NCCL while it
+computes (sequence_sharded_exact_gb300.ring); value = the whole sequence's work / the slowest
+rank's time (strong scaling: the same workload at every N).  --ring runs that path at N = 1 too (one
+device, one block); --replicas gives the older mode, one independent copy of the workload per rank.
 """
 from __future__ import annotations
 
@@ -80,6 +84,25 @@ def max_over_ranks(value, dist_mod=None, device="cpu"):
 def whole_job_tflops(world, flops_per_step, steps, max_total_ms):
     """All ranks' algorithmic work over the slowest rank's time, in TFLOP/s."""
     return world * flops_per_step * steps / (max_total_ms / 1e3) / 1e12
+
+
+# NVIDIA's published dense BF16 tensor-core rate of one GB300 (Blackwell Ultra) GPU: the GB300 NVL72
+# figure of 360 PFLOPS FP16/BF16 for 72 GPUs is quoted with 2:4 sparsity, i.e. 2.5 PFLOP/s dense per
+# GPU (the HGX B300 figure of 36 PFLOPS for 8 GPUs, also sparse, gives 2.25 dense per GPU).
+PUBLISHED_BF16_DENSE_TFLOPS = 2500.0
+PUBLISHED_BF16_SOURCE = ("NVIDIA GB300 NVL72 specifications: 360 PFLOPS FP16/BF16 tensor (with sparsity) for "
+                         "72 GPUs = 2.5 PFLOP/s dense per GPU")
+# Dense bf16 tcgen05 rate per SM and clock: one 128 x 128 x 16 MMA (524288 flop) every 64 cycles,
+# measured on this GPU with a microbenchmark of back-to-back tcgen05.mma instructions.
+FLOP_PER_CLK_PER_SM = 8192
+
+
+def per_clock_peak_tflops(sm_mhz):
+    """SMs x 8192 flop/clock x the SM clock sampled under load (TFLOP/s), or None."""
+    if not sm_mhz or not torch.cuda.is_available():
+        return None
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * FLOP_PER_CLK_PER_SM * sm_mhz * 1e6 / 1e12
 
 
 def peaks():
@@ -270,6 +293,10 @@ def main():
                          "fwd, the 64K training workload for --step train)")
     ap.add_argument("--step", default="fwd", choices=["fwd", "train"],
                     help="fwd: one ring-attention forward per step; train: forward + backward")
+    ap.add_argument("--ring", action="store_true",
+                    help="run the multi-device ring path also at N = 1 (the default for N > 1)")
+    ap.add_argument("--replicas", action="store_true",
+                    help="N > 1: one independent copy of the workload per rank instead of the ring")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -287,6 +314,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.ring or (world > 1 and not args.replicas):
+        run_ring(args, w, world, rank, local)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist_mod
@@ -433,19 +463,229 @@ def main():
         del h_in, h_out
 
     line["clocks"] = clk.summary()
+    add_peak_fractions(line["roofline"], line["clocks"])
 
     if rank == 0 and not args.no_extra and not train:
         line["extra"] = secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args)
-    if rank == 0:
+    if rank == 0 and world == 1:
         arrs, count = oracle_calibrate(x, w, args.oracle_seconds)
         tf, secs, rows, cores, oflops = oracle_sample(arrs, w, count, seed=11)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{rows} random query rows of the workload "
                                           f"({oflops / 1e9:.1f} GFLOP, {secs:.1f} s, float64)"}
+    if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def add_peak_fractions(roof, clocks):
+    """The roofline's other denominators: the per-clock tensor peak at the SM clock sampled under load
+    (SMs x 8192 flop/clock x MHz: it separates what the kernel does per cycle from the clock the power
+    cap allows) and NVIDIA's published dense BF16 figure."""
+    pc = per_clock_peak_tflops(clocks.get("sm_mhz"))
+    roof["per_clock_peak"] = pc
+    roof["frac_of_per_clock_peak"] = roof["achieved"] / pc if pc else None
+    roof["per_clock_peak_how"] = f"SMs x {FLOP_PER_CLK_PER_SM} flop/clock x median sampled SM MHz"
+    roof["published_peak"] = PUBLISHED_BF16_DENSE_TFLOPS
+    roof["frac_of_published_peak"] = roof["achieved"] / PUBLISHED_BF16_DENSE_TFLOPS
+    roof["published_peak_source"] = PUBLISHED_BF16_SOURCE
+
+
+class TimedOps:
+    """The ring's library calls with CUDA events around every block forward / backward launch, so that
+    the dominant kernel's own launch time can be reported."""
+
+    def __init__(self, stream):
+        from sequence_sharded_exact_gb300 import ring
+
+        self.inner = ring.LibraryOps(stream)
+        self.stream = stream
+        self.events = {"fwd": [], "bwd": []}
+        self.record = False
+
+    def __getattr__(self, name):
+        return getattr(self.inner, name)
+
+    def _timed(self, kind, fn, *a):
+        if not self.record:
+            return fn(*a)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        fn(*a)
+        e1.record(self.stream)
+        self.events[kind].append((e0, e1))
+
+    def block_fwd(self, *a):
+        self._timed("fwd", self.inner.block_fwd, *a)
+
+    def block_bwd(self, *a):
+        self._timed("bwd", self.inner.block_bwd, *a)
+
+    def mean_ms(self, kind):
+        ev = self.events[kind]
+        return statistics.mean(a.elapsed_time(b) for a, b in ev) if ev else None
+
+
+def run_ring(args, w, world, rank, local):
+    """The multi-device ring: n = world shards of the workload's sequence, one per rank, blocks passed
+    round the ring over NCCL (one rank per GPU; gloo only when torch has no NCCL)."""
+    import torch.distributed as dist
+    import sequence_sharded_exact_gb300 as ra
+    from sequence_sharded_exact_gb300 import ring, synth
+
+    torch.cuda.set_device(local if world > 1 else 0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    else:
+        dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % free_port(), rank=0, world_size=1)
+    comm = ring.RingComm()
+    stream = torch.cuda.current_stream(dev)
+    B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
+    n, causal, layout = world, w["causal"], w["layout"]
+    if layout == "zigzag" and L % (2 * n):
+        raise SystemExit(f"L = {L} does not split into 2 x {n} zigzag chunks")
+    train = args.step == "train"
+    # every rank draws the same whole-sequence inputs (seeded) and keeps its own shard's rows
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=w["dtype"], seed=w["seed"], spike_frac=w["spike_frac"],
+                          with_dout=train, device=dev, gen_device=dev)
+    S = L // n
+    mine = {t: x[t][:, :, rank * S:(rank + 1) * S].contiguous() for t in x}
+    del x
+    torch.cuda.empty_cache()
+    ops = TimedOps(stream)
+    ff = fwd_flops(B, H, L, d, causal)
+    flops = 3.5 * ff if train else ff
+    res = {}
+
+    def step():
+        out, lse = ring.ring_fwd(mine["q"], mine["k"], mine["v"], comm, causal, layout, ops=ops)
+        if train:
+            ring.ring_bwd(mine["q"], mine["k"], mine["v"], out, lse, mine["dout"], comm, causal, layout, ops=ops)
+        res["out"], res["lse"] = out, lse
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ops.record = True
+    with ClockSampler(dev.index) as clk:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ops.record = False
+    dist.barrier()
+    torch.cuda.synchronize()
+    total_ms = max_over_ranks(ev0.elapsed_time(ev1), dist if world > 1 else None, dev)
+    status = ra.device_status()
+    value = flops * args.steps / (total_ms / 1e3) / 1e12  # the whole sequence's work, all ranks together
+    peak_b, peak_s, hbm, peak_kind = peaks()
+    kind = "bwd" if train else "fwd"
+    kms = ops.mean_ms(kind)
+    per_launch = (2.5 * ff if train else ff) / (n * n)  # each rank runs n of the n^2 blocks per pass
+    achieved = per_launch / (kms / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: q,k,v ~ N(0,1) bf16" + (", 1% of key rows x8" if w["spike_frac"] else "")
+                + (", dO ~ N(0,1)" if train else "") + ", seeded",
+        "config": dict(config_dict(dict(w, n=n), args.step),
+                       parallelism=f"context parallel: ring over {world} device(s), one shard of {S} tokens each",
+                       mode="multi-device ring (blocks over NCCL)" if world > 1 else "ring path on one device"),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_b, "unit": "TFLOP/s",
+                     "frac": achieved / peak_b, "traffic": None,
+                     "peak_kind": f"{peak_kind} bf16 burst (MEASURED_PEAKS bf16_tflops)",
+                     "kernel": "bwd_tc_kernel (block calls)" if train else "fwd_tc_kernel (block calls)",
+                     "timed": f"mean of the {kind} block launches of rank {rank}, CUDA events",
+                     "algorithmic_flops_per_launch": per_launch},
+        # forward: n block launches + 1 conversion; backward: preprocess, zero, n blocks, 2 (n - 1) adds
+        # of the travelling dK / dV accumulators, 3 conversions
+        "gpu_launches": args.steps * (n + 1 + (3 * n + 3 if train else 0)),
+        "device_status": status,
+    }
+    line["clocks"] = clk.summary()
+    add_peak_fractions(line["roofline"], line["clocks"])
+    # end to end: this rank's shard from pinned host memory, the ring, its results back to the host
+    h_in = {t: mine[t].cpu().pin_memory() for t in mine}
+    h_out = [torch.empty(res["out"].shape, dtype=res["out"].dtype, pin_memory=True),
+             torch.empty(res["lse"].shape, dtype=torch.float32, pin_memory=True)]
+    d_in = {t: torch.empty_like(mine[t]) for t in mine}
+
+    def e2e_step():
+        for t in mine:
+            d_in[t].copy_(h_in[t], non_blocking=True)
+        out, lse = ring.ring_fwd(d_in["q"], d_in["k"], d_in["v"], comm, causal, layout, ops=ops)
+        if train:
+            ring.ring_bwd(d_in["q"], d_in["k"], d_in["v"], out, lse, d_in["dout"], comm, causal, layout, ops=ops)
+        h_out[0].copy_(out, non_blocking=True)
+        h_out[1].copy_(lse, non_blocking=True)
+
+    e2e_steps = max(2, args.steps // 2)
+    for _ in range(1):
+        e2e_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1), dist if world > 1 else None, dev) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    line["e2e"] = {"value": flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                   "what": "every rank: its shard from pinned host memory, the ring, its out and lse back",
+                   "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world, "ms_per_step": e2e_ms}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def free_port():
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def other_workload(ra, name, stream, dev, peak_b):
+    """Forward (and, for a training workload, forward + backward) of another synthetic workload:
+    TFLOP/s and the fraction of the measured bf16 peak, 3 timed calls after 1 warm-up."""
+    from sequence_sharded_exact_gb300 import synth
+
+    ww = synth.WORKLOADS[name]
+    B, H, Hkv, L, d, n = ww["B"], ww["H"], ww["Hkv"], ww["L"], ww["d"], ww["n"]
+    xx = synth.make_workload(name, device=dev, gen_device=dev)
+    o, l = ra.fwd(xx["q"], xx["k"], xx["v"], n, ww["causal"], ww["layout"])
+    ff = fwd_flops(B, H, L, d, ww["causal"])
+    fms = statistics.mean(time_launches(lambda: ra.fwd(xx["q"], xx["k"], xx["v"], n, ww["causal"], ww["layout"],
+                                                       out=o, lse=l, stream=stream), 3, 1, stream))
+    res = {"workload": f"B{B} H{H} Hkv{Hkv} d{d} L{L} n{n} causal {ww['layout']}",
+           "fwd_ms": fms, "fwd_tflops": ff / (fms / 1e3) / 1e12, "fwd_frac": ff / (fms / 1e3) / 1e12 / peak_b,
+           "path": ra.fwd_path(B, H, Hkv, L, d, n, ww["causal"], ww["layout"], ww["dtype"])}
+    if ww["backward"]:
+        grads = [torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (xx["q"], xx["k"], xx["v"])]
+        wsb = torch.empty(max(256, ra.bwd_workspace_size(B, H, Hkv, L, d, torch.float32)), dtype=torch.uint8,
+                          device=dev)
+        bms = statistics.mean(time_launches(lambda: ra.bwd(xx["q"], xx["k"], xx["v"], o, l, xx["dout"], n, ww["causal"],
+                                                           ww["layout"], dq=grads[0], dk=grads[1], dv=grads[2],
+                                                           workspace=wsb, stream=stream), 3, 1, stream))
+        res.update(bwd_ms=bms, bwd_tflops=2.5 * ff / (bms / 1e3) / 1e12, bwd_frac=2.5 * ff / (bms / 1e3) / 1e12 / peak_b,
+                   train_tflops=3.5 * ff / ((fms + bms) / 1e3) / 1e12)
+        del grads, wsb
+    del xx, o, l
+    return res
 
 
 def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
@@ -550,6 +790,11 @@ def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
                                        out=ot, lse=lt, stream=stream), 3, 1, stream)
     res["train_fwd_only"] = {"tflops": ff / (statistics.mean(fms) / 1e3) / 1e12,
                              "ms": statistics.mean(fms)}
+    del xt, ot, lt, dq, dk, dv, wsb
+    # head dim 64 and the striped layout: the long-context forward and the training step
+    for name in ("zigzag_gqa_128k_d64", "striped_gqa_128k", "zigzag_gqa_64k_train_d64", "striped_gqa_64k_train"):
+        res["workload_" + name] = other_workload(ra, name, stream, dev, peak_b)
+    torch.cuda.empty_cache()
     res["device_status"] = ra.device_status()
     return res
 

@@ -233,7 +233,9 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                 continue;
             }
             const int pq = u.p0 + w * kTile;  // natural position of this Q tile's first row (not striped)
-            float m_run = -INFINITY, l_run = 0.f;
+            // l_run: running sum of the weights; c_run: running sum of (bf16(P_max) - P_max) over the
+            // tiles (see below).  O is normalised by l_run + c_run, lse is m_run + log2(l_run).
+            float m_run = -INFINITY, l_run = 0.f, c_run = 0.f;
             KvWalk walk;
             walk.begin(a, u);
             for (int jj = 0; jj < u.ntiles; ++jj, ++tcount) {
@@ -314,13 +316,15 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
                 }
                 const float2 s2 = add2(add2(s4[0], s4[1]), add2(s4[2], s4[3]));
                 // P V multiplies V by the weights rounded to bf16, while the sum above adds them
-                // unrounded.  For the tile's largest weight the difference is added to the sum, so that
-                // a row dominated by one key is normalised by exactly the weight its V row received
-                // (the same fma and ex2 as that element: the same value bit for bit).
+                // unrounded.  For the tile's largest weight the difference is kept, so that the output
+                // of a row dominated by one key is normalised by exactly the weight its V row received
+                // (the same fma and ex2 as that element: the same value bit for bit); lse keeps the
+                // unrounded sum.
                 const float p_max = ex2_approx(fmaf(mx, sl2, -ref));
                 const float p_max_bf16 = __uint_as_float(pack_bf16x2(p_max, 0.f) << 16);
-                const float rsum = s2.x + s2.y + (p_max_bf16 - p_max);
+                const float rsum = s2.x + s2.y;
                 l_run = l_run * alpha + rsum;
+                c_run = c_run * alpha + (p_max_bf16 - p_max);
                 tmem_st_wait();
                 const bool need = jj > 0 && alpha != 1.0f;
                 if (__any_sync(0xffffffffu, need)) {
@@ -353,7 +357,7 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
             tc_fence_after_sync();
             __syncwarp();
             const bool any = l_run > 0.f;
-            const float inv = any ? 1.0f / l_run : 0.f;
+            const float inv = any ? 1.0f / (l_run + c_run) : 0.f;
             if (a.mode == kFwdFused) {
                 __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + row_g * kHd;
 #pragma unroll 1

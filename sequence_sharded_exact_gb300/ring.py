@@ -1,0 +1,184 @@
+"""The multi-device ring: one process per device, each holding one shard of the sequence.
+
+Device i keeps its query shard Q_i and, at ring step r = 0..n-1, computes the block attention of
+Q_i against the K/V block it holds -- that of shard j = (i - r) mod n -- folds it into its running
+output, and meanwhile passes the block to device i + 1 and receives the next one from device i - 1
+(LLM-101-CN "distributed hands-on code", section 6.2: block_attention, ring_send_recv_kv and
+forward; airsota "M4-051 Ring Attention and sequence parallelism", section 3; "Lecture 30:
+TP/PP/SP/CP", section 3.2).  The transfer of the next block runs while the current one is computed
+(the questions after section 6.2 ask for exactly this overlap; M4-051's "communication overlap").
+In the backward the K/V blocks go round again and the dK/dV accumulator of each block travels with
+it: every device adds its contribution and passes it on, and after the n-th step the accumulator
+arrives at the block's owner.
+
+This module only schedules: every step of the arithmetic runs in the library's block calls
+(ring_attn_block_fwd / ring_attn_block_bwd and their helpers, through ``ops``), and the blocks move
+with torch.distributed point-to-point operations (NCCL between GPUs; gloo, staged through host
+memory, in tests).
+
+Shapes on device i: q, out, dout [B, H, S, d], k, v [B, Hkv, S, d], lse [B, H, S], with S = L / n
+and n = world size; the rows are shard i's rows of the layout (contiguous, zigzag or striped), i.e.
+rows [i*S, (i+1)*S) of the whole-sequence buffers of the single-device calls.
+"""
+from __future__ import annotations
+
+import torch
+import torch.distributed as dist
+
+
+class RingComm:
+    """Point-to-point exchange with the ring neighbours: every call sends to rank + 1 and receives
+    from rank - 1 (the direction of the pages' code, so that step r holds shard (rank - r) mod n).
+
+    With the gloo backend and CUDA tensors the blocks are staged through host memory (gloo moves CPU
+    tensors only); with NCCL they move device to device on NCCL's stream, ordered after the work
+    already queued on the current stream, and ``wait`` orders the current stream after them."""
+
+    def __init__(self, group=None):
+        self.group = group
+        self.rank = dist.get_rank(group)
+        self.world = dist.get_world_size(group)
+        self.next = (self.rank + 1) % self.world
+        self.prev = (self.rank - 1) % self.world
+        self.backend = dist.get_backend(group)
+        self._gnext = dist.get_global_rank(group, self.next) if group is not None else self.next
+        self._gprev = dist.get_global_rank(group, self.prev) if group is not None else self.prev
+
+    def start(self, send, recv, tag=0):
+        """Starts sending the tensors `send` to rank + 1 and receiving into `recv` (same shapes and
+        dtypes) from rank - 1, with message tags tag, tag + 1, ...: transfers that are in flight at
+        the same time must use different tags.  Returns a handle for ``wait``."""
+        assert len(send) == len(recv)
+        staged = self.backend == "gloo" and any(t.is_cuda for t in send)
+        if staged:
+            torch.cuda.current_stream().synchronize()  # the blocks to send are complete
+            s_host = [t.cpu() for t in send]
+            r_host = [torch.empty(t.shape, dtype=t.dtype) for t in recv]
+        else:
+            s_host, r_host = list(send), list(recv)
+        ops = []
+        for x, (s, r) in enumerate(zip(s_host, r_host)):
+            ops.append(dist.P2POp(dist.isend, s, self._gnext, self.group, tag + x))
+            ops.append(dist.P2POp(dist.irecv, r, self._gprev, self.group, tag + x))
+        works = dist.batch_isend_irecv(ops)
+        return works, (r_host if staged else None), recv
+
+    @staticmethod
+    def wait(handle):
+        """Completes a transfer: afterwards the received tensors may be read on the current stream."""
+        works, r_host, recv = handle
+        for w in works:
+            w.wait()
+        if r_host is not None:
+            for dst, src in zip(recv, r_host):
+                dst.copy_(src, non_blocking=False)
+
+
+class LibraryOps:
+    """The per-device compute of the ring: the library's block calls (CUDA)."""
+
+    def __init__(self, stream=None):
+        from . import binding
+
+        self.b = binding
+        self.stream = stream
+
+    def empty_acc(self, shape, like):
+        """A running-state or gradient accumulator (float32, on `like`'s device)."""
+        return torch.empty(shape, dtype=torch.float32, device=like.device)
+
+    def block_fwd(self, q, k, v, o_acc, lse_acc, n, i, j, accumulate, causal, layout):
+        self.b.block_fwd(q, k, v, o_acc, lse_acc, n, i, j, accumulate, causal, layout, stream=self.stream)
+
+    def convert(self, src, dtype):
+        return self.b.f32_convert(src, dtype, stream=self.stream)
+
+    def preprocess(self, out, dout):
+        return self.b.bwd_preprocess(out, dout, stream=self.stream)
+
+    def zero(self, x):
+        self.b.f32_zero(x, stream=self.stream)
+
+    def block_bwd(self, q, k, v, dout, lse, D, dq_acc, dk, dv, n, i, j, accumulate_kv, causal, layout):
+        self.b.block_bwd(q, k, v, dout, lse, D, dq_acc, dk, dv, n, i, j, accumulate_kv, causal, layout,
+                         stream=self.stream)
+
+    def add(self, acc, part):
+        self.b.f32_add(acc, part, stream=self.stream)
+
+
+def ring_fwd(q, k, v, comm, causal=True, layout="zigzag", ops=None):
+    """Ring forward on this device (rank i of n = world size): q [B,H,S,d] and k, v [B,Hkv,S,d] are
+    shard i.  Returns (out [B,H,S,d] in q's dtype, lse [B,H,S] float32) for shard i's rows."""
+    ops = ops or LibraryOps()
+    n, i = comm.world, comm.rank
+    B, H, S, d = q.shape
+    o_acc = ops.empty_acc((B, H, S, d), q)
+    lse_acc = ops.empty_acc((B, H, S), q)
+    spare = _spare_blocks(k, v, n)
+    cur = (k, v)
+    for r in range(n):
+        j = (i - r) % n
+        # pass the block we hold on and take the next while this one is computed
+        nxt = spare[r % 2] if r < n - 1 else None
+        h = comm.start(cur, nxt) if nxt is not None else None
+        ops.block_fwd(q, cur[0], cur[1], o_acc, lse_acc, n, i, j, r > 0, causal, layout)
+        if h is not None:
+            comm.wait(h)
+            cur = nxt
+    return ops.convert(o_acc, q.dtype), lse_acc
+
+
+def _spare_blocks(k, v, n):
+    """The two receive slots of the K/V rotation.  A block is received into the slot that held the
+    block of two steps before (computed and passed on by then), never into the caller's k and v."""
+    return [(torch.empty_like(k), torch.empty_like(v)) for _ in range(min(2, n - 1))]
+
+
+def ring_bwd(q, k, v, out, lse, dout, comm, causal=True, layout="zigzag", grad_dtype=torch.float32, ops=None):
+    """Ring backward on this device: the inputs of ring_fwd plus its (out, lse) and the upstream
+    gradient dout of shard i.  Returns (dq [B,H,S,d], dk, dv [B,Hkv,S,d]) of shard i in grad_dtype.
+
+    Per step r (block j = (i - r) mod n): the K/V transfer of the next block starts, this device's
+    contribution to block j's dK/dV is computed into `part` (dQ is added into the local dq_acc), the
+    accumulator of block j arrives from device i - 1 (it holds the contributions of devices j .. i-1),
+    `part` is added to it and it goes on to device i + 1.  After step n - 1 the accumulator that
+    arrives is this device's own block, complete."""
+    ops = ops or LibraryOps()
+    n, i = comm.world, comm.rank
+    B, H, S, d = q.shape
+    Hkv = k.shape[1]
+    D = ops.preprocess(out, dout)
+    dq_acc = ops.empty_acc((B, H, S, d), q)
+    ops.zero(dq_acc)
+    kshape = (B, Hkv, S, d)
+    acc = [tuple(ops.empty_acc(kshape, q) for _ in range(2)) for _ in range(2)]  # two accumulator slots
+    part = tuple(ops.empty_acc(kshape, q) for _ in range(2)) if n > 1 else None
+    spare = _spare_blocks(k, v, n)
+    cur = (k, v)
+    h_acc = None
+    slot = 0
+    for r in range(n):
+        j = (i - r) % n
+        nxt = spare[r % 2] if r < n - 1 else None
+        h_kv = comm.start(cur, nxt) if nxt is not None else None
+        if r == 0:
+            # the first contribution to this device's own block starts its accumulator
+            ops.block_bwd(q, cur[0], cur[1], dout, lse, D, dq_acc, acc[0][0], acc[0][1], n, i, j, False, causal,
+                          layout)
+        else:
+            ops.block_bwd(q, cur[0], cur[1], dout, lse, D, dq_acc, part[0], part[1], n, i, j, False, causal,
+                          layout)
+            comm.wait(h_acc)  # block j's accumulator from device i - 1, now in acc[slot]
+            ops.add(acc[slot][0], part[0])
+            ops.add(acc[slot][1], part[1])
+        if n > 1:
+            h_acc = comm.start(acc[slot], acc[1 - slot], tag=2)  # in flight with the K/V transfer
+            slot = 1 - slot
+        if h_kv is not None:
+            comm.wait(h_kv)
+            cur = nxt
+    if n > 1:
+        comm.wait(h_acc)  # this device's own block, with every device's contribution
+    dk_acc, dv_acc = acc[slot]
+    return ops.convert(dq_acc, grad_dtype), ops.convert(dk_acc, grad_dtype), ops.convert(dv_acc, grad_dtype)

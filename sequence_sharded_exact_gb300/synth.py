@@ -18,7 +18,7 @@ import torch
 
 # The workloads of the benchmark and parity suite (sizes as quoted on the pages' examples: 128K
 # tokens over 8 shards of 16K, head dim 128, inner tile 128).  The striped ones repeat the zigzag
-# sizes in the round-robin layout.
+# sizes in the round-robin layout, the _d64 ones with head dim 64.
 WORKLOADS = {
     "tiny_f32": dict(B=1, H=1, Hkv=1, L=256, d=64, n=4, causal=False, layout="contiguous",
                      dtype=torch.float32, spike_frac=0.0, backward=False, seed=1001),
@@ -36,6 +36,12 @@ WORKLOADS = {
     "striped_gqa_64k_train": dict(B=1, H=32, Hkv=8, L=65536, d=128, n=16, causal=True,
                                   layout="striped", dtype=torch.bfloat16, spike_frac=0.0,
                                   backward=True, seed=1007),
+    # head dim 64 (the other head dim of the tensor-core kernels), same sequences
+    "zigzag_gqa_128k_d64": dict(B=1, H=32, Hkv=8, L=131072, d=64, n=8, causal=True, layout="zigzag",
+                                dtype=torch.bfloat16, spike_frac=0.01, backward=False, seed=1008),
+    "zigzag_gqa_64k_train_d64": dict(B=1, H=32, Hkv=8, L=65536, d=64, n=16, causal=True,
+                                     layout="zigzag", dtype=torch.bfloat16, spike_frac=0.0,
+                                     backward=True, seed=1009),
 }
 
 

@@ -1,0 +1,211 @@
+"""Worker side of the multi-process ring tests (spawned ranks; imported by the test modules).
+
+Each rank builds the same seeded whole-sequence inputs, keeps its own shard, runs the ring forward
+and backward through sequence_sharded_exact_gb300.ring with torch.distributed (gloo) moving the
+blocks, and checks its shard of the results against the float64 oracle of the whole sequence."""
+import os
+import socket
+import sys
+import traceback
+
+import numpy as np
+import torch
+import torch.distributed as dist
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def shard(t, i, n):
+    S = t.shape[2] // n
+    return t[:, :, i * S:(i + 1) * S].contiguous()
+
+
+class OracleOps:
+    """The ring's per-device compute done by the float64 oracle's block functions (CPU), so that the
+    driver's schedule and transfers can be checked on CPU ranks.  Records every block call."""
+
+    def __init__(self, L):
+        import oracle
+
+        self.oracle = oracle
+        self.L = L
+        self.calls = []
+
+    def empty_acc(self, shape, like):
+        return torch.empty(shape, dtype=torch.float64)
+
+    def block_fwd(self, q, k, v, o_acc, lse_acc, n, i, j, accumulate, causal, layout):
+        self.calls.append(("fwd", i, j, bool(accumulate)))
+        o, l = self.oracle.block_fwd(q, k, v, self.L, n, causal, layout, i, j)
+        o, l = torch.from_numpy(o), torch.from_numpy(l)
+        if not accumulate:
+            o_acc.copy_(o)
+            lse_acc.copy_(l)
+            return
+        new = torch.logaddexp(lse_acc, l)
+        keep = torch.isneginf(new)
+        wa = torch.where(keep, torch.zeros_like(new), torch.exp(lse_acc - new))
+        wb = torch.where(keep, torch.zeros_like(new), torch.exp(l - new))
+        o_acc.copy_(wa[..., None] * o_acc + wb[..., None] * o)
+        lse_acc.copy_(torch.where(keep, lse_acc, new))
+
+    def convert(self, src, dtype):
+        return src.clone()
+
+    def preprocess(self, out, dout):
+        return (out.double() * dout.double()).sum(-1)
+
+    def zero(self, x):
+        x.zero_()
+
+    def block_bwd(self, q, k, v, dout, lse, D, dq_acc, dk, dv, n, i, j, accumulate_kv, causal, layout):
+        self.calls.append(("bwd", i, j, bool(accumulate_kv)))
+        a, b, c = self.oracle.block_bwd(q, k, v, dout, lse, D, self.L, n, causal, layout, i, j)
+        dq_acc += torch.from_numpy(a)
+        if accumulate_kv:
+            dk += torch.from_numpy(b)
+            dv += torch.from_numpy(c)
+        else:
+            dk.copy_(torch.from_numpy(b))
+            dv.copy_(torch.from_numpy(c))
+
+    def add(self, acc, part):
+        acc += part
+
+
+def errors(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    ma = float(np.abs(got - ref).max())
+    rl = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+    return ma, rl
+
+
+def run_rank(rank, world, port, cases, device, result_dir):
+    """One rank: every case is (B, H, Hkv, L, d, causal, layout, dtype name, grad dtype name, seed)."""
+    os.environ.setdefault("GLOO_SOCKET_IFNAME", "lo")
+    ok = True
+    try:
+        dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+        import oracle
+        from sequence_sharded_exact_gb300 import ring, synth
+
+        if device != "cpu":
+            torch.cuda.set_device(0)
+        comm = ring.RingComm()
+        assert comm.rank == rank and comm.world == world and comm.next == (rank + 1) % world
+        n = world
+        for (B, H, Hkv, L, d, causal, layout, dt, gdt, seed) in cases:
+            dtype = getattr(torch, dt)
+            gdtype = getattr(torch, gdt)
+            x = synth.make_inputs(B, H, Hkv, L, d, dtype=dtype, seed=seed, with_dout=True)
+            ref_file = os.path.join(result_dir, f"ref_{seed}.npz")
+            if os.path.exists(ref_file):  # precomputed once by the launching process
+                z = np.load(ref_file)
+                ref_o, ref_l, rq, rk, rv = (z[t] for t in ("o", "l", "dq", "dk", "dv"))
+            else:
+                ref_o, ref_l = oracle.attn_fwd(x["q"], x["k"], x["v"], n, causal, layout)
+                rq, rk, rv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], n, causal, layout)
+            S = L // n
+            sl = slice(rank * S, (rank + 1) * S)
+            mine = {t: shard(x[t], rank, n) for t in ("q", "k", "v", "dout")}
+            if device == "cpu":
+                ops = OracleOps(L)
+                out, lse = ring.ring_fwd(mine["q"], mine["k"], mine["v"], comm, causal, layout, ops=ops)
+                dq, dk, dv = ring.ring_bwd(mine["q"], mine["k"], mine["v"], out, lse, mine["dout"], comm, causal,
+                                           layout, ops=ops)
+                # the schedule: step r computes block (rank - r) mod n; the first block writes, later
+                # ones fold in; the backward stores each contribution (the accumulators travel)
+                fwd = [c for c in ops.calls if c[0] == "fwd"]
+                bwd = [c for c in ops.calls if c[0] == "bwd"]
+                assert fwd == [("fwd", rank, (rank - r) % n, r > 0) for r in range(n)], fwd
+                assert bwd == [("bwd", rank, (rank - r) % n, False) for r in range(n)], bwd
+                tol = {"out": 1e-10, "lse": 1e-10, "dq": 1e-10, "dk": 1e-10, "dv": 1e-10}
+                rel = 1e-10
+            else:
+                dev = torch.device("cuda", 0)
+                g = {t: v.to(dev) for t, v in mine.items()}
+                out, lse = ring.ring_fwd(g["q"], g["k"], g["v"], comm, causal, layout)
+                dq, dk, dv = ring.ring_bwd(g["q"], g["k"], g["v"], out, lse, g["dout"], comm, causal, layout,
+                                           grad_dtype=gdtype)
+                torch.cuda.synchronize()
+                from sequence_sharded_exact_gb300 import binding
+
+                assert binding.device_status() == 0
+                lim = 1e-4 if dtype == torch.float32 else 2e-2
+                tol = {"out": lim, "lse": lim, "dq": lim, "dk": lim, "dv": lim}
+                rel = 1.0 if dtype == torch.float32 else 5e-3
+                if gdtype == torch.bfloat16:  # stored in bf16: its own rounding on top
+                    for t in ("dq", "dk", "dv"):
+                        tol[t] = None
+            # the ring passes copies of the blocks on: the caller's own k and v are left as they were
+            for t in ("k", "v"):
+                held = mine[t] if device == "cpu" else g[t].cpu()
+                assert torch.equal(held, shard(x[t], rank, n)), f"the ring overwrote the caller's {t}"
+            got = {"out": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+            ref = {"out": ref_o[:, :, sl], "lse": ref_l[:, :, sl], "dq": rq[:, :, sl], "dk": rk[:, :, sl],
+                   "dv": rv[:, :, sl]}
+            for name in got:
+                gv = got[name].detach().double().cpu().numpy()
+                ma, rl = errors(gv, ref[name])
+                if tol[name] is None:
+                    excess = np.abs(gv - ref[name]) - (2e-2 + np.abs(ref[name]) * 2.0 ** -8)
+                    assert excess.max() <= 0 and rl <= 5e-3, f"{name}: {excess.max():.3e} {rl:.3e}"
+                else:
+                    assert ma <= tol[name] and rl <= rel, \
+                        f"rank {rank}/{world} {layout} causal={causal} {dt} {name}: max-abs {ma:.3e}, rel-L2 {rl:.3e}"
+        dist.barrier()
+    except Exception:
+        ok = False
+        with open(os.path.join(result_dir, f"rank{rank}.err"), "w") as f:
+            f.write(traceback.format_exc())
+    finally:
+        if dist.is_initialized():
+            dist.destroy_process_group()
+    if ok:
+        open(os.path.join(result_dir, f"rank{rank}.ok"), "w").close()
+
+
+def precompute_refs(world, cases, result_dir):
+    """The oracle of every case's whole sequence, computed once here for all ranks."""
+    import oracle
+    from sequence_sharded_exact_gb300 import synth
+
+    for (B, H, Hkv, L, d, causal, layout, dt, gdt, seed) in cases:
+        x = synth.make_inputs(B, H, Hkv, L, d, dtype=getattr(torch, dt), seed=seed, with_dout=True)
+        o, l = oracle.attn_fwd(x["q"], x["k"], x["v"], world, causal, layout)
+        dq, dk, dv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], world, causal, layout)
+        np.savez(os.path.join(result_dir, f"ref_{seed}.npz"), o=o, l=l, dq=dq, dk=dk, dv=dv)
+
+
+def launch(world, cases, device, result_dir, timeout=600):
+    """Spawns `world` ranks running run_rank and returns (all ok, error texts)."""
+    import torch.multiprocessing as mp
+
+    port = free_port()
+    ctx = mp.start_processes(run_rank, args=(world, port, cases, device, result_dir), nprocs=world, join=False,
+                             start_method="spawn")
+    import time
+
+    t0 = time.time()
+    while not ctx.join(timeout=5):
+        if time.time() - t0 > timeout:
+            for p in ctx.processes:
+                if p.is_alive():
+                    p.kill()
+            return False, ["timed out"]
+    errs = []
+    for r in range(world):
+        e = os.path.join(result_dir, f"rank{r}.err")
+        if os.path.exists(e):
+            errs.append(open(e).read())
+    oks = all(os.path.exists(os.path.join(result_dir, f"rank{r}.ok")) for r in range(world))
+    return oks and not errs, errs

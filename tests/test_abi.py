@@ -233,3 +233,29 @@ def test_device_check_reports_its_codes(lib):
     st = ctypes.c_uint(7)
     assert lib.ring_attn_device_status(ctypes.byref(st), None) == binding.RA_ERR_NO_DEVICE
     assert st.value == 7  # untouched on failure
+
+
+def test_block_calls_check_their_arguments(lib):
+    """The per-device block calls refuse bad shard indices, flags, counts and pointers before any
+    CUDA call (so these run without a GPU)."""
+    P = ctypes.c_void_p
+    ok16 = P(16)
+
+    def fwd(i=1, j=0, acc=0, L=4096, n=4, ptr=ok16):
+        return lib.ring_attn_block_fwd(ptr, ok16, ok16, ok16, ok16, 1, 2, 1, L, 128, n, i, j, acc, 1, 1, 1, None)
+
+    def bwd(i=1, j=0, acc=0):
+        return lib.ring_attn_block_bwd(*([ok16] * 9), 1, 2, 1, 4096, 128, 4, i, j, acc, 1, 1, 1, None)
+
+    for st in (fwd(i=4), fwd(j=-1), fwd(acc=2), fwd(L=4100), fwd(ptr=P(8)), fwd(ptr=None), bwd(i=-1), bwd(j=4),
+               bwd(acc=3)):
+        assert st == binding.RA_ERR_INVALID_ARG
+    assert "shard indices" in lib.ring_attn_last_error().decode() or "must be 0 or 1" in lib.ring_attn_last_error().decode()
+    LL = ctypes.c_longlong
+    assert lib.ring_attn_f32_zero(ok16, LL(-1), None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_f32_add(ok16, P(8), LL(4), None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_f32_convert(ok16, ok16, LL(4), 7, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_bwd_preprocess(ok16, ok16, ok16, LL(4), 0, 1, None) == binding.RA_ERR_INVALID_ARG
+    # an empty count enqueues nothing and needs no device
+    assert lib.ring_attn_f32_zero(None, LL(0), None) == binding.RA_OK
+    assert lib.ring_attn_f32_convert(None, None, LL(0), 1, None) == binding.RA_OK

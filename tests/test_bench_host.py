@@ -54,3 +54,15 @@ def test_sample_rows_are_distinct_sorted_and_in_range():
     assert len(rows) == 500 and np.all(np.diff(rows) > 0)
     assert rows[0] >= 0 and rows[-1] < 2 * 4 * 1000
     assert np.array_equal(rows, bench.sample_rows(2, 4, 1000, 500, seed=3))
+
+
+def test_peak_fractions_published_and_per_clock():
+    """The roofline's extra denominators: NVIDIA's published dense figure always, the per-clock peak
+    (SMs x 8192 flop/clock x sampled MHz) only when a clock was sampled on a device."""
+    roof = {"achieved": 1250.0}
+    bench.add_peak_fractions(roof, {"sm_mhz": None})
+    assert roof["per_clock_peak"] is None and roof["frac_of_per_clock_peak"] is None
+    assert roof["published_peak"] == 2500.0 and roof["frac_of_published_peak"] == 0.5
+    assert "sparsity" in roof["published_peak_source"]
+    if not __import__("torch").cuda.is_available():
+        assert bench.per_clock_peak_tflops(2000.0) is None

@@ -1,0 +1,32 @@
+"""The multi-device ring through the library's block kernels, with its ranks as separate processes
+that share cuda:0 and pass the blocks over gloo (staged through host memory).  No kernel waits on
+another rank: every exchange happens on the host between launches, so the ranks' kernels are
+independent launches.  Each rank checks its shard of out, lse, dq, dk and dv against the float64
+oracle of the whole sequence, in the contiguous, zigzag and striped layouts, on the tensor-core
+path (bf16, head dim 128 and 64) and on the CUDA-core path (float32)."""
+import pytest
+import torch
+
+from ring_ranks import launch, precompute_refs
+
+pytestmark = pytest.mark.gpu
+
+CASES = {  # B, H, Hkv, L, d, causal, layout, dtype, grad dtype, seed
+    2: [(1, 4, 2, 4096, 128, True, "zigzag", "bfloat16", "float32", 201),
+        (1, 2, 1, 2048, 128, True, "contiguous", "bfloat16", "bfloat16", 202),
+        (1, 2, 2, 2048, 64, True, "striped", "bfloat16", "float32", 203),
+        (1, 2, 1, 512, 64, True, "zigzag", "float32", "float32", 204)],
+    4: [(1, 4, 2, 4096, 128, True, "zigzag", "bfloat16", "float32", 205),
+        (2, 2, 1, 2048, 128, True, "contiguous", "bfloat16", "float32", 206),
+        (1, 4, 1, 4096, 128, True, "striped", "bfloat16", "float32", 207),
+        (1, 2, 1, 2048, 128, False, "zigzag", "bfloat16", "float32", 208),
+        (1, 2, 2, 512, 128, True, "zigzag", "float32", "float32", 209)],
+}
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_ring_processes_on_one_gpu_match_the_oracle(world, tmp_path):
+    assert torch.cuda.is_available()
+    precompute_refs(world, CASES[world], str(tmp_path))
+    ok, errs = launch(world, CASES[world], "cuda", str(tmp_path), timeout=900)
+    assert ok, "\n".join(errs)

@@ -441,3 +441,94 @@ def test_rope_attention_gradient_chain_matches_autograd():
     out.backward(tdo)
     np.testing.assert_allclose(dq[:, :, inv], tq.grad.numpy(), rtol=0, atol=2e-6)
     np.testing.assert_allclose(dk[:, :, inv], tk.grad.numpy(), rtol=0, atol=2e-6)
+
+
+# ------------------------------------------------------------------------------------------------
+# One device of the multi-device ring: the block functions
+# ------------------------------------------------------------------------------------------------
+def _shard(t, i, n):
+    """Rows [i*S, (i+1)*S) of a [B, heads, L, d] (or [B, heads, L]) tensor: device i's local buffer."""
+    S = t.shape[2] // n
+    return t[:, :, i * S:(i + 1) * S].contiguous()
+
+
+BLOCK_CASES = [  # B, H, Hkv, L, d, n, causal, layout
+    (1, 2, 1, 32, 8, 4, True, "zigzag"),
+    (2, 4, 2, 24, 8, 3, True, "contiguous"),
+    (1, 2, 2, 32, 8, 4, True, "striped"),
+    (1, 2, 1, 24, 8, 2, False, "zigzag"),
+    (1, 1, 1, 16, 8, 1, True, "contiguous"),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,d,n,causal,layout", BLOCK_CASES)
+def test_block_fwd_blocks_recombine_into_full_attention(B, H, Hkv, L, d, n, causal, layout):
+    """The n blocks a device meets partition its rows' key sets, so their (o_part, lse_part) merged by
+    log-sum-exp weights give full attention (the pages: after n steps the ring result equals full
+    attention).  Compared with the full-sequence oracle, which is pinned to torch's attention."""
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=torch.float32, seed=77 + L + n)
+    ref_o, ref_l = oracle.attn_fwd(x["q"], x["k"], x["v"], n, causal, layout)
+    for i in range(n):
+        parts = [oracle.block_fwd(_shard(x["q"], i, n), _shard(x["k"], j, n), _shard(x["v"], j, n), L, n, causal,
+                                  layout, i, j) for j in range(n)]
+        lse = np.logaddexp.reduce(np.stack([p[1] for p in parts]), axis=0)
+        o = sum(np.exp(p[1] - lse)[..., None] * p[0] for p in parts)
+        S = L // n
+        assert np.abs(lse - ref_l[:, :, i * S:(i + 1) * S]).max() < 1e-12
+        assert np.abs(o - ref_o[:, :, i * S:(i + 1) * S]).max() < 1e-12
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
+def test_block_fwd_sees_exactly_the_ring_walks_pairs(layout):
+    """With V the identity (d = S, v_t = e_t) the block output row shows which keys of the block the
+    query saw; their count per (i, j) equals the visible pairs the oracle's ring walk counts at that
+    step, which are pinned to closed forms elsewhere.  A block that sees nothing has lse = -inf, o = 0.
+    This ties block (i, j) to the keys of shard j, not of another shard."""
+    L, n = 32, 4
+    S = L // n
+    x = synth.make_inputs(1, 1, 1, L, S, dtype=torch.float32, seed=5)
+    v = torch.eye(S).repeat(n, 1).view(1, 1, L, S)
+    _, _, pairs = oracle.ring_fwd(x["q"], x["k"], v, n, True, layout)
+    for i in range(n):
+        for j in range(n):
+            o, lse = oracle.block_fwd(_shard(x["q"], i, n), _shard(x["k"], j, n), _shard(v, j, n), L, n, True,
+                                      layout, i, j)
+            assert int((o > 0).sum()) == pairs[i, j]
+            empty = np.isneginf(lse)
+            assert np.all(o[empty] == 0)
+            assert np.all((o > 0).sum(axis=-1)[~empty] > 0)
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,d,n,causal,layout", BLOCK_CASES)
+def test_block_bwd_contributions_sum_to_the_full_gradients(B, H, Hkv, L, d, n, causal, layout):
+    """Summed over the key shards j, a query shard's dq contributions are its rows of the full dq;
+    summed over the query shards i, a key shard's dk and dv contributions are its rows of the full dk
+    and dv (oracle_attn_bwd, pinned to torch autograd and finite differences)."""
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=torch.float32, seed=91 + L + n, with_dout=True)
+    out, lse = oracle.attn_fwd(x["q"], x["k"], x["v"], n, causal, layout)
+    D = (x["dout"].double().numpy() * out).sum(-1)
+    rq, rk, rv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], n, causal, layout)
+    S = L // n
+    dq = np.zeros_like(rq)
+    dk = np.zeros_like(rk)
+    dv = np.zeros_like(rv)
+    for i in range(n):
+        for j in range(n):
+            a, b, c = oracle.block_bwd(_shard(x["q"], i, n), _shard(x["k"], j, n), _shard(x["v"], j, n),
+                                       _shard(x["dout"], i, n), lse[:, :, i * S:(i + 1) * S],
+                                       D[:, :, i * S:(i + 1) * S], L, n, causal, layout, i, j)
+            dq[:, :, i * S:(i + 1) * S] += a
+            dk[:, :, j * S:(j + 1) * S] += b
+            dv[:, :, j * S:(j + 1) * S] += c
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert np.abs(got - ref).max() < 1e-11
+
+
+def test_block_bwd_empty_block_is_zero():
+    """Causal contiguous: keys of a later shard are never visible, so the block contributes nothing."""
+    L, n = 24, 3
+    x = synth.make_inputs(1, 2, 1, L, 8, dtype=torch.float32, seed=3, with_dout=True)
+    lse = np.zeros((1, 2, 8))
+    a, b, c = oracle.block_bwd(_shard(x["q"], 0, n), _shard(x["k"], 2, n), _shard(x["v"], 2, n),
+                               _shard(x["dout"], 0, n), lse, lse, L, n, True, "contiguous", 0, 2)
+    assert not a.any() and not b.any() and not c.any()

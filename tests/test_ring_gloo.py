@@ -1,0 +1,22 @@
+"""The multi-device ring on CPU ranks (gloo, world sizes 2 to 4): sequence_sharded_exact_gb300.ring
+schedules the blocks and moves them with torch.distributed point-to-point operations, and the
+per-device compute is the float64 oracle's block functions.  Every rank checks its shard of out,
+lse, dq, dk and dv against the oracle of the whole sequence (1e-10), and the order of its block calls
+(step r computes block (rank - r) mod n; the first writes, the later ones fold in)."""
+import pytest
+
+from ring_ranks import launch
+
+CASES = [  # B, H, Hkv, L, d, causal, layout, dtype, grad dtype, seed
+    (1, 2, 1, 48, 8, True, "zigzag", "float32", "float32", 11),
+    (1, 2, 2, 48, 8, True, "contiguous", "float32", "float32", 12),
+    (2, 2, 1, 48, 8, True, "striped", "float32", "float32", 13),
+    (1, 2, 1, 48, 8, False, "zigzag", "float32", "float32", 14),
+]
+
+
+@pytest.mark.parametrize("world", [2, 3, 4])
+def test_ring_on_gloo_ranks_matches_full_attention(world, tmp_path):
+    cases = [c for c in CASES if c[3] % (2 * world) == 0]
+    ok, errs = launch(world, cases, "cpu", str(tmp_path), timeout=300)
+    assert ok, "\n".join(errs)
