@@ -39,12 +39,12 @@ WORKLOAD = "zigzag_gqa_128k"
 TRAIN_WORKLOAD = "zigzag_gqa_64k_train"
 METRIC = "ring-attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from ncu captures summarised in
-# profiles/ (forward: the 32K capture scaled to 128K by rows, each Q/K/V/O byte moving once;
-# backward: a single-pass capture of the kernel itself at 64K).  Update or drop an entry whenever
-# that kernel changes; a workload without an entry reports null.
-TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4 * 650.5e6, ("zigzag_gqa_32k", "fwd"): 650.5e6,
-                 ("zigzag_gqa_64k_train", "train"): 8.51e9 + 4.51e9}
+# DRAM bytes (read + write) per launch of the dominant kernel, measured by ncu on one launch at the
+# bench size (summaries in profiles/: fwd_tc_kernel_zigzag_gqa_128k_metrics.md and
+# bwd_tc_kernel_zigzag_gqa_64k_train_metrics.md).  Update or drop an entry whenever that kernel
+# changes; a workload without an entry reports null.
+TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 4.364235776e9 + 1.085255680e9,
+                 ("zigzag_gqa_64k_train", "train"): 7.695254016e9 + 4.134671872e9}
 
 
 def copy_bandwidth(host, device_t, stream):
