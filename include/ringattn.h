@@ -265,6 +265,17 @@ RA_API ra_status ring_attn_block_bwd(const void* q, const void* k, const void* v
  */
 RA_API ra_status ring_attn_bwd_preprocess(const void* out, const void* dout, float* D, long long rows, int d,
                                           int dtype, void* stream);
+
+/*
+ * ring_attn_block_rope -- ring_attn_rope on one device's local buffer: x [B][H][S][d] holds shard
+ * `shard`'s rows (rows [shard*S, (shard+1)*S) of the whole-sequence layout), and every row turns by
+ * the angle of its natural position in the whole sequence, so that the K/V blocks a device passes
+ * on carry their positions with them (LLM-101-CN section 6, the questions after 6.2).  Same rotation,
+ * arguments and requirements as ring_attn_rope plus shard in [0, n_shards); bit-identical to the
+ * same rows of ring_attn_rope on the whole sequence.
+ */
+RA_API ra_status ring_attn_block_rope(void* x, int B, int H, int L, int d, int n_shards, int shard, int layout,
+                                      int dtype, double base, int inverse, void* stream);
 RA_API ra_status ring_attn_f32_zero(float* x, long long count, void* stream);
 RA_API ra_status ring_attn_f32_add(float* acc, const float* part, long long count, void* stream);
 RA_API ra_status ring_attn_f32_convert(const float* src, void* dst, long long count, int dtype, void* stream);

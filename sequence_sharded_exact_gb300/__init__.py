@@ -23,6 +23,7 @@ from .binding import (  # noqa: F401
     bwd_preprocess,
     block_bwd,
     block_fwd,
+    block_rope,
     f32_add,
     f32_convert,
     f32_zero,

@@ -35,7 +35,7 @@ EXPORTS = (
     "ring_attn_ring_step_fwd_accumulate",
     "ring_attn_fwd_host_workspace_size", "ring_attn_selftest_bounded_wait", "ring_attn_device_check",
     "ring_attn_block_fwd", "ring_attn_block_bwd", "ring_attn_bwd_preprocess", "ring_attn_f32_zero",
-    "ring_attn_f32_add", "ring_attn_f32_convert",
+    "ring_attn_f32_add", "ring_attn_f32_convert", "ring_attn_block_rope",
 )
 
 
@@ -84,6 +84,8 @@ def library():
         lib.ring_attn_f32_add.restype = ctypes.c_int
         lib.ring_attn_f32_convert.argtypes = [P, P, LL, I, P]
         lib.ring_attn_f32_convert.restype = ctypes.c_int
+        lib.ring_attn_block_rope.argtypes = [P, I, I, I, I, I, I, I, I, ctypes.c_double, I, P]
+        lib.ring_attn_block_rope.restype = ctypes.c_int
         lib.ring_attn_last_error.argtypes = []
         lib.ring_attn_last_error.restype = ctypes.c_char_p
         lib.ring_attn_abi_version.argtypes = []
@@ -650,3 +652,20 @@ def f32_convert(src, dtype, dst=None, stream=None):
     _check(library().ring_attn_f32_convert(_ptr(src), _ptr(dst), int(src.numel()), _dtype_code(dtype),
                                            _stream(stream, src.device)))
     return dst
+
+
+def block_rope(x, n_shards, shard, layout="zigzag", base=10000.0, inverse=False, stream=None):
+    """ring_attn_block_rope: rotary position embedding, in place, of one device's shard x [B, H, S, d]
+    (shard `shard` of n_shards; bf16 or float32), each row by its natural position in the whole
+    sequence.  Returns x."""
+    if x.dim() != 4:
+        raise ValueError("x must be [B, H, S, d]")
+    _need(x, "x", x.device)
+    B, H, S, d = (int(t) for t in x.shape)
+    n = int(n_shards)
+    if not 0 <= int(shard) < n:
+        raise ValueError("shard must lie in [0, n_shards)")
+    _check(library().ring_attn_block_rope(_ptr(x), B, H, n * S, d, n, int(shard), _layout(layout),
+                                          _dtype_code(x.dtype), float(base), int(bool(inverse)),
+                                          _stream(stream, x.device)))
+    return x

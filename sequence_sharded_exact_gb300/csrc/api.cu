@@ -541,6 +541,20 @@ ra_status ring_attn_rope(void* x, int B, int H, int L, int d, int n_shards, int 
     return RA_OK;
 }
 
+ra_status ring_attn_block_rope(void* x, int B, int H, int L, int d, int n_shards, int shard, int layout, int dtype,
+                               double base, int inverse, void* stream)
+{
+    Problem p{B, H, H, L, d, n_shards, 0, layout, dtype};
+    ra_status st = check_block(p, shard, shard, 0, "-");
+    if (st != RA_OK) return st;
+    if (!(base > 0.0) || !isfinite(base)) return fail(RA_ERR_INVALID_ARG, "base must be positive and finite");
+    if ((st = check_ptrs({x})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaError_t e = launch_rope(p, x, base, inverse, static_cast<cudaStream_t>(stream), shard);
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_block_rope launch");
+    return RA_OK;
+}
+
 namespace {
 
 ra_status check_ulysses_heads(const Problem& p)

@@ -68,8 +68,9 @@ cudaError_t launch_bwd_tc(const Problem& p, const void* q, const void* k, const 
                           const BlockView* blk = nullptr);
 
 // HBM-bound helper kernels.
-// Rotary position embedding by natural position, in place, of a [B][H][L][d] buffer (p.H heads).
-cudaError_t launch_rope(const Problem& p, void* x, double base, int inverse, cudaStream_t s);
+// Rotary position embedding by natural position, in place, of a [B][H][L][d] buffer (p.H heads),
+// or (shard >= 0) of one device's [B][H][L/n][d] buffer holding shard `shard`'s rows.
+cudaError_t launch_rope(const Problem& p, void* x, double base, int inverse, cudaStream_t s, int shard = -1);
 // Ulysses all-to-all re-layout between the token split [n][B][S][H][row] and the head split
 // [n][B][H/n][L][row] (direction 0 token -> head, 1 back); row_bytes a multiple of 4.
 cudaError_t launch_ulysses_a2a(const Geometry& geo, int B, int H, int row_bytes, const void* src, void* dst,

@@ -15,6 +15,8 @@
 //
 // One thread owns a 16-byte chunk of one (batch, position) row and computes its angles once, then
 // rotates that chunk in every head (the heads of a position share its angles).
+// A buffer holds `rows` rows per head: the whole sequence (rows = L, row_off = 0), or one device's
+// shard (rows = S = L / n, row_off = shard * S: local row r is whole-sequence row r + row_off).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -26,6 +28,7 @@ namespace {
 struct RopeArgs {
     Geometry geo;
     int B, H;
+    int rows, row_off;  // rows per head in the buffer; whole-sequence row of local row 0
     int inverse;
     unsigned long long turn[64];  // theta_i / (2 pi) in units of 2^-64 turn
 };
@@ -42,7 +45,7 @@ template <int D>
 __global__ void __launch_bounds__(256) rope_bf16_kernel(__nv_bfloat16* __restrict__ x, const RopeArgs a)
 {
     constexpr int kChunks = D / 8;  // 8 bf16 = 4 pairs per chunk
-    const long long L = a.geo.L;
+    const long long L = a.rows;
     const long long total = (long long)a.B * L * kChunks;
     const long long step = (long long)gridDim.x * blockDim.x;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += step) {
@@ -50,7 +53,7 @@ __global__ void __launch_bounds__(256) rope_bf16_kernel(__nv_bfloat16* __restric
         const long long br = idx / kChunks;
         const int r = (int)(br % L);
         const int b = (int)(br / L);
-        const unsigned long long p = (unsigned long long)natural_position(a.geo, r);
+        const unsigned long long p = (unsigned long long)natural_position(a.geo, r + a.row_off);
         float c[4], s[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -81,7 +84,7 @@ template <int D>
 __global__ void __launch_bounds__(256) rope_f32_kernel(float* __restrict__ x, const RopeArgs a)
 {
     constexpr int kChunks = D / 4;  // 4 floats = 2 pairs per chunk
-    const long long L = a.geo.L;
+    const long long L = a.rows;
     const long long total = (long long)a.B * L * kChunks;
     const long long step = (long long)gridDim.x * blockDim.x;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += step) {
@@ -89,7 +92,7 @@ __global__ void __launch_bounds__(256) rope_f32_kernel(float* __restrict__ x, co
         const long long br = idx / kChunks;
         const int r = (int)(br % L);
         const int b = (int)(br / L);
-        const unsigned long long p = (unsigned long long)natural_position(a.geo, r);
+        const unsigned long long p = (unsigned long long)natural_position(a.geo, r + a.row_off);
         float c[2], s[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -119,12 +122,14 @@ unsigned rope_grid(long long items)
 
 }  // namespace
 
-cudaError_t launch_rope(const Problem& p, void* x, double base, int inverse, cudaStream_t s)
+cudaError_t launch_rope(const Problem& p, void* x, double base, int inverse, cudaStream_t s, int shard)
 {
     RopeArgs a;
     a.geo = p.geo();
     a.B = p.B;
     a.H = p.H;
+    a.rows = shard < 0 ? p.L : p.L / p.n;
+    a.row_off = shard < 0 ? 0 : shard * (p.L / p.n);
     a.inverse = inverse ? 1 : 0;
     const double two_pi = 6.283185307179586476925;
     for (int i = 0; i < 64; ++i) {
@@ -135,7 +140,7 @@ cudaError_t launch_rope(const Problem& p, void* x, double base, int inverse, cud
             a.turn[i] = (unsigned long long)ldexp(frac, 64);
         }
     }
-    const long long rows = (long long)p.B * p.L;
+    const long long rows = (long long)p.B * a.rows;
     if (p.dtype == 1) {
         const long long items = rows * (p.d / 8);
         if (p.d == 128)

@@ -89,8 +89,28 @@ def errors(got, ref):
     return ma, rl
 
 
+def reference(x, n, causal, layout, rope_base):
+    """The float64 oracle of the whole sequence: out, lse and the gradients with respect to q, k, v.
+    With rope_base, q and k are first rotated by natural position (the oracle's rotation, rounded to
+    the inputs' dtype as the in-place rotation stores it) and dq, dk are rotated back."""
+    import oracle
+
+    q, k = x["q"], x["k"]
+    if rope_base:
+        q = torch.from_numpy(oracle.rope(q, n, layout, rope_base)).to(x["q"].dtype)
+        k = torch.from_numpy(oracle.rope(k, n, layout, rope_base)).to(x["k"].dtype)
+    o, l = oracle.attn_fwd(q, k, x["v"], n, causal, layout)
+    dq, dk, dv = oracle.attn_bwd(q, k, x["v"], x["dout"], n, causal, layout)
+    if rope_base:
+        dq = oracle.rope(dq, n, layout, rope_base, inverse=True)
+        dk = oracle.rope(dk, n, layout, rope_base, inverse=True)
+    return o, l, dq, dk, dv
+
+
 def run_rank(rank, world, port, cases, device, result_dir):
-    """One rank: every case is (B, H, Hkv, L, d, causal, layout, dtype name, grad dtype name, seed)."""
+    """One rank: every case is (B, H, Hkv, L, d, causal, layout, dtype name, grad dtype name, seed[,
+    rope base]); with a rope base the rank rotates its q and k shards before the ring and its dq, dk
+    back after it (GPU ranks only)."""
     os.environ.setdefault("GLOO_SOCKET_IFNAME", "lo")
     ok = True
     try:
@@ -103,7 +123,8 @@ def run_rank(rank, world, port, cases, device, result_dir):
         comm = ring.RingComm()
         assert comm.rank == rank and comm.world == world and comm.next == (rank + 1) % world
         n = world
-        for (B, H, Hkv, L, d, causal, layout, dt, gdt, seed) in cases:
+        for case in cases:
+            (B, H, Hkv, L, d, causal, layout, dt, gdt, seed), rope_base = case[:10], (case[10:] or (0.0,))[0]
             dtype = getattr(torch, dt)
             gdtype = getattr(torch, gdt)
             x = synth.make_inputs(B, H, Hkv, L, d, dtype=dtype, seed=seed, with_dout=True)
@@ -112,8 +133,7 @@ def run_rank(rank, world, port, cases, device, result_dir):
                 z = np.load(ref_file)
                 ref_o, ref_l, rq, rk, rv = (z[t] for t in ("o", "l", "dq", "dk", "dv"))
             else:
-                ref_o, ref_l = oracle.attn_fwd(x["q"], x["k"], x["v"], n, causal, layout)
-                rq, rk, rv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], n, causal, layout)
+                ref_o, ref_l, rq, rk, rv = reference(x, n, causal, layout, rope_base)
             S = L // n
             sl = slice(rank * S, (rank + 1) * S)
             mine = {t: shard(x[t], rank, n) for t in ("q", "k", "v", "dout")}
@@ -131,13 +151,21 @@ def run_rank(rank, world, port, cases, device, result_dir):
                 tol = {"out": 1e-10, "lse": 1e-10, "dq": 1e-10, "dk": 1e-10, "dv": 1e-10}
                 rel = 1e-10
             else:
+                from sequence_sharded_exact_gb300 import binding
+
                 dev = torch.device("cuda", 0)
                 g = {t: v.to(dev) for t, v in mine.items()}
-                out, lse = ring.ring_fwd(g["q"], g["k"], g["v"], comm, causal, layout)
-                dq, dk, dv = ring.ring_bwd(g["q"], g["k"], g["v"], out, lse, g["dout"], comm, causal, layout,
-                                           grad_dtype=gdtype)
+                qr, kr = g["q"], g["k"]
+                if rope_base:  # positions follow the blocks: each rank turns its own rows by natural position
+                    qr = binding.block_rope(g["q"].clone(), n, rank, layout, base=rope_base)
+                    kr = binding.block_rope(g["k"].clone(), n, rank, layout, base=rope_base)
+                out, lse = ring.ring_fwd(qr, kr, g["v"], comm, causal, layout)
+                dq, dk, dv = ring.ring_bwd(qr, kr, g["v"], out, lse, g["dout"], comm, causal, layout,
+                                           grad_dtype=torch.float32 if rope_base else gdtype)
+                if rope_base:  # gradients with respect to the unrotated q and k
+                    binding.block_rope(dq, n, rank, layout, base=rope_base, inverse=True)
+                    binding.block_rope(dk, n, rank, layout, base=rope_base, inverse=True)
                 torch.cuda.synchronize()
-                from sequence_sharded_exact_gb300 import binding
 
                 assert binding.device_status() == 0
                 lim = 1e-4 if dtype == torch.float32 else 2e-2
@@ -179,10 +207,10 @@ def precompute_refs(world, cases, result_dir):
     import oracle
     from sequence_sharded_exact_gb300 import synth
 
-    for (B, H, Hkv, L, d, causal, layout, dt, gdt, seed) in cases:
+    for case in cases:
+        (B, H, Hkv, L, d, causal, layout, dt, gdt, seed), rope_base = case[:10], (case[10:] or (0.0,))[0]
         x = synth.make_inputs(B, H, Hkv, L, d, dtype=getattr(torch, dt), seed=seed, with_dout=True)
-        o, l = oracle.attn_fwd(x["q"], x["k"], x["v"], world, causal, layout)
-        dq, dk, dv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], world, causal, layout)
+        o, l, dq, dk, dv = reference(x, world, causal, layout, rope_base)
         np.savez(os.path.join(result_dir, f"ref_{seed}.npz"), o=o, l=l, dq=dq, dk=dk, dv=dv)
 
 

@@ -9,7 +9,8 @@ Depth of the element-by-element checks, per workload:
   * zigzag_gqa_64k_train (L65536, n16): dQ on 4096 seeded rows; dK and dV on keys of one kv head
     spread over the whole natural range -- natural positions 0-127 (every query of the group sees
     them: the longest accumulations), the first and last key of every chunk, and seeded random keys;
-  * the striped workloads and a 262144-token sequence: sampled rows plus chunk edges.
+  * the striped workloads, the head-dim-64 workloads and a 262144-token sequence: sampled rows plus
+    chunk edges (backward: sampled dQ rows and the last keys' dK/dV).
 Every check reports max-abs and relative L2 error per tensor; the bound is the bf16 one (max-abs 2e-2
 and relative L2 5e-3, both).  Properties that hold at any size (finite outputs, sum identities of
 the gradients) are checked as well."""
@@ -35,18 +36,33 @@ def _clean_status():
     assert ra.device_status() == 0, "a bounded wait ran out inside a kernel"
 
 
-def sampled_rows(w, count, seed):
+def sampled_rows(w, count, seed, split=False):
     """Random rows over all heads, plus the first and last rows of every chunk of the first and
-    last head (chunk boundaries, the start of the sequence and the diagonal tiles)."""
+    last head (chunk boundaries, the start of the sequence and the diagonal tiles).  With split,
+    returns (all rows, mask of the uniformly drawn ones)."""
     B, H, L, n = w["B"], w["H"], w["L"], w["n"]
     rng = np.random.default_rng(seed)
-    rows = set(rng.choice(B * H * L, size=count, replace=False).tolist())
+    uniform = set(rng.choice(B * H * L, size=count, replace=False).tolist())
+    rows = set(uniform)
     chunk = L // n // (2 if w["layout"] == "zigzag" else 1)
     for h in (0, H - 1):
         for c in range(L // chunk):
             for r in (c * chunk, c * chunk + 1, c * chunk + chunk - 1):
                 rows.add(((B - 1) * H + h) * L + r)
-    return np.array(sorted(rows), dtype=np.int64)
+    rows = np.array(sorted(rows), dtype=np.int64)
+    if split:
+        return rows, np.array([r in uniform for r in rows])
+    return rows
+
+
+def check_sampled(got, ref, uniform, what):
+    """The bf16 bound on sampled rows: max-abs on every checked row, relative L2 (a per-tensor
+    statistic) estimated from the uniformly drawn rows only -- the chunk-edge rows include the
+    sequence's second and third tokens, whose few visible keys give the largest gradients of the
+    tensor, and would dominate a norm over the hand-picked set."""
+    ma = float(np.abs(np.asarray(got) - np.asarray(ref)).max())
+    _, rl = errors(np.asarray(got)[uniform], np.asarray(ref)[uniform])
+    assert ma <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"{what}: max-abs {ma:.3e}, rel-L2 (uniform rows) {rl:.3e}"
 
 
 def report(capsys, name, what, got, ref):
@@ -137,6 +153,16 @@ def test_training_backward_over_the_whole_range(capsys):
     nat = np.array([oracle.natural_position(r, L, n, w["layout"]) for r in range(L)], dtype=np.int64)
     row_of = np.empty(L, dtype=np.int64)
     row_of[nat] = np.arange(L)
+    # the first 64 positions of every head: few visible keys, the largest gradients of the tensor
+    # (element-wise bound only: a relative L2 is a per-tensor statistic, estimated above)
+    early = np.array([((b * H + h) * L + int(row_of[p])) for b in range(B) for h in range(H) for p in range(64)],
+                     dtype=np.int64)
+    ref_e = oracle.attn_bwd_dq_rows(host["q"], host["k"], host["v"], host["dout"], n, w["causal"], w["layout"], early)
+    got_e = to_np(dq.view(-1, d)[torch.from_numpy(early).to(DEV)])
+    ma = float(np.abs(got_e - ref_e).max())
+    with capsys.disabled():
+        print(f"\n[parity] {name} dq, positions 0-63 of every head: {ref_e.size} values, max-abs {ma:.3e}")
+    assert ma <= BF16_MAX_ABS, f"dq at early positions: max-abs {ma:.3e}"
     chunk = L // (2 * n)
     positions = set(range(128))
     for c in range(L // chunk):
@@ -153,7 +179,7 @@ def test_training_backward_over_the_whole_range(capsys):
     report(capsys, name, "dv, " + what, to_np(dv.view(-1, d)[idx]), ref_dv)
 
 
-@pytest.mark.parametrize("name", ["zigzag_gqa_64k_train", "striped_gqa_128k"])
+@pytest.mark.parametrize("name", ["zigzag_gqa_64k_train", "striped_gqa_128k", "zigzag_gqa_128k_d64"])
 def test_full_size_forward_sampled_rows(name):
     w = synth.WORKLOADS[name]
     B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
@@ -163,15 +189,14 @@ def test_full_size_forward_sampled_rows(name):
     torch.cuda.synchronize()
     # properties at any size: finite everywhere, lse bounded by log of the visible count + max score
     assert torch.isfinite(out).all().item() and torch.isfinite(lse).all().item()
-    rows = sampled_rows(w, 384, seed=L)
+    rows, uniform = sampled_rows(w, 384, seed=L, split=True)
     host = {t: x[t].cpu() for t in ("q", "k", "v")}
     ref_o, ref_l = oracle.attn_fwd_rows(host["q"], host["k"], host["v"], n, w["causal"],
                                         w["layout"], rows)
     got_o = to_np(out.view(-1, d)[torch.from_numpy(rows).to(DEV)])
     got_l = to_np(lse.view(-1)[torch.from_numpy(rows).to(DEV)])
     for got, ref, what in ((got_o, ref_o, "out"), (got_l, ref_l, "lse")):
-        ma, rl = errors(got, ref)
-        assert ma <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"{name} {what}: {ma:.3e} {rl:.3e}"
+        check_sampled(got, ref, uniform, f"{name} {what}")
 
 
 def test_full_size_stepwise_matches_fused():
@@ -188,7 +213,7 @@ def test_full_size_stepwise_matches_fused():
     assert (l1 - l2).abs().max().item() < 1e-3
 
 
-@pytest.mark.parametrize("name", ["zigzag_gqa_64k_train", "striped_gqa_64k_train"])
+@pytest.mark.parametrize("name", ["zigzag_gqa_64k_train", "striped_gqa_64k_train", "zigzag_gqa_64k_train_d64"])
 def test_full_size_training_backward(name):
     """The training workload (L=65536, n=16, causal, GQA 4:1): dQ on sampled rows and
     dK/dV on the last keys of the sequence (whose visible queries are few enough for the oracle),
@@ -208,12 +233,11 @@ def test_full_size_training_backward(name):
     assert (dv.double().sum(dim=2) - dsum).abs().max().item() < 0.5
     assert dk.double().sum(dim=2).abs().max().item() < 0.5
     host = {t: x[t].cpu() for t in ("q", "k", "v", "dout")}
-    rows = sampled_rows(w, 96, seed=5)
+    rows, uniform = sampled_rows(w, 96, seed=5, split=True)
     ref_dq = oracle.attn_bwd_dq_rows(host["q"], host["k"], host["v"], host["dout"], n,
                                      w["causal"], w["layout"], rows)
     got_dq = to_np(dq.view(-1, d)[torch.from_numpy(rows).to(DEV)])
-    ma, rl = errors(got_dq, ref_dq)
-    assert ma <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"dq {ma:.3e} {rl:.3e}"
+    check_sampled(got_dq, ref_dq, uniform, f"{name} dq")
     # keys at the last natural positions, in both kv heads at the ends of the head range
     last = [oracle.natural_position(r, L, n, w["layout"]) for r in range(L)]
     order = np.argsort(last)[-24:]
@@ -236,10 +260,9 @@ def test_forward_at_262144_tokens_sampled_rows():
     torch.cuda.synchronize()
     assert torch.isfinite(out).all().item() and torch.isfinite(lse).all().item()
     w = dict(B=B, H=H, L=L, n=n, layout="zigzag")
-    rows = sampled_rows(w, 160, seed=3)
+    rows, uniform = sampled_rows(w, 160, seed=3, split=True)
     host = {t: x[t].cpu() for t in ("q", "k", "v")}
     ref_o, ref_l = oracle.attn_fwd_rows(host["q"], host["k"], host["v"], n, True, "zigzag", rows)
     idx = torch.from_numpy(rows).to(DEV)
     for got, ref, what in ((to_np(out.view(-1, d)[idx]), ref_o, "out"), (to_np(lse.view(-1)[idx]), ref_l, "lse")):
-        ma, rl = errors(got, ref)
-        assert ma <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"{what}: {ma:.3e} {rl:.3e}"
+        check_sampled(got, ref, uniform, what)

@@ -3,7 +3,8 @@ that share cuda:0 and pass the blocks over gloo (staged through host memory).  N
 another rank: every exchange happens on the host between launches, so the ranks' kernels are
 independent launches.  Each rank checks its shard of out, lse, dq, dk and dv against the float64
 oracle of the whole sequence, in the contiguous, zigzag and striped layouts, on the tensor-core
-path (bf16, head dim 128 and 64) and on the CUDA-core path (float32)."""
+path (bf16, head dim 128 and 64) and on the CUDA-core path (float32); two cases rotate q and k by
+natural position on each rank first (ring_attn_block_rope), as the pages ask when blocks travel."""
 import pytest
 import torch
 
@@ -15,12 +16,14 @@ CASES = {  # B, H, Hkv, L, d, causal, layout, dtype, grad dtype, seed
     2: [(1, 4, 2, 4096, 128, True, "zigzag", "bfloat16", "float32", 201),
         (1, 2, 1, 2048, 128, True, "contiguous", "bfloat16", "bfloat16", 202),
         (1, 2, 2, 2048, 64, True, "striped", "bfloat16", "float32", 203),
-        (1, 2, 1, 512, 64, True, "zigzag", "float32", "float32", 204)],
+        (1, 2, 1, 512, 64, True, "zigzag", "float32", "float32", 204),
+        (1, 4, 2, 4096, 128, True, "zigzag", "bfloat16", "float32", 210, 10000.0)],  # RoPE by natural position
     4: [(1, 4, 2, 4096, 128, True, "zigzag", "bfloat16", "float32", 205),
         (2, 2, 1, 2048, 128, True, "contiguous", "bfloat16", "float32", 206),
         (1, 4, 1, 4096, 128, True, "striped", "bfloat16", "float32", 207),
         (1, 2, 1, 2048, 128, False, "zigzag", "bfloat16", "float32", 208),
-        (1, 2, 2, 512, 128, True, "zigzag", "float32", "float32", 209)],
+        (1, 2, 2, 512, 128, True, "zigzag", "float32", "float32", 209),
+        (1, 2, 1, 4096, 128, True, "striped", "bfloat16", "float32", 211, 500000.0)],
 }
 
 

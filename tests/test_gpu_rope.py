@@ -86,3 +86,19 @@ def test_rope_gradient_chain(layout):
     assert_close(to_np(dq), oracle.rope(rq.astype(np.float32), n, layout, inverse=True), torch.bfloat16, "dq")
     assert_close(to_np(dk), oracle.rope(rk.astype(np.float32), n, layout, inverse=True), torch.bfloat16, "dk")
     assert_close(to_np(dv), rv, torch.bfloat16, "dv")
+
+
+@pytest.mark.parametrize("layout,n", [("contiguous", 4), ("zigzag", 4), ("striped", 8), ("zigzag", 1)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("inverse", [False, True])
+def test_block_rope_equals_the_whole_sequence_rotation(layout, n, dtype, inverse):
+    """One device's rotation of its own shard (ring_attn_block_rope) gives bit for bit the rows of the
+    whole-sequence rotation: every row turns by its natural position, wherever it is stored."""
+    B, H, L, d = 2, 3, 4096, 128
+    x = synth.make_inputs(B, H, H, L, d, dtype=dtype, seed=77, device="cuda:0")["q"]
+    whole = ra.rope(x.clone(), n, layout, base=500000.0, inverse=inverse)
+    S = L // n
+    for i in range(n):
+        part = x[:, :, i * S:(i + 1) * S].contiguous()
+        ra.block_rope(part, n, i, layout, base=500000.0, inverse=inverse)
+        assert torch.equal(part, whole[:, :, i * S:(i + 1) * S]), f"shard {i}"
