@@ -145,6 +145,7 @@ struct KvUnit {
     int shard;     // kv shard
     int per_head;  // query tiles per head
     int ntiles;    // query tiles over all heads of the group
+    int rev;       // walk the heads of the group last to first (the second tile of a mirrored pair)
 };
 
 // The query rows of chunk c of the shard the K/V tile meets at step st that can see it, widened
@@ -174,14 +175,24 @@ __device__ __forceinline__ int q_tiles_per_head(const BwdArgs& a, int shard, int
 
 __device__ __forceinline__ bool unit_of(const BwdArgs& a, long long item, int member, KvUnit& u)
 {
-    const int pair = (int)(item % a.pairs);
-    long long rest = item / a.pairs;
     // striped and block calls: tiles of consecutive rows inside one shard
     const bool rowwise = a.geo.layout == 2 || a.blk;
     int shard = a.blk ? a.kv_shard : 0;
+    int pair;
+    long long rest;
     if (a.geo.layout == 2 && !a.blk) {
-        shard = (int)(rest % a.geo.n);
-        rest /= a.geo.n;
+        // Striped: the shard index varies fastest, so that the CTAs running at the same time hold the
+        // same few local tiles of every shard -- tiles whose query walks are equally long.  With the
+        // pair index fastest they held every local tile of a few shards, walked the query heads at
+        // rates up to 1.9x apart, and spread their Q, dO and dQ over all heads of the group at once
+        // (L2 read misses 30%, 206 GB of DRAM traffic per 64K launch).
+        shard = (int)(item % a.geo.n);
+        rest = item / a.geo.n;
+        pair = (int)(rest % a.pairs);
+        rest /= a.pairs;
+    } else {
+        pair = (int)(item % a.pairs);
+        rest = item / a.pairs;
     }
     u.g = (int)(rest % a.Hkv);
     u.b = (int)(rest / a.Hkv);
@@ -196,6 +207,7 @@ __device__ __forceinline__ bool unit_of(const BwdArgs& a, long long item, int me
     }
     u.shard = u.rk / a.geo.S;
     u.per_head = q_tiles_per_head(a, u.shard, u.pk);
+    u.rev = member & 1;
     u.ntiles = u.per_head * a.G;
     return true;
 }
@@ -232,15 +244,24 @@ __device__ __forceinline__ bool unit_in_slot(const BwdArgs& a, int s, KvUnit& u)
 }
 
 // Query tiles of a unit: heads of the group in turn, each walking the query shards in ring order.
+// The second tile of a mirrored pair walks the heads last to first, so that a CTA goes on with the
+// head it has just finished and the CTAs running together keep to the same heads (their Q, dO and
+// dQ stay in L2).  Striped layout (whole sequence): the query shards are walked in one order for
+// every unit (shard 0, 1, ...), so that the CTAs running together -- the same local tile of every
+// shard, which see the same query tiles -- walk them in step (in ring order they started at 16
+// different shards and each query tile was read at widely spread times).  The order of the sum
+// over query tiles changes only the rounding of dK, dV and dQ.
 struct QWalk {
     Geometry geo;
-    int shard, pk, st, st0, st1, c, t, nt, hh;
+    int shard, pk, st, st0, st1, c, t, nt, hh, G, rev, global;
+    // ring step at which this unit meets walk position st
+    __device__ __forceinline__ int step_of(int s) const { return global ? (s - shard + geo.n) % geo.n : s; }
     KvRange qr;
     __device__ __forceinline__ void settle()
     {
         while (true) {
             while (st < st1) {
-                qr = q_tile_range(geo, shard, st, c, pk);
+                qr = q_tile_range(geo, shard, step_of(st), c, pk);
                 nt = qr.count / kQT;
                 if (nt > 0) return;
                 if (++c == geo.cps) {
@@ -259,6 +280,9 @@ struct QWalk {
         geo = a.geo;
         shard = u.shard;
         pk = u.pk;
+        G = a.G;
+        rev = u.rev;
+        global = a.geo.layout == 2 && !a.blk;
         st0 = a.blk ? a.step : 0;  // a block call walks its one ring step
         st1 = a.blk ? a.step + 1 : a.geo.n;
         st = st0;
@@ -270,7 +294,7 @@ struct QWalk {
     // head within the group, buffer row and natural position of the next query tile
     __device__ __forceinline__ void next(int& head, int& row, int& nat)
     {
-        head = hh;
+        head = rev ? G - 1 - hh : hh;
         row = qr.row0 + t * kQT;
         nat = qr.nat0 + t * kQT * geo.stride;
         if (++t == nt) {
