@@ -1,6 +1,7 @@
 """The multi-device ring on CPU ranks (gloo, world sizes 2 to 4): sequence_sharded_exact_gb300.ring
 schedules the blocks and moves them with torch.distributed point-to-point operations, and the
-per-device compute is the float64 oracle's block functions.  Every rank checks its shard of out,
+per-device compute is the float64 oracle's block functions (world size 1 is the degenerate ring: one
+device, one block, no transfer).  Every rank checks its shard of out,
 lse, dq, dk and dv against the oracle of the whole sequence (1e-10), and the order of its block calls
 (step r computes block (rank - r) mod n; the first writes, the later ones fold in)."""
 import pytest
@@ -15,7 +16,7 @@ CASES = [  # B, H, Hkv, L, d, causal, layout, dtype, grad dtype, seed
 ]
 
 
-@pytest.mark.parametrize("world", [2, 3, 4])
+@pytest.mark.parametrize("world", [1, 2, 3, 4])
 def test_ring_on_gloo_ranks_matches_full_attention(world, tmp_path):
     cases = [c for c in CASES if c[3] % (2 * world) == 0]
     ok, errs = launch(world, cases, "cpu", str(tmp_path), timeout=300)
