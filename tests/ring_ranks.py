@@ -237,3 +237,35 @@ def launch(world, cases, device, result_dir, timeout=600):
             errs.append(open(e).read())
     oks = all(os.path.exists(os.path.join(result_dir, f"rank{r}.ok")) for r in range(world))
     return oks and not errs, errs
+
+
+def run_failing_rank(rank, world, port, mode, result_dir):
+    """Failure detection on the ring (host side, gloo, no GPU): rank 1 leaves before its first transfer
+    ("exit") or stops answering ("stall"); the other ranks' ring_fwd must end with an error within the
+    process group's timeout instead of waiting for ever.  Writes rank<r>.detected with the seconds it
+    took, or rank<r>.err."""
+    import datetime
+    import time
+
+    os.environ.setdefault("GLOO_SOCKET_IFNAME", "lo")
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=5))
+    from sequence_sharded_exact_gb300 import ring, synth
+
+    comm = ring.RingComm()
+    L = 48
+    x = synth.make_inputs(1, 2, 1, L, 8, dtype=torch.float32, seed=3)
+    mine = {t: shard(x[t], rank, world) for t in ("q", "k", "v")}
+    if rank == 1:
+        if mode == "exit":
+            os._exit(0)  # leaves between steps: nothing of it is in flight
+        time.sleep(3600)  # stalls; the launcher kills it
+    t0 = time.time()
+    try:
+        ring.ring_fwd(mine["q"], mine["k"], mine["v"], comm, True, "zigzag", ops=OracleOps(L))
+        with open(os.path.join(result_dir, f"rank{rank}.err"), "w") as f:
+            f.write("ring_fwd returned although a neighbour was gone")
+    except Exception as e:  # the transfer failed: the failure was detected
+        with open(os.path.join(result_dir, f"rank{rank}.detected"), "w") as f:
+            f.write(f"{time.time() - t0:.2f} {type(e).__name__}: {str(e)[:200]}")
+    os._exit(0)  # no orderly shutdown: the group has lost a member
