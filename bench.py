@@ -298,6 +298,9 @@ def main():
                     help="run the multi-device ring path also at N = 1 (the default for N > 1)")
     ap.add_argument("--replicas", action="store_true",
                     help="N > 1: one independent copy of the workload per rank instead of the ring")
+    ap.add_argument("--ring-groups", type=int, default=1,
+                    help="the ring as a hierarchical ring: a local ring inside each of this many groups "
+                         "of consecutive ranks (e.g. the GPUs of one node), a global ring across them")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -543,6 +546,11 @@ def run_ring(args, w, world, rank, local):
     else:
         dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % free_port(), rank=0, world_size=1)
     comm = ring.RingComm()
+    grid = ring.RingGrid(comm, args.ring_groups) if args.ring_groups > 1 else None
+    rfwd = (lambda *a, **kw: ring.ring_fwd(*a[:3], comm, *a[3:], **kw)) if grid is None else \
+        (lambda *a, **kw: ring.ring_fwd_2d(*a[:3], grid, *a[3:], **kw))
+    rbwd = (lambda *a, **kw: ring.ring_bwd(*a[:6], comm, *a[6:], **kw)) if grid is None else \
+        (lambda *a, **kw: ring.ring_bwd_2d(*a[:6], grid, *a[6:], **kw))
     stream = torch.cuda.current_stream(dev)
     B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
     n, causal, layout = world, w["causal"], w["layout"]
@@ -562,9 +570,9 @@ def run_ring(args, w, world, rank, local):
     res = {}
 
     def step():
-        out, lse = ring.ring_fwd(mine["q"], mine["k"], mine["v"], comm, causal, layout, ops=ops)
+        out, lse = rfwd(mine["q"], mine["k"], mine["v"], causal, layout, ops=ops)
         if train:
-            ring.ring_bwd(mine["q"], mine["k"], mine["v"], out, lse, mine["dout"], comm, causal, layout, ops=ops)
+            rbwd(mine["q"], mine["k"], mine["v"], out, lse, mine["dout"], causal, layout, ops=ops)
         res["out"], res["lse"] = out, lse
 
     for _ in range(args.warmup):
@@ -598,7 +606,9 @@ def run_ring(args, w, world, rank, local):
         "data": "synthetic: q,k,v ~ N(0,1) bf16" + (", 1% of key rows x8" if w["spike_frac"] else "")
                 + (", dO ~ N(0,1)" if train else "") + ", seeded",
         "config": dict(config_dict(dict(w, n=n), args.step),
-                       parallelism=f"context parallel: ring over {world} device(s), one shard of {S} tokens each",
+                       parallelism=f"context parallel: ring over {world} device(s), one shard of {S} tokens each"
+                                   + (f", hierarchical: {args.ring_groups} groups of {world // args.ring_groups}"
+                                      if grid is not None else ""),
                        mode="multi-device ring (blocks over NCCL)" if world > 1 else "ring path on one device"),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_b, "unit": "TFLOP/s",
                      "frac": achieved / peak_b, "traffic": None,
@@ -622,9 +632,9 @@ def run_ring(args, w, world, rank, local):
     def e2e_step():
         for t in mine:
             d_in[t].copy_(h_in[t], non_blocking=True)
-        out, lse = ring.ring_fwd(d_in["q"], d_in["k"], d_in["v"], comm, causal, layout, ops=ops)
+        out, lse = rfwd(d_in["q"], d_in["k"], d_in["v"], causal, layout, ops=ops)
         if train:
-            ring.ring_bwd(d_in["q"], d_in["k"], d_in["v"], out, lse, d_in["dout"], comm, causal, layout, ops=ops)
+            rbwd(d_in["q"], d_in["k"], d_in["v"], out, lse, d_in["dout"], causal, layout, ops=ops)
         h_out[0].copy_(out, non_blocking=True)
         h_out[1].copy_(lse, non_blocking=True)
 

@@ -44,10 +44,17 @@ class RingComm:
         self._gnext = dist.get_global_rank(group, self.next) if group is not None else self.next
         self._gprev = dist.get_global_rank(group, self.prev) if group is not None else self.prev
 
-    def start(self, send, recv, tag=0):
-        """Starts sending the tensors `send` to rank + 1 and receiving into `recv` (same shapes and
-        dtypes) from rank - 1, with message tags tag, tag + 1, ...: transfers that are in flight at
-        the same time must use different tags.  Returns a handle for ``wait``."""
+    def global_rank(self, r):
+        """Global rank of rank r of this communicator's group."""
+        return dist.get_global_rank(self.group, r) if self.group is not None else r
+
+    def start(self, send, recv, tag=0, dst=None, src=None):
+        """Starts sending the tensors `send` to rank dst (default rank + 1) and receiving into `recv`
+        (same shapes and dtypes) from rank src (default rank - 1), ranks of this group, with message
+        tags tag, tag + 1, ...: transfers that are in flight at the same time must use different
+        tags.  Returns a handle for ``wait``."""
+        gdst = self._gnext if dst is None else self.global_rank(dst)
+        gsrc = self._gprev if src is None else self.global_rank(src)
         assert len(send) == len(recv)
         staged = self.backend == "gloo" and any(t.is_cuda for t in send)
         if staged:
@@ -58,8 +65,8 @@ class RingComm:
             s_host, r_host = list(send), list(recv)
         ops = []
         for x, (s, r) in enumerate(zip(s_host, r_host)):
-            ops.append(dist.P2POp(dist.isend, s, self._gnext, self.group, tag + x))
-            ops.append(dist.P2POp(dist.irecv, r, self._gprev, self.group, tag + x))
+            ops.append(dist.P2POp(dist.isend, s, gdst, self.group, tag + x))
+            ops.append(dist.P2POp(dist.irecv, r, gsrc, self.group, tag + x))
         works = dist.batch_isend_irecv(ops)
         return works, (r_host if staged else None), recv
 
@@ -180,5 +187,125 @@ def ring_bwd(q, k, v, out, lse, dout, comm, causal=True, layout="zigzag", grad_d
             cur = nxt
     if n > 1:
         comm.wait(h_acc)  # this device's own block, with every device's contribution
+    dk_acc, dv_acc = acc[slot]
+    return ops.convert(dq_acc, grad_dtype), ops.convert(dk_acc, grad_dtype), ops.convert(dv_acc, grad_dtype)
+
+
+# ------------------------------------------------------------------------------------------------
+# Hierarchical ring: a local ring inside each group of devices, a global ring across the groups
+# ------------------------------------------------------------------------------------------------
+class RingGrid:
+    """The ranks of a RingComm as `groups` groups of Q = world / groups consecutive ranks: rank
+    r = p * Q + q is member q of group p.  The local ring runs inside a group (fast links, e.g. the
+    devices of one node), the global ring across the groups at the same member index (the slow links
+    between nodes): the hierarchical ring the pages suggest for very long contexts (agentalpha "Ring
+    Attention vs tensor parallelism", follow-up 2).  Rank r still holds shard r."""
+
+    def __init__(self, comm, groups):
+        if groups < 1 or comm.world % groups:
+            raise ValueError(f"{groups} groups do not divide {comm.world} ranks")
+        self.comm = comm
+        self.P = groups
+        self.Q = comm.world // groups
+        self.p, self.q = divmod(comm.rank, self.Q)
+
+    def rank(self, p, q):
+        return (p % self.P) * self.Q + (q % self.Q)
+
+    def held(self, a, b):
+        """Shard of the K/V block this rank holds at global step a, local step b."""
+        return self.rank(self.p - a, self.q - b)
+
+
+def ring_fwd_2d(q, k, v, grid, causal=True, layout="zigzag", ops=None):
+    """Ring forward over a RingGrid: for each global step a = 0..P-1 the block that arrived over the
+    global ring (at a = 0 the device's own) goes round the local ring in Q local steps, while the next
+    one comes from the previous group: one inter-group transfer per Q block steps, overlapped with
+    them.  At (a, b) this rank holds the block of shard grid.held(a, b); over the P * Q steps it meets
+    every shard once.  Same inputs and results as ring_fwd."""
+    ops = ops or LibraryOps()
+    comm, P, Q = grid.comm, grid.P, grid.Q
+    n, i = comm.world, comm.rank
+    B, H, S, d = q.shape
+    o_acc = ops.empty_acc((B, H, S, d), q)
+    lse_acc = ops.empty_acc((B, H, S), q)
+    local_spare = _spare_blocks(k, v, Q)
+    global_spare = _spare_blocks(k, v, P)
+    origin = (k, v)
+    step = 0
+    for a in range(P):
+        # this global step's block goes on to the next group while it circulates in this one
+        h_g = (comm.start(origin, global_spare[a % 2], tag=4, dst=grid.rank(grid.p + 1, grid.q),
+                          src=grid.rank(grid.p - 1, grid.q)) if a < P - 1 else None)
+        cur = origin
+        for b in range(Q):
+            nxt = local_spare[b % 2] if b < Q - 1 else None
+            h_l = (comm.start(cur, nxt, tag=0, dst=grid.rank(grid.p, grid.q + 1), src=grid.rank(grid.p, grid.q - 1))
+                   if nxt is not None else None)
+            ops.block_fwd(q, cur[0], cur[1], o_acc, lse_acc, n, i, grid.held(a, b), step > 0, causal, layout)
+            step += 1
+            if h_l is not None:
+                comm.wait(h_l)
+                cur = nxt
+        if h_g is not None:
+            comm.wait(h_g)
+            origin = global_spare[a % 2]
+    return ops.convert(o_acc, q.dtype), lse_acc
+
+
+def ring_bwd_2d(q, k, v, out, lse, dout, grid, causal=True, layout="zigzag", grad_dtype=torch.float32, ops=None):
+    """Ring backward over a RingGrid.  K/V move as in ring_fwd_2d; the dK/dV accumulator of a block
+    always goes to the rank that holds that block next: the next member of the group inside a local
+    round, the next member of the next group (one step along both rings) after its last local step,
+    and after the last step of all to the block's owner.  Same inputs and results as ring_bwd."""
+    ops = ops or LibraryOps()
+    comm, P, Q = grid.comm, grid.P, grid.Q
+    n, i = comm.world, comm.rank
+    B, H, S, d = q.shape
+    Hkv = k.shape[1]
+    D = ops.preprocess(out, dout)
+    dq_acc = ops.empty_acc((B, H, S, d), q)
+    ops.zero(dq_acc)
+    kshape = (B, Hkv, S, d)
+    acc = [tuple(ops.empty_acc(kshape, q) for _ in range(2)) for _ in range(2)]
+    part = tuple(ops.empty_acc(kshape, q) for _ in range(2)) if n > 1 else None
+    local_spare = _spare_blocks(k, v, Q)
+    global_spare = _spare_blocks(k, v, P)
+    origin = (k, v)
+    h_acc, slot, step = None, 0, 0
+    for a in range(P):
+        h_g = (comm.start(origin, global_spare[a % 2], tag=4, dst=grid.rank(grid.p + 1, grid.q),
+                          src=grid.rank(grid.p - 1, grid.q)) if a < P - 1 else None)
+        cur = origin
+        for b in range(Q):
+            nxt = local_spare[b % 2] if b < Q - 1 else None
+            h_l = (comm.start(cur, nxt, tag=0, dst=grid.rank(grid.p, grid.q + 1), src=grid.rank(grid.p, grid.q - 1))
+                   if nxt is not None else None)
+            j = grid.held(a, b)
+            if step == 0:
+                ops.block_bwd(q, cur[0], cur[1], dout, lse, D, dq_acc, acc[0][0], acc[0][1], n, i, j, False, causal,
+                              layout)
+            else:
+                ops.block_bwd(q, cur[0], cur[1], dout, lse, D, dq_acc, part[0], part[1], n, i, j, False, causal,
+                              layout)
+                comm.wait(h_acc)  # block j's accumulator from its previous holder, now in acc[slot]
+                ops.add(acc[slot][0], part[0])
+                ops.add(acc[slot][1], part[1])
+            if n > 1:
+                if b < Q - 1:  # the next holder: the next member of this group
+                    dst, src = grid.rank(grid.p, grid.q + 1), grid.rank(grid.p, grid.q - 1)
+                else:  # after a local round: the next member of the next group
+                    dst, src = grid.rank(grid.p + 1, grid.q + 1), grid.rank(grid.p - 1, grid.q - 1)
+                h_acc = comm.start(acc[slot], acc[1 - slot], tag=2, dst=dst, src=src)
+                slot = 1 - slot
+            step += 1
+            if h_l is not None:
+                comm.wait(h_l)
+                cur = nxt
+        if h_g is not None:
+            comm.wait(h_g)
+            origin = global_spare[a % 2]
+    if n > 1:
+        comm.wait(h_acc)  # this rank's own block, with every rank's contribution
     dk_acc, dv_acc = acc[slot]
     return ops.convert(dq_acc, grad_dtype), ops.convert(dk_acc, grad_dtype), ops.convert(dv_acc, grad_dtype)

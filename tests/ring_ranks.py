@@ -107,10 +107,11 @@ def reference(x, n, causal, layout, rope_base):
     return o, l, dq, dk, dv
 
 
-def run_rank(rank, world, port, cases, device, result_dir):
+def run_rank(rank, world, port, cases, device, result_dir, groups=None):
     """One rank: every case is (B, H, Hkv, L, d, causal, layout, dtype name, grad dtype name, seed[,
     rope base]); with a rope base the rank rotates its q and k shards before the ring and its dq, dk
-    back after it (GPU ranks only)."""
+    back after it (GPU ranks only).  With `groups`, the hierarchical ring (ring_fwd_2d / ring_bwd_2d
+    over that many groups) instead of the flat one."""
     os.environ.setdefault("GLOO_SOCKET_IFNAME", "lo")
     ok = True
     try:
@@ -123,6 +124,21 @@ def run_rank(rank, world, port, cases, device, result_dir):
         comm = ring.RingComm()
         assert comm.rank == rank and comm.world == world and comm.next == (rank + 1) % world
         n = world
+        grid = ring.RingGrid(comm, groups) if groups else None
+
+        def fwd(q_, k_, v_, causal_, layout_, **kw):
+            if grid is None:
+                return ring.ring_fwd(q_, k_, v_, comm, causal_, layout_, **kw)
+            return ring.ring_fwd_2d(q_, k_, v_, grid, causal_, layout_, **kw)
+
+        def bwd(q_, k_, v_, o_, l_, do_, causal_, layout_, **kw):
+            if grid is None:
+                return ring.ring_bwd(q_, k_, v_, o_, l_, do_, comm, causal_, layout_, **kw)
+            return ring.ring_bwd_2d(q_, k_, v_, o_, l_, do_, grid, causal_, layout_, **kw)
+
+        # the block each step computes: (rank - r) mod n on the flat ring, grid.held(a, b) on the grid
+        order = ([(rank - r) % n for r in range(n)] if grid is None else
+                 [grid.held(a, b) for a in range(grid.P) for b in range(grid.Q)])
         for case in cases:
             (B, H, Hkv, L, d, causal, layout, dt, gdt, seed), rope_base = case[:10], (case[10:] or (0.0,))[0]
             dtype = getattr(torch, dt)
@@ -139,15 +155,15 @@ def run_rank(rank, world, port, cases, device, result_dir):
             mine = {t: shard(x[t], rank, n) for t in ("q", "k", "v", "dout")}
             if device == "cpu":
                 ops = OracleOps(L)
-                out, lse = ring.ring_fwd(mine["q"], mine["k"], mine["v"], comm, causal, layout, ops=ops)
-                dq, dk, dv = ring.ring_bwd(mine["q"], mine["k"], mine["v"], out, lse, mine["dout"], comm, causal,
-                                           layout, ops=ops)
-                # the schedule: step r computes block (rank - r) mod n; the first block writes, later
-                # ones fold in; the backward stores each contribution (the accumulators travel)
-                fwd = [c for c in ops.calls if c[0] == "fwd"]
-                bwd = [c for c in ops.calls if c[0] == "bwd"]
-                assert fwd == [("fwd", rank, (rank - r) % n, r > 0) for r in range(n)], fwd
-                assert bwd == [("bwd", rank, (rank - r) % n, False) for r in range(n)], bwd
+                out, lse = fwd(mine["q"], mine["k"], mine["v"], causal, layout, ops=ops)
+                dq, dk, dv = bwd(mine["q"], mine["k"], mine["v"], out, lse, mine["dout"], causal, layout, ops=ops)
+                # the schedule: the first block writes, later ones fold in; the backward stores each
+                # contribution (the accumulators travel); every shard exactly once
+                fcalls = [c for c in ops.calls if c[0] == "fwd"]
+                bcalls = [c for c in ops.calls if c[0] == "bwd"]
+                assert sorted(order) == list(range(n)), order
+                assert fcalls == [("fwd", rank, j, r > 0) for r, j in enumerate(order)], fcalls
+                assert bcalls == [("bwd", rank, j, False) for j in order], bcalls
                 tol = {"out": 1e-10, "lse": 1e-10, "dq": 1e-10, "dk": 1e-10, "dv": 1e-10}
                 rel = 1e-10
             else:
@@ -159,9 +175,9 @@ def run_rank(rank, world, port, cases, device, result_dir):
                 if rope_base:  # positions follow the blocks: each rank turns its own rows by natural position
                     qr = binding.block_rope(g["q"].clone(), n, rank, layout, base=rope_base)
                     kr = binding.block_rope(g["k"].clone(), n, rank, layout, base=rope_base)
-                out, lse = ring.ring_fwd(qr, kr, g["v"], comm, causal, layout)
-                dq, dk, dv = ring.ring_bwd(qr, kr, g["v"], out, lse, g["dout"], comm, causal, layout,
-                                           grad_dtype=torch.float32 if rope_base else gdtype)
+                out, lse = fwd(qr, kr, g["v"], causal, layout)
+                dq, dk, dv = bwd(qr, kr, g["v"], out, lse, g["dout"], causal, layout,
+                                 grad_dtype=torch.float32 if rope_base else gdtype)
                 if rope_base:  # gradients with respect to the unrotated q and k
                     binding.block_rope(dq, n, rank, layout, base=rope_base, inverse=True)
                     binding.block_rope(dk, n, rank, layout, base=rope_base, inverse=True)
@@ -214,13 +230,13 @@ def precompute_refs(world, cases, result_dir):
         np.savez(os.path.join(result_dir, f"ref_{seed}.npz"), o=o, l=l, dq=dq, dk=dk, dv=dv)
 
 
-def launch(world, cases, device, result_dir, timeout=600):
+def launch(world, cases, device, result_dir, timeout=600, groups=None):
     """Spawns `world` ranks running run_rank and returns (all ok, error texts)."""
     import torch.multiprocessing as mp
 
     port = free_port()
-    ctx = mp.start_processes(run_rank, args=(world, port, cases, device, result_dir), nprocs=world, join=False,
-                             start_method="spawn")
+    ctx = mp.start_processes(run_rank, args=(world, port, cases, device, result_dir, groups), nprocs=world,
+                             join=False, start_method="spawn")
     import time
 
     t0 = time.time()

@@ -33,3 +33,12 @@ def test_ring_processes_on_one_gpu_match_the_oracle(world, tmp_path):
     precompute_refs(world, CASES[world], str(tmp_path))
     ok, errs = launch(world, CASES[world], "cuda", str(tmp_path), timeout=900)
     assert ok, "\n".join(errs)
+
+
+def test_hierarchical_ring_processes_on_one_gpu_match_the_oracle(tmp_path):
+    """The hierarchical ring over 4 ranks in 2 groups of 2 (local ring inside a group, global ring
+    across the groups), through the library's kernels."""
+    cases = [CASES[4][0], CASES[4][2], CASES[4][4]]
+    precompute_refs(4, cases, str(tmp_path))
+    ok, errs = launch(4, cases, "cuda", str(tmp_path), timeout=900, groups=2)
+    assert ok, "\n".join(errs)

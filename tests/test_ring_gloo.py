@@ -21,3 +21,13 @@ def test_ring_on_gloo_ranks_matches_full_attention(world, tmp_path):
     cases = [c for c in CASES if c[3] % (2 * world) == 0]
     ok, errs = launch(world, cases, "cpu", str(tmp_path), timeout=300)
     assert ok, "\n".join(errs)
+
+
+@pytest.mark.parametrize("world,groups", [(4, 2), (6, 2), (6, 3), (3, 1), (3, 3), (8, 4)])
+def test_hierarchical_ring_on_gloo_ranks_matches_full_attention(world, groups, tmp_path):
+    """The hierarchical ring (local ring inside groups of world / groups ranks, global ring across
+    them): same results as the flat ring, every shard met once, accumulators home at the end."""
+    cases = [c for c in CASES if c[3] % (2 * world) == 0] or [(1, 2, 1, 96, 8, True, "zigzag", "float32",
+                                                                 "float32", 15)]
+    ok, errs = launch(world, cases, "cpu", str(tmp_path), timeout=300, groups=groups)
+    assert ok, "\n".join(errs)
