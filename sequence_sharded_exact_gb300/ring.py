@@ -22,8 +22,20 @@ rows [i*S, (i+1)*S) of the whole-sequence buffers of the single-device calls.
 """
 from __future__ import annotations
 
+import contextlib
+
 import torch
 import torch.distributed as dist
+
+
+@contextlib.contextmanager
+def _range(name):
+    """An NVTX range (named step of the ring) for profilers that record them; free otherwise."""
+    torch.cuda.nvtx.range_push(name)
+    try:
+        yield
+    finally:
+        torch.cuda.nvtx.range_pop()
 
 
 class RingComm:
@@ -129,7 +141,8 @@ def ring_fwd(q, k, v, comm, causal=True, layout="zigzag", ops=None):
         # pass the block we hold on and take the next while this one is computed
         nxt = spare[r % 2] if r < n - 1 else None
         h = comm.start(cur, nxt) if nxt is not None else None
-        ops.block_fwd(q, cur[0], cur[1], o_acc, lse_acc, n, i, j, r > 0, causal, layout)
+        with _range(f"ring fwd step {r}: block {j}"):
+            ops.block_fwd(q, cur[0], cur[1], o_acc, lse_acc, n, i, j, r > 0, causal, layout)
         if h is not None:
             comm.wait(h)
             cur = nxt
@@ -169,13 +182,11 @@ def ring_bwd(q, k, v, out, lse, dout, comm, causal=True, layout="zigzag", grad_d
         j = (i - r) % n
         nxt = spare[r % 2] if r < n - 1 else None
         h_kv = comm.start(cur, nxt) if nxt is not None else None
-        if r == 0:
+        with _range(f"ring bwd step {r}: block {j}"):
             # the first contribution to this device's own block starts its accumulator
-            ops.block_bwd(q, cur[0], cur[1], dout, lse, D, dq_acc, acc[0][0], acc[0][1], n, i, j, False, causal,
-                          layout)
-        else:
-            ops.block_bwd(q, cur[0], cur[1], dout, lse, D, dq_acc, part[0], part[1], n, i, j, False, causal,
-                          layout)
+            dst = acc[0] if r == 0 else part
+            ops.block_bwd(q, cur[0], cur[1], dout, lse, D, dq_acc, dst[0], dst[1], n, i, j, False, causal, layout)
+        if r > 0:
             comm.wait(h_acc)  # block j's accumulator from device i - 1, now in acc[slot]
             ops.add(acc[slot][0], part[0])
             ops.add(acc[slot][1], part[1])
@@ -242,7 +253,8 @@ def ring_fwd_2d(q, k, v, grid, causal=True, layout="zigzag", ops=None):
             nxt = local_spare[b % 2] if b < Q - 1 else None
             h_l = (comm.start(cur, nxt, tag=0, dst=grid.rank(grid.p, grid.q + 1), src=grid.rank(grid.p, grid.q - 1))
                    if nxt is not None else None)
-            ops.block_fwd(q, cur[0], cur[1], o_acc, lse_acc, n, i, grid.held(a, b), step > 0, causal, layout)
+            with _range(f"ring fwd step {a}.{b}: block {grid.held(a, b)}"):
+                ops.block_fwd(q, cur[0], cur[1], o_acc, lse_acc, n, i, grid.held(a, b), step > 0, causal, layout)
             step += 1
             if h_l is not None:
                 comm.wait(h_l)
@@ -282,12 +294,10 @@ def ring_bwd_2d(q, k, v, out, lse, dout, grid, causal=True, layout="zigzag", gra
             h_l = (comm.start(cur, nxt, tag=0, dst=grid.rank(grid.p, grid.q + 1), src=grid.rank(grid.p, grid.q - 1))
                    if nxt is not None else None)
             j = grid.held(a, b)
-            if step == 0:
-                ops.block_bwd(q, cur[0], cur[1], dout, lse, D, dq_acc, acc[0][0], acc[0][1], n, i, j, False, causal,
-                              layout)
-            else:
-                ops.block_bwd(q, cur[0], cur[1], dout, lse, D, dq_acc, part[0], part[1], n, i, j, False, causal,
-                              layout)
+            with _range(f"ring bwd step {a}.{b}: block {j}"):
+                dst = acc[0] if step == 0 else part  # the first contribution starts the own block's accumulator
+                ops.block_bwd(q, cur[0], cur[1], dout, lse, D, dq_acc, dst[0], dst[1], n, i, j, False, causal, layout)
+            if step > 0:
                 comm.wait(h_acc)  # block j's accumulator from its previous holder, now in acc[slot]
                 ops.add(acc[slot][0], part[0])
                 ops.add(acc[slot][1], part[1])
