@@ -453,12 +453,14 @@ def main():
                     "with the compute of other kv-head groups")
 
         e2e_steps = max(2, args.steps // 2)
-        e2e_ms = sum(time_launches(e2e_step, e2e_steps, 1, stream)) / e2e_steps
+        with ClockSampler(dev.index) as e2e_clk:
+            e2e_ms = sum(time_launches(e2e_step, e2e_steps, 1, stream)) / e2e_steps
         h2d = sum(t.numel() * t.element_size() for t in h_in)
         d2h = sum(t.numel() * t.element_size() for t in h_out)
         line["e2e"] = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "what": what,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": e2e_ms, "copy_GBps": copy_bandwidth(h_in[0], ins[0], stream)}
+                       "ms_per_step": e2e_ms, "copy_GBps": copy_bandwidth(h_in[0], ins[0], stream),
+                       "clocks": e2e_clk.summary()}
         if not train:
             # the results that came back match the device-resident forward of the timed region
             line["e2e"]["matches_device_forward"] = bool(torch.equal(h_out[0], out.cpu()) and
