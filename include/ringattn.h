@@ -36,8 +36,8 @@
  *     RA_ERR_INVALID_ARG or RA_ERR_UNSUPPORTED and enqueues nothing.  A failed launch returns
  *     RA_ERR_CUDA.  ring_attn_last_error() gives a message for the calling thread's last failure.
  *     Kernels never trap: every wait inside a kernel is bounded, and a wait that runs out sets a
- *     device status word (read it with ring_attn_device_status) and the kernel returns.
- *     Nothing throws across this interface.
+ *     device status word and the kernel returns; ring_attn_device_status reads the word,
+ *     ring_attn_device_check turns it into RA_ERR_TIMEOUT.  Nothing throws across this interface.
  */
 #ifndef RINGATTN_H
 #define RINGATTN_H
