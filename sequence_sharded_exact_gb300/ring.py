@@ -319,3 +319,40 @@ def ring_bwd_2d(q, k, v, out, lse, dout, grid, causal=True, layout="zigzag", gra
         comm.wait(h_acc)  # this rank's own block, with every rank's contribution
     dk_acc, dv_acc = acc[slot]
     return ops.convert(dq_acc, grad_dtype), ops.convert(dk_acc, grad_dtype), ops.convert(dv_acc, grad_dtype)
+
+
+# ------------------------------------------------------------------------------------------------
+# The ring as a differentiable operation on each device
+# ------------------------------------------------------------------------------------------------
+class _DistributedRingAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, comm, groups, causal, layout, ops):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        if groups > 1:
+            grid = RingGrid(comm, groups)
+            out, lse = ring_fwd_2d(q, k, v, grid, causal, layout, ops=ops)
+        else:
+            out, lse = ring_fwd(q, k, v, comm, causal, layout, ops=ops)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.cfg = (comm, groups, causal, layout, ops)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        comm, groups, causal, layout, ops = ctx.cfg
+        dout = dout.contiguous()
+        if groups > 1:
+            grads = ring_bwd_2d(q, k, v, out, lse, dout, RingGrid(comm, groups), causal, layout, q.dtype, ops=ops)
+        else:
+            grads = ring_bwd(q, k, v, out, lse, dout, comm, causal, layout, q.dtype, ops=ops)
+        return grads + (None,) * 5
+
+
+def ring_attention_distributed(q, k, v, comm, causal=True, layout="zigzag", groups=1, ops=None):
+    """Ring attention on this device as a differentiable operation (the pages' RingAttention module,
+    LLM-101-CN section 6.2): q [B,H,S,d], k, v [B,Hkv,S,d] are this rank's shard; the forward runs
+    the ring (hierarchical with groups > 1) and the backward passes the blocks round again, so that
+    every rank receives the gradients of its own shard.  Every rank of the communicator must call it
+    with tensors of the same shapes."""
+    return _DistributedRingAttention.apply(q, k, v, comm, int(groups), causal, layout, ops or LibraryOps())

@@ -285,3 +285,53 @@ def run_failing_rank(rank, world, port, mode, result_dir):
         with open(os.path.join(result_dir, f"rank{rank}.detected"), "w") as f:
             f.write(f"{time.time() - t0:.2f} {type(e).__name__}: {str(e)[:200]}")
     os._exit(0)  # no orderly shutdown: the group has lost a member
+
+
+def run_autograd_rank(rank, world, port, groups, result_dir, device="cpu"):
+    """ring_attention_distributed under autograd: the output and the gradients that backward() leaves
+    on this rank's q, k, v equal its shard of the oracle's whole sequence.  CPU ranks use the oracle's
+    block ops (float64, 1e-10); GPU ranks (sharing cuda:0) the library's kernels (bf16 inputs and
+    gradients: the bf16 bounds, stored-bf16 for the gradients)."""
+    os.environ.setdefault("GLOO_SOCKET_IFNAME", "lo")
+    try:
+        dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+        import oracle
+        from sequence_sharded_exact_gb300 import ring, synth
+
+        comm = ring.RingComm()
+        cpu = device == "cpu"
+        B, H, Hkv, L, d = (1, 2, 1, 48, 8) if cpu else (1, 4, 2, 2048, 128)
+        dt = torch.float32 if cpu else torch.bfloat16
+        x = synth.make_inputs(B, H, Hkv, L, d, dtype=dt, seed=77, with_dout=True)
+        ref_o, _ = oracle.attn_fwd(x["q"], x["k"], x["v"], world, True, "zigzag")
+        rq, rk, rv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], world, True, "zigzag")
+        S = L // world
+        sl = slice(rank * S, (rank + 1) * S)
+        if cpu:
+            q, k, v = (shard(x[t], rank, world).double().requires_grad_(True) for t in ("q", "k", "v"))
+            do, ops = shard(x["dout"], rank, world).double(), OracleOps(L)
+        else:
+            torch.cuda.set_device(0)
+            q, k, v = (shard(x[t], rank, world).cuda().requires_grad_(True) for t in ("q", "k", "v"))
+            do, ops = shard(x["dout"], rank, world).cuda(), None
+        out = ring.ring_attention_distributed(q, k, v, comm, True, "zigzag", groups=groups, ops=ops)
+        (out.float() * do.float()).sum().backward()
+        for got, ref, name in ((out.detach(), ref_o[:, :, sl], "out"), (q.grad, rq[:, :, sl], "dq"),
+                               (k.grad, rk[:, :, sl], "dk"), (v.grad, rv[:, :, sl], "dv")):
+            g = got.double().cpu().numpy()
+            if cpu:
+                err = float(np.abs(g - ref).max())
+                assert err < 1e-10, f"rank {rank} {name}: {err:.3e}"
+            else:
+                assert got.dtype == torch.bfloat16
+                excess = float((np.abs(g - ref) - (2e-2 + np.abs(ref) * 2.0 ** -8)).max())
+                ma, rl = errors(g, ref)
+                assert excess <= 0 and rl <= 5e-3, f"rank {rank} {name}: max-abs {ma:.3e}, rel-L2 {rl:.3e}"
+        dist.barrier()
+        open(os.path.join(result_dir, f"rank{rank}.ok"), "w").close()
+    except Exception:
+        with open(os.path.join(result_dir, f"rank{rank}.err"), "w") as f:
+            f.write(traceback.format_exc())
+    finally:
+        if dist.is_initialized():
+            dist.destroy_process_group()

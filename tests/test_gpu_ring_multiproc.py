@@ -42,3 +42,18 @@ def test_hierarchical_ring_processes_on_one_gpu_match_the_oracle(tmp_path):
     precompute_refs(4, cases, str(tmp_path))
     ok, errs = launch(4, cases, "cuda", str(tmp_path), timeout=900, groups=2)
     assert ok, "\n".join(errs)
+
+
+@pytest.mark.parametrize("groups", [1, 2])
+def test_distributed_ring_attention_autograd_on_one_gpu(groups, tmp_path):
+    """ring_attention_distributed with the library's kernels: 4 ranks (flat, or 2 groups of 2) share
+    cuda:0; forward and autograd gradients (bf16) of every rank against the oracle."""
+    import os
+    import torch.multiprocessing as mp
+
+    from ring_ranks import free_port, run_autograd_rank
+
+    mp.start_processes(run_autograd_rank, args=(4, free_port(), groups, str(tmp_path), "cuda"), nprocs=4,
+                       join=True, start_method="spawn")
+    errs = [open(tmp_path / f"rank{r}.err").read() for r in range(4) if os.path.exists(tmp_path / f"rank{r}.err")]
+    assert not errs, "\n".join(errs)

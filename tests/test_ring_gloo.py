@@ -31,3 +31,19 @@ def test_hierarchical_ring_on_gloo_ranks_matches_full_attention(world, groups, t
                                                                  "float32", 15)]
     ok, errs = launch(world, cases, "cpu", str(tmp_path), timeout=300, groups=groups)
     assert ok, "\n".join(errs)
+
+
+@pytest.mark.parametrize("world,groups", [(2, 1), (4, 2)])
+def test_distributed_ring_attention_under_autograd(world, groups, tmp_path):
+    """ring_attention_distributed: the forward and the gradients autograd produces on every rank are
+    that rank's shard of the whole-sequence oracle (flat and hierarchical ring)."""
+    import os
+    import torch.multiprocessing as mp
+
+    from ring_ranks import free_port, run_autograd_rank
+
+    mp.start_processes(run_autograd_rank, args=(world, free_port(), groups, str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    errs = [open(tmp_path / f"rank{r}.err").read() for r in range(world) if os.path.exists(tmp_path / f"rank{r}.err")]
+    assert not errs, "\n".join(errs)
+    assert all(os.path.exists(tmp_path / f"rank{r}.ok") for r in range(world))
