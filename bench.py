@@ -82,6 +82,16 @@ def max_over_ranks(value, dist_mod=None, device="cpu"):
     return float(t.item())
 
 
+def visible_tile_flops(B, H, L, d, n, causal, layout, tile=128):
+    """Forward flops of every (query tile, key tile) pair with at least one visible (q, k) element at
+    the kernels' 128-row tiles, each counted whole (diagonal tiles in full): what the tensor cores
+    execute at the least.  The algorithmic count (fwd_flops) halves the diagonal tiles instead."""
+    import sequence_sharded_exact_gb300 as ra
+
+    tiles = sum(ra.shard_tiles(L, n, causal, layout, tile))
+    return 4.0 * B * H * tiles * tile * tile * d
+
+
 def whole_job_tflops(world, flops_per_step, steps, max_total_ms):
     """All ranks' algorithmic work over the slowest rank's time, in TFLOP/s."""
     return world * flops_per_step * steps / (max_total_ms / 1e3) / 1e12
@@ -416,7 +426,9 @@ def main():
                      "traffic": TRAFFIC_BYTES.get((args.workload, args.step)),
                      "peak_kind": f"{peak_kind} bf16 burst (MEASURED_PEAKS bf16_tflops)",
                      "frac_of_sustained": achieved / peak_s,
-                     "kernel": kname, "timed": note, "algorithmic_flops_per_launch": kflops},
+                     "kernel": kname, "timed": note, "algorithmic_flops_per_launch": kflops,
+                     "visible_tile_flops_per_launch": (2.5 if train else 1.0) * visible_tile_flops(
+                         B, H, L, d, n, w["causal"], w["layout"])},
         "gpu_launches": args.steps * (4 if train else 1),
         "path": path,
         "device_status": status,

@@ -39,4 +39,4 @@ from .binding import (  # noqa: F401
     ulysses_fwd,
 )
 from .autograd import ring_attention  # noqa: F401
-from .ring import ring_attention_distributed  # noqa: F401
+from .ring import RingAttention, ring_attention_distributed  # noqa: F401

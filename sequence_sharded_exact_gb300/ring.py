@@ -356,3 +356,36 @@ def ring_attention_distributed(q, k, v, comm, causal=True, layout="zigzag", grou
     every rank receives the gradients of its own shard.  Every rank of the communicator must call it
     with tensors of the same shapes."""
     return _DistributedRingAttention.apply(q, k, v, comm, int(groups), causal, layout, ops or LibraryOps())
+
+
+class RingAttention(torch.nn.Module):
+    """The pages' per-rank object (LLM-101-CN section 6.2): built from the model width ``dim``, the
+    number of query heads, this rank and the world size; ``forward(Q, K, V)`` takes this rank's
+    shard, Q [bs, heads, S, dim // heads] and K, V [bs, kv_heads, S, dim // heads], and returns this
+    rank's rows of the output.  The scores are scaled by 1/sqrt(dim // heads), as on the page.
+
+    Differences from the page's listing: the running maximum starts at minus infinity instead of
+    -1e4 (so that no score is ever clipped), the transfers of the next block overlap the current
+    block's work, K/V may have fewer heads than Q (grouped-query attention), and ``causal``,
+    ``layout`` and ``groups`` select the causal mask, the shard layout and the hierarchical ring.
+    The defaults are the page's: no mask, contiguous shards, one flat ring.  The output is
+    differentiable; the backward passes the blocks round the ring again."""
+
+    def __init__(self, dim, heads, rank=None, world_size=None, causal=False, layout="contiguous",
+                 groups=1, group=None, ops=None):
+        super().__init__()
+        if heads <= 0 or dim % heads:
+            raise ValueError(f"dim {dim} is not a multiple of heads {heads}")
+        self.dim, self.heads, self.head_dim = dim, heads, dim // heads
+        self.comm = RingComm(group)
+        if rank is not None and rank != self.comm.rank:
+            raise ValueError(f"rank {rank} is not this process's rank {self.comm.rank} in the group")
+        if world_size is not None and world_size != self.comm.world:
+            raise ValueError(f"world_size {world_size} is not the group's size {self.comm.world}")
+        self.rank, self.world_size = self.comm.rank, self.comm.world
+        self.causal, self.layout, self.groups, self.ops = causal, layout, int(groups), ops
+
+    def forward(self, Q, K, V):
+        if Q.dim() != 4 or Q.shape[1] != self.heads or Q.shape[-1] != self.head_dim:
+            raise ValueError(f"Q of shape {tuple(Q.shape)} is not [bs, {self.heads}, S, {self.head_dim}]")
+        return ring_attention_distributed(Q, K, V, self.comm, self.causal, self.layout, self.groups, self.ops)

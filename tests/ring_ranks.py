@@ -287,11 +287,13 @@ def run_failing_rank(rank, world, port, mode, result_dir):
     os._exit(0)  # no orderly shutdown: the group has lost a member
 
 
-def run_autograd_rank(rank, world, port, groups, result_dir, device="cpu"):
+def run_autograd_rank(rank, world, port, groups, result_dir, device="cpu", causal=True, layout="zigzag",
+                      module=False):
     """ring_attention_distributed under autograd: the output and the gradients that backward() leaves
     on this rank's q, k, v equal its shard of the oracle's whole sequence.  CPU ranks use the oracle's
     block ops (float64, 1e-10); GPU ranks (sharing cuda:0) the library's kernels (bf16 inputs and
-    gradients: the bf16 bounds, stored-bf16 for the gradients)."""
+    gradients: the bf16 bounds, stored-bf16 for the gradients).  With ``module`` the call goes
+    through the pages' per-rank object, RingAttention(dim, heads, rank, world_size)."""
     os.environ.setdefault("GLOO_SOCKET_IFNAME", "lo")
     try:
         dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
@@ -303,8 +305,8 @@ def run_autograd_rank(rank, world, port, groups, result_dir, device="cpu"):
         B, H, Hkv, L, d = (1, 2, 1, 48, 8) if cpu else (1, 4, 2, 2048, 128)
         dt = torch.float32 if cpu else torch.bfloat16
         x = synth.make_inputs(B, H, Hkv, L, d, dtype=dt, seed=77, with_dout=True)
-        ref_o, _ = oracle.attn_fwd(x["q"], x["k"], x["v"], world, True, "zigzag")
-        rq, rk, rv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], world, True, "zigzag")
+        ref_o, _ = oracle.attn_fwd(x["q"], x["k"], x["v"], world, causal, layout)
+        rq, rk, rv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], world, causal, layout)
         S = L // world
         sl = slice(rank * S, (rank + 1) * S)
         if cpu:
@@ -314,7 +316,22 @@ def run_autograd_rank(rank, world, port, groups, result_dir, device="cpu"):
             torch.cuda.set_device(0)
             q, k, v = (shard(x[t], rank, world).cuda().requires_grad_(True) for t in ("q", "k", "v"))
             do, ops = shard(x["dout"], rank, world).cuda(), None
-        out = ring.ring_attention_distributed(q, k, v, comm, True, "zigzag", groups=groups, ops=ops)
+        if module:
+            att = ring.RingAttention(H * d, H, rank, world, causal=causal, layout=layout, groups=groups, ops=ops)
+            out = att(q, k, v)
+            for bad in (dict(rank=(rank + 1) % world, world_size=world), dict(rank=rank, world_size=world + 1)):
+                try:
+                    ring.RingAttention(H * d, H, **bad)
+                    raise AssertionError(f"RingAttention accepted {bad}")
+                except ValueError:
+                    pass
+            try:
+                ring.RingAttention(H * d // 2, H, rank, world)(q, k, v)   # head dim half of q's
+                raise AssertionError("RingAttention accepted q with the wrong head dim")
+            except ValueError:
+                pass
+        else:
+            out = ring.ring_attention_distributed(q, k, v, comm, causal, layout, groups=groups, ops=ops)
         (out.float() * do.float()).sum().backward()
         for got, ref, name in ((out.detach(), ref_o[:, :, sl], "out"), (q.grad, rq[:, :, sl], "dq"),
                                (k.grad, rk[:, :, sl], "dk"), (v.grad, rv[:, :, sl], "dv")):

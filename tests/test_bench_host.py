@@ -66,3 +66,17 @@ def test_peak_fractions_published_and_per_clock():
     assert "sparsity" in roof["published_peak_source"]
     if not __import__("torch").cuda.is_available():
         assert bench.per_clock_peak_tflops(2000.0) is None
+
+
+def test_visible_tile_flops_exceed_the_algorithmic_count_by_the_diagonal_halves():
+    """Zigzag at 131072 / 8 shards: 65600 tile pairs per shard and head (closed form
+    (2n-1)c^2 + c(c+1), c = 64), of which 2n*c = 1024 per head are diagonal tiles, counted whole
+    here and as halves in the algorithmic count."""
+    vis = bench.visible_tile_flops(1, 32, 131072, 128, 8, True, "zigzag")
+    assert vis == 4.0 * 32 * 8 * 65600 * 128 * 128 * 128
+    alg = bench.fwd_flops(1, 32, 131072, 128, True)
+    # the algorithmic count 4 B H L^2 d / 2 is the off-diagonal tiles plus half of each diagonal one
+    half_diag = 4.0 * 32 * 1024 * 128 * 128 * 128 / 2
+    assert vis - alg == pytest.approx(half_diag, rel=1e-12)
+    # non-causal: every tile is visible and the two counts agree
+    assert bench.visible_tile_flops(2, 8, 8192, 128, 8, False, "contiguous") == bench.fwd_flops(2, 8, 8192, 128, False)

@@ -57,3 +57,18 @@ def test_distributed_ring_attention_autograd_on_one_gpu(groups, tmp_path):
                        join=True, start_method="spawn")
     errs = [open(tmp_path / f"rank{r}.err").read() for r in range(4) if os.path.exists(tmp_path / f"rank{r}.err")]
     assert not errs, "\n".join(errs)
+
+
+def test_pages_ring_attention_object_on_one_gpu(tmp_path):
+    """RingAttention(dim, heads, rank, world_size) with its defaults (no mask, contiguous shards) on
+    the library's kernels: 2 ranks share cuda:0; forward and gradients against the oracle."""
+    import os
+    import torch.multiprocessing as mp
+
+    from ring_ranks import free_port, run_autograd_rank
+
+    mp.start_processes(run_autograd_rank, args=(2, free_port(), 1, str(tmp_path), "cuda", False, "contiguous", True),
+                       nprocs=2, join=True, start_method="spawn")
+    errs = [open(tmp_path / f"rank{r}.err").read() for r in range(2) if os.path.exists(tmp_path / f"rank{r}.err")]
+    assert not errs, "\n".join(errs)
+    assert all(os.path.exists(tmp_path / f"rank{r}.ok") for r in range(2))

@@ -47,3 +47,21 @@ def test_distributed_ring_attention_under_autograd(world, groups, tmp_path):
     errs = [open(tmp_path / f"rank{r}.err").read() for r in range(world) if os.path.exists(tmp_path / f"rank{r}.err")]
     assert not errs, "\n".join(errs)
     assert all(os.path.exists(tmp_path / f"rank{r}.ok") for r in range(world))
+
+
+@pytest.mark.parametrize("world,groups,causal,layout", [(3, 1, False, "contiguous"), (4, 2, True, "striped")])
+def test_pages_ring_attention_object(world, groups, causal, layout, tmp_path):
+    """RingAttention(dim, heads, rank, world_size), the pages' per-rank object (no mask and contiguous
+    shards by default): forward and autograd gradients on every rank equal its shard of the oracle;
+    a rank or world size that disagrees with the process group, and a q whose head dim is not
+    dim // heads, are refused."""
+    import os
+    import torch.multiprocessing as mp
+
+    from ring_ranks import free_port, run_autograd_rank
+
+    mp.start_processes(run_autograd_rank, args=(world, free_port(), groups, str(tmp_path), "cpu", causal, layout, True),
+                       nprocs=world, join=True, start_method="spawn")
+    errs = [open(tmp_path / f"rank{r}.err").read() for r in range(world) if os.path.exists(tmp_path / f"rank{r}.err")]
+    assert not errs, "\n".join(errs)
+    assert all(os.path.exists(tmp_path / f"rank{r}.ok") for r in range(world))
