@@ -308,6 +308,9 @@ def main():
                     help="run the multi-device ring path also at N = 1 (the default for N > 1)")
     ap.add_argument("--replicas", action="store_true",
                     help="N > 1: one independent copy of the workload per rank instead of the ring")
+    ap.add_argument("--dist-backend", default="nccl", choices=["nccl", "gloo"],
+                    help="N > 1 ring: the process group's backend (gloo stages the blocks through host "
+                         "memory; with fewer GPUs than ranks, ranks share devices round robin)")
     ap.add_argument("--ring-groups", type=int, default=1,
                     help="the ring as a hierarchical ring: a local ring inside each of this many groups "
                          "of consecutive ranks (e.g. the GPUs of one node), a global ring across them")
@@ -553,10 +556,12 @@ def run_ring(args, w, world, rank, local):
     import sequence_sharded_exact_gb300 as ra
     from sequence_sharded_exact_gb300 import ring, synth
 
-    torch.cuda.set_device(local if world > 1 else 0)
+    torch.cuda.set_device(local % torch.cuda.device_count() if world > 1 else 0)
     dev = torch.device("cuda", torch.cuda.current_device())
-    if world > 1:
+    if world > 1 and args.dist_backend == "nccl":
         dist.init_process_group("nccl", device_id=dev)
+    elif world > 1:
+        dist.init_process_group("gloo")
     else:
         dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % free_port(), rank=0, world_size=1)
     comm = ring.RingComm()
@@ -623,7 +628,13 @@ def run_ring(args, w, world, rank, local):
                        parallelism=f"context parallel: ring over {world} device(s), one shard of {S} tokens each"
                                    + (f", hierarchical: {args.ring_groups} groups of {world // args.ring_groups}"
                                       if grid is not None else ""),
-                       mode="multi-device ring (blocks over NCCL)" if world > 1 else "ring path on one device"),
+                       l2=f"each rank's shard of q, k, v ({(H + 2 * Hkv) * B * S * d * 2 / 1e9:.2f} GB) "
+                          + ("larger than L2; no flush" if (H + 2 * Hkv) * B * S * d * 2 > 129e6
+                             else "smaller than L2 (129 MB): repeated steps may hit in L2"),
+                       mode=(f"multi-device ring (blocks over {args.dist_backend.upper()}"
+                             + (f", {world} ranks on {torch.cuda.device_count()} GPU(s)"
+                                if world > torch.cuda.device_count() else "") + ")")
+                       if world > 1 else "ring path on one device"),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_b, "unit": "TFLOP/s",
                      "frac": achieved / peak_b, "traffic": None,
                      "peak_kind": f"{peak_kind} bf16 burst (MEASURED_PEAKS bf16_tflops)",

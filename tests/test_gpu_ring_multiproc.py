@@ -72,3 +72,37 @@ def test_pages_ring_attention_object_on_one_gpu(tmp_path):
     errs = [open(tmp_path / f"rank{r}.err").read() for r in range(2) if os.path.exists(tmp_path / f"rank{r}.err")]
     assert not errs, "\n".join(errs)
     assert all(os.path.exists(tmp_path / f"rank{r}.ok") for r in range(2))
+
+
+@pytest.mark.parametrize("step", ["fwd", "train"])
+def test_bench_ring_mode_with_two_ranks(step):
+    """bench.py's multi-rank ring mode, as a launcher runs it for N > 1 (here 2 gloo ranks sharing
+    cuda:0 instead of NCCL across 2 GPUs): one JSON line from rank 0 with the whole sequence's
+    TFLOP/s, a clean status word, the roofline of the block launches and the end-to-end leg."""
+    import json
+    import pathlib
+    import subprocess
+    import sys
+
+    from ring_ranks import free_port
+
+    root = pathlib.Path(__file__).resolve().parents[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), "bench.py", "--gpus", "2",
+           "--steps", "2", "--warmup", "3", "--workload", "zigzag_gqa_32k", "--step", step,
+           "--dist-backend", "gloo"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = lines[0]
+    assert line["n_gpus"] == 2 and line["steps"] == 2 and line["scaling"] == "strong"
+    assert line["device_status"] == 0 and line["value"] > 0 and line["ms_per_step"] > 0
+    assert line["config"]["n_shards"] == 2 and "GLOO" in line["config"]["mode"]
+    assert 0 < line["roofline"]["frac"] < 1.5
+    # each rank copies in its shard of q, k, v (and dO) and copies out its out and lse
+    L, H, Hkv, d = 32768, 32, 8, 128
+    h2d = 2 * L * d * (2 * H + 2 * Hkv) + (2 * L * d * H if step == "train" else 0)
+    assert line["e2e"]["h2d_bytes_per_step"] == h2d
+    assert line["e2e"]["d2h_bytes_per_step"] == 2 * L * d * H + 4 * L * H
+    assert line["e2e"]["value"] > 0
