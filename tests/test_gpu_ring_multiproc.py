@@ -100,9 +100,10 @@ def test_bench_ring_mode_with_two_ranks(step):
     assert line["device_status"] == 0 and line["value"] > 0 and line["ms_per_step"] > 0
     assert line["config"]["n_shards"] == 2 and "GLOO" in line["config"]["mode"]
     assert 0 < line["roofline"]["frac"] < 1.5
-    # each rank copies in its shard of q, k, v (and dO) and copies out its out and lse
+    # the two ranks together copy in every row of q, k, v (and dO), bf16, and copy out every row of
+    # out (bf16) and lse (float32)
     L, H, Hkv, d = 32768, 32, 8, 128
-    h2d = 2 * L * d * (2 * H + 2 * Hkv) + (2 * L * d * H if step == "train" else 0)
+    h2d = 2 * L * d * (H + 2 * Hkv) + (2 * L * d * H if step == "train" else 0)
     assert line["e2e"]["h2d_bytes_per_step"] == h2d
     assert line["e2e"]["d2h_bytes_per_step"] == 2 * L * d * H + 4 * L * H
     assert line["e2e"]["value"] > 0
