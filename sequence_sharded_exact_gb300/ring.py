@@ -60,6 +60,19 @@ class RingComm:
         """Global rank of rank r of this communicator's group."""
         return dist.get_global_rank(self.group, r) if self.group is not None else r
 
+    def twin(self):
+        """A second communicator over the same ranks, with the same rank numbering, created on first
+        use (a collective call: every rank must reach it in the same order) and kept.  NCCL runs all
+        point-to-point transfers of one communicator on one stream, one after the other; transfers
+        on the twin run beside them, so a slow transfer on one does not hold back the other's.  Falls
+        back to this communicator if the new group would number the ranks differently."""
+        if getattr(self, "_twin", None) is None:
+            ranks = [self.global_rank(r) for r in range(self.world)]
+            group = dist.new_group(ranks=ranks, backend=self.backend)
+            same = all(dist.get_group_rank(group, g) == r for r, g in enumerate(ranks))
+            self._twin = RingComm(group) if same else self
+        return self._twin
+
     def start(self, send, recv, tag=0, dst=None, src=None):
         """Starts sending the tensors `send` to rank dst (default rank + 1) and receiving into `recv`
         (same shapes and dtypes) from rank src (default rank - 1), ranks of this group, with message
@@ -210,12 +223,15 @@ class RingGrid:
     r = p * Q + q is member q of group p.  The local ring runs inside a group (fast links, e.g. the
     devices of one node), the global ring across the groups at the same member index (the slow links
     between nodes): the hierarchical ring the pages suggest for very long contexts (agentalpha "Ring
-    Attention vs tensor parallelism", follow-up 2).  Rank r still holds shard r."""
+    Attention vs tensor parallelism", follow-up 2).  Rank r still holds shard r.  Transfers between
+    groups go over `gcomm`, the communicator's twin, so that they overlap the local ring's transfers
+    instead of queueing with them."""
 
     def __init__(self, comm, groups):
         if groups < 1 or comm.world % groups:
             raise ValueError(f"{groups} groups do not divide {comm.world} ranks")
         self.comm = comm
+        self.gcomm = comm.twin() if groups > 1 else comm
         self.P = groups
         self.Q = comm.world // groups
         self.p, self.q = divmod(comm.rank, self.Q)
@@ -246,8 +262,8 @@ def ring_fwd_2d(q, k, v, grid, causal=True, layout="zigzag", ops=None):
     step = 0
     for a in range(P):
         # this global step's block goes on to the next group while it circulates in this one
-        h_g = (comm.start(origin, global_spare[a % 2], tag=4, dst=grid.rank(grid.p + 1, grid.q),
-                          src=grid.rank(grid.p - 1, grid.q)) if a < P - 1 else None)
+        h_g = (grid.gcomm.start(origin, global_spare[a % 2], tag=4, dst=grid.rank(grid.p + 1, grid.q),
+                                src=grid.rank(grid.p - 1, grid.q)) if a < P - 1 else None)
         cur = origin
         for b in range(Q):
             nxt = local_spare[b % 2] if b < Q - 1 else None
@@ -286,8 +302,8 @@ def ring_bwd_2d(q, k, v, out, lse, dout, grid, causal=True, layout="zigzag", gra
     origin = (k, v)
     h_acc, slot, step = None, 0, 0
     for a in range(P):
-        h_g = (comm.start(origin, global_spare[a % 2], tag=4, dst=grid.rank(grid.p + 1, grid.q),
-                          src=grid.rank(grid.p - 1, grid.q)) if a < P - 1 else None)
+        h_g = (grid.gcomm.start(origin, global_spare[a % 2], tag=4, dst=grid.rank(grid.p + 1, grid.q),
+                                src=grid.rank(grid.p - 1, grid.q)) if a < P - 1 else None)
         cur = origin
         for b in range(Q):
             nxt = local_spare[b % 2] if b < Q - 1 else None
@@ -303,10 +319,10 @@ def ring_bwd_2d(q, k, v, out, lse, dout, grid, causal=True, layout="zigzag", gra
                 ops.add(acc[slot][1], part[1])
             if n > 1:
                 if b < Q - 1:  # the next holder: the next member of this group
-                    dst, src = grid.rank(grid.p, grid.q + 1), grid.rank(grid.p, grid.q - 1)
-                else:  # after a local round: the next member of the next group
-                    dst, src = grid.rank(grid.p + 1, grid.q + 1), grid.rank(grid.p - 1, grid.q - 1)
-                h_acc = comm.start(acc[slot], acc[1 - slot], tag=2, dst=dst, src=src)
+                    via, dst, src = comm, grid.rank(grid.p, grid.q + 1), grid.rank(grid.p, grid.q - 1)
+                else:  # after a local round: the next member of the next group (between groups)
+                    via, dst, src = grid.gcomm, grid.rank(grid.p + 1, grid.q + 1), grid.rank(grid.p - 1, grid.q - 1)
+                h_acc = via.start(acc[slot], acc[1 - slot], tag=2, dst=dst, src=src)
                 slot = 1 - slot
             step += 1
             if h_l is not None:
