@@ -727,7 +727,7 @@ def other_workload(ra, name, stream, dev, peak_b):
 
 def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
     """Training workload (fwd + bwd), stepwise ring (steps folded into a running result), and the
-    LSE merge bandwidth."""
+    bandwidth of the HBM-bound kernels (LSE merge, backward preprocess, RoPE, Ulysses all-to-all)."""
     from sequence_sharded_exact_gb300 import synth
 
     res = {}
@@ -754,6 +754,14 @@ def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
     res["lse_merge"] = {"GB/s": gbytes / (statistics.mean(ms) / 1e3), "peak_GB/s": hbm,
                         "frac": gbytes / (statistics.mean(ms) / 1e3) / hbm, "ms": statistics.mean(ms)}
     del ws, out2, lse2, part, la, lb, o_acc
+    # backward preprocess D = rowsum(dO * O) alone, on the workload's out with q standing in for dO
+    # (same shape and dtype); bytes = rows * (2 * d * 2 + 4) (read O and dO in bf16, write D)
+    Dv = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    ms = time_launches(lambda: ra.bwd_preprocess(out, x["q"], D=Dv, stream=stream), 10, 3, stream)
+    gbytes = rows * (2 * d * out.element_size() + 4) / 1e9
+    res["bwd_preprocess"] = {"GB/s": gbytes / (statistics.mean(ms) / 1e3), "peak_GB/s": hbm,
+                             "frac": gbytes / (statistics.mean(ms) / 1e3) / hbm, "ms": statistics.mean(ms)}
+    del Dv
     # rotary positions on a copy of the workload's q, in place; bytes = read + write of q per launch
     qr = x["q"].clone()
     qb = qr.numel() * qr.element_size()

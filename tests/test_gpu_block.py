@@ -113,3 +113,22 @@ def test_block_bwd_every_pair_both_modes(B, H, Hkv, L, d, n, causal, layout, dty
         assert_close(to_np(dq_acc), rq[:, :, sl], dtype, f"shard {i} dq (all blocks)")
     assert_close(to_np(torch.cat(dk_acc, dim=2)), rk, dtype, "dk (all blocks)")
     assert_close(to_np(torch.cat(dv_acc, dim=2)), rv, dtype, "dv (all blocks)")
+
+
+@pytest.mark.parametrize("rows,d,dtype", [(1, 128, torch.bfloat16), (13, 128, torch.bfloat16),
+                                          (1000, 64, torch.bfloat16), (4099, 128, torch.bfloat16),
+                                          (37, 96, torch.bfloat16), (50, 128, torch.float32)])
+def test_bwd_preprocess_row_sums(rows, d, dtype):
+    """D = rowsum(out * dout) for row counts that fill no whole group of rows (the bf16 kernel for head
+    dims 64 and 128 works on 8 or 16 rows per warp) and for the general path, against float64 sums
+    of the same rounded inputs; rows past the end are not written."""
+    g = torch.Generator().manual_seed(rows * 1000 + d)
+    o = torch.randn(rows, d, generator=g).to(dtype)
+    do = torch.randn(rows, d, generator=g).to(dtype)
+    D = torch.full((rows + 64,), float("nan"), device=DEV)
+    ra.bwd_preprocess(o.to(DEV), do.to(DEV), D=D[:rows])
+    torch.cuda.synchronize()
+    ref = (o.double() * do.double()).sum(-1).numpy()
+    got = D[:rows].double().cpu().numpy()
+    assert np.allclose(got, ref, rtol=1e-5, atol=1e-5 * np.sqrt(d))
+    assert torch.isnan(D[rows:]).all()
