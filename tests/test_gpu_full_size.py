@@ -21,7 +21,7 @@ import torch
 import oracle
 import sequence_sharded_exact_gb300 as ra
 from sequence_sharded_exact_gb300 import synth
-from parity_util import BF16_MAX_ABS, BF16_REL_L2, errors, to_np
+from parity_util import BF16_MAX_ABS, BF16_REL_L2, assert_close, errors, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -266,3 +266,37 @@ def test_forward_at_262144_tokens_sampled_rows():
     idx = torch.from_numpy(rows).to(DEV)
     for got, ref, what in ((to_np(out.view(-1, d)[idx]), ref_o, "out"), (to_np(lse.view(-1)[idx]), ref_l, "lse")):
         check_sampled(got, ref, uniform, what)
+
+
+def test_million_tokens_forward_dq_and_rope_sampled_rows():
+    """A million tokens (L = 2^20) over 32 zigzag shards, 8 query heads on 2 kv heads: the pages'
+    long-context case for one device's worth of compute.  Sampled rows of the forward (out, lse) and
+    of dQ, with the first, second and last rows of every chunk of the first and last head, against
+    the oracle; RoPE of one head in place against the oracle's rotation of every row (positions up
+    to 2^20 - 1).  Flat indices pass 2^32 elements here (dQ: 2^30 floats per tensor with 8 heads)."""
+    B, H, Hkv, L, d, n = 1, 8, 2, 1 << 20, 128, 32
+    x = synth.make_inputs(B, H, Hkv, L, d, dtype=torch.bfloat16, seed=1 << 20, with_dout=True,
+                          device=DEV, gen_device=DEV)
+    assert ra.fwd_path(B, H, Hkv, L, d, n, True, "zigzag", torch.bfloat16) == "tcgen05"
+    assert ra.bwd_path(B, H, Hkv, L, d, n, True, "zigzag", torch.bfloat16) == "tcgen05"
+    out, lse = ra.fwd(x["q"], x["k"], x["v"], n, True, "zigzag")
+    dq, dk, dv = ra.bwd(x["q"], x["k"], x["v"], out, lse, x["dout"], n, True, "zigzag")
+    torch.cuda.synchronize()
+    for t in (out, lse, dq, dk, dv):
+        assert torch.isfinite(t).all().item()
+    w = dict(B=B, H=H, L=L, n=n, layout="zigzag")
+    rows, uniform = sampled_rows(w, 96, seed=20, split=True)
+    host = {t: x[t].cpu() for t in ("q", "k", "v", "dout")}
+    ref_o, ref_l = oracle.attn_fwd_rows(host["q"], host["k"], host["v"], n, True, "zigzag", rows)
+    ref_dq = oracle.attn_bwd_dq_rows(host["q"], host["k"], host["v"], host["dout"], n, True, "zigzag", rows)
+    idx = torch.from_numpy(rows).to(DEV)
+    for got, ref, what in ((out.view(-1, d)[idx], ref_o, "out"), (lse.view(-1)[idx], ref_l, "lse"),
+                           (dq.view(-1, d)[idx], ref_dq, "dq")):
+        check_sampled(to_np(got), ref, uniform, what)
+    del out, lse, dq, dk, dv
+    # RoPE of the last kv head's keys, every row
+    kh = x["k"][:, Hkv - 1:].contiguous()
+    ref_r = oracle.rope(kh.cpu(), n, "zigzag")
+    ra.rope(kh, n, "zigzag")
+    torch.cuda.synchronize()
+    assert_close(to_np(kh), ref_r, torch.bfloat16, "rope of 2^20 rows", stored_bf16=True)
