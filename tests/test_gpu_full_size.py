@@ -273,7 +273,7 @@ def test_million_tokens_forward_dq_and_rope_sampled_rows():
     long-context case for one device's worth of compute.  Sampled rows of the forward (out, lse) and
     of dQ, with the first, second and last rows of every chunk of the first and last head, against
     the oracle; RoPE of one head in place against the oracle's rotation of every row (positions up
-    to 2^20 - 1).  Flat indices pass 2^32 elements here (dQ: 2^30 floats per tensor with 8 heads)."""
+    to 2^20 - 1).  The float32 dQ tensor holds 2^30 elements (4 GiB): byte offsets pass 2^32."""
     B, H, Hkv, L, d, n = 1, 8, 2, 1 << 20, 128, 32
     x = synth.make_inputs(B, H, Hkv, L, d, dtype=torch.bfloat16, seed=1 << 20, with_dout=True,
                           device=DEV, gen_device=DEV)
