@@ -107,3 +107,21 @@ def test_bench_ring_mode_with_two_ranks(step):
     assert line["e2e"]["h2d_bytes_per_step"] == h2d
     assert line["e2e"]["d2h_bytes_per_step"] == 2 * L * d * H + 4 * L * H
     assert line["e2e"]["value"] > 0
+
+
+def test_eight_ranks_at_16k_flat_and_hierarchical(tmp_path):
+    """Eight ranks (processes sharing cuda:0) on a 16384-token zigzag sequence, 8 query heads on 2 kv
+    heads: the flat ring, then the hierarchical ring in 2 groups of 4; every rank's shard of out,
+    lse, dq, dk and dv against the float64 oracle of the whole sequence (computed once)."""
+    import os
+
+    case = (1, 8, 2, 16384, 128, True, "zigzag", "bfloat16", "float32", 212)
+    precompute_refs(8, [case], str(tmp_path))
+    for groups in (None, 2):
+        for r in range(8):
+            for suffix in ("ok", "err"):
+                f = tmp_path / f"rank{r}.{suffix}"
+                if os.path.exists(f):
+                    os.remove(f)
+        ok, errs = launch(8, [case], "cuda", str(tmp_path), timeout=900, groups=groups)
+        assert ok, f"groups={groups}:\n" + "\n".join(errs)
