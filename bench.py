@@ -287,7 +287,7 @@ def config_dict(w, step="fwd"):
                         f"L{w['L']} n{w['n']} {'causal' if w['causal'] else 'full'} {w['layout']}",
             "B": w["B"], "H": w["H"], "Hkv": w["Hkv"], "L": w["L"], "d": w["d"], "n_shards": w["n"],
             "causal": w["causal"], "layout": w["layout"], "tile": 128,
-            "key_rows_x8": w["spike_frac"],
+            "key_rows_x8": w["spike_frac"], "seed": w["seed"],
             "l2": f"inputs ({(w['H'] + 2 * w['Hkv']) * w['B'] * w['L'] * w['d'] * 2 / 1e9:.2f} GB) "
                   "larger than L2; no flush"}
 
@@ -303,6 +303,8 @@ def main():
     ap.add_argument("--workload", default=None,
                     help="synthetic workload name (default: the long-context forward for --step "
                          "fwd, the 64K training workload for --step train)")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="seed of the synthetic inputs (default: the workload's own)")
     ap.add_argument("--step", default="fwd", choices=["fwd", "train"],
                     help="fwd: one ring-attention forward per step; train: forward + backward")
     ap.add_argument("--ring", action="store_true",
@@ -323,6 +325,8 @@ def main():
     if args.workload is None:
         args.workload = WORKLOAD if args.step == "fwd" else TRAIN_WORKLOAD
     w = dict(synth.WORKLOADS[args.workload])
+    if args.seed is not None:
+        w["seed"] = args.seed
     if args.impl == "reference":
         run_reference(args, w)
         return
