@@ -436,8 +436,9 @@ __device__ __forceinline__ void producer_role(const FwdArgs& a, uint32_t sbase, 
     tma_prefetch_desc(tmK);
     tma_prefetch_desc(tmV);
     // Each Q tile is read once; K/V tiles are read again by every unit of the kv head.  Q's lines go
-    // first when L2 needs room (L = 131072: DRAM reads per launch 4.3 -> 3.6 GB, time unchanged;
-    // the same hint on K/V as evict_last, or on the output stores, raised the reads instead).
+    // first when L2 needs room (L = 131072, one A/B on one box: DRAM reads per launch 4.3 -> 3.6 GB,
+    // time unchanged; across boxes the reads vary by as much; the same hint on K/V as evict_last,
+    // or on the output stores, raised the reads instead).
     const uint64_t pol_q = l2_policy_evict_first();
     uint32_t kc = 0, qc = 0;
     bool ok = true;
