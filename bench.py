@@ -44,8 +44,8 @@ METRIC = "ring-attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor p
 # bwd_tc_kernel_zigzag_gqa_64k_train_metrics.md, bwd_tc_kernel_striped_gqa_64k_train_metrics.md; the
 # mean of the captures listed there).  Update or drop an entry whenever that kernel changes; a
 # workload without an entry reports null.
-TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 3.917484501e9 + 1.081772245e9,
-                 ("zigzag_gqa_64k_train", "train"): 7.208011776e9 + 3.860009899e9,
+TRAFFIC_BYTES = {("zigzag_gqa_128k", "fwd"): 3.765638144e9 + 1.081261056e9,
+                 ("zigzag_gqa_64k_train", "train"): 7.372813995e9 + 3.979190101e9,
                  ("striped_gqa_64k_train", "train"): 6.576252672e9 + 3.563336192e9}
 
 
