@@ -31,7 +31,10 @@
  *     16-byte aligned.  The library never allocates or frees device memory and keeps no pointer
  *     after a call returns.
  *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).  Work is enqueued on
- *     it; no call synchronises the host unless stated.
+ *     it; no call synchronises the host unless stated.  The device calls enqueue kernel launches
+ *     only: after one call on a device has run outside stream capture (it sets the kernels'
+ *     launch attributes and looks up the status word), they may be recorded into a CUDA graph
+ *     (ring_attn_fwd_host, which synchronises on host buffers, may not).
  *   - Errors: arguments are checked before anything is enqueued; a rejected call returns
  *     RA_ERR_INVALID_ARG or RA_ERR_UNSUPPORTED and enqueues nothing.  A failed launch returns
  *     RA_ERR_CUDA.  ring_attn_last_error() gives a message for the calling thread's last failure.
