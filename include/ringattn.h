@@ -34,7 +34,7 @@
  *     it; no call synchronises the host unless stated.  The device calls enqueue kernel launches
  *     only: after one call on a device has run outside stream capture (it sets the kernels'
  *     launch attributes and looks up the status word), they may be recorded into a CUDA graph
- *     (ring_attn_fwd_host, which synchronises on host buffers, may not).
+ *     (not ring_attn_fwd_host, whose copies and kernels run on streams of the library).
  *   - Errors: arguments are checked before anything is enqueued; a rejected call returns
  *     RA_ERR_INVALID_ARG or RA_ERR_UNSUPPORTED and enqueues nothing.  A failed launch returns
  *     RA_ERR_CUDA.  ring_attn_last_error() gives a message for the calling thread's last failure.
