@@ -251,6 +251,10 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    ring_mode = args.ring or (world > 1 and not args.replicas)
+    if ring_mode:
+        w = dict(w, n=world)  # the same sequence cut into one shard per rank, as the ring arm runs it
     from sequence_sharded_exact_gb300 import synth
 
     gen = "cuda" if torch.cuda.is_available() else "cpu"
@@ -271,8 +275,8 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / max(1, args.steps) * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w, args.step),
+        "scaling": "strong" if ring_mode else "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": ring_config(w, world, args) if ring_mode else config_dict(w, args.step),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{count} random query rows of the workload per step, "
                                    f"{args.steps} timed steps (float64 two-pass attention rows)"},
@@ -554,6 +558,25 @@ class TimedOps:
         return statistics.mean(a.elapsed_time(b) for a, b in ev) if ev else None
 
 
+def ring_config(w, world, args):
+    """The config of the ring mode: the workload cut into one shard per rank (the reference arm
+    reports the same)."""
+    B, H, Hkv, L, d = w["B"], w["H"], w["Hkv"], w["L"], w["d"]
+    S = L // world
+    shard_bytes = (H + 2 * Hkv) * B * S * d * 2
+    ngpu = torch.cuda.device_count()
+    return dict(config_dict(dict(w, n=world), args.step),
+                parallelism=f"context parallel: ring over {world} device(s), one shard of {S} tokens each"
+                            + (f", hierarchical: {args.ring_groups} groups of {world // args.ring_groups}"
+                               if args.ring_groups > 1 else ""),
+                l2=f"each rank's shard of q, k, v ({shard_bytes / 1e9:.2f} GB) "
+                   + ("larger than L2; no flush" if shard_bytes > 129e6
+                      else "smaller than L2 (129 MB): repeated steps may hit in L2"),
+                mode=(f"multi-device ring (blocks over {args.dist_backend.upper()}"
+                      + (f", {world} ranks on {ngpu} GPU(s)" if world > ngpu else "") + ")")
+                if world > 1 else "ring path on one device")
+
+
 def run_ring(args, w, world, rank, local):
     """The multi-device ring: n = world shards of the workload's sequence, one per rank, blocks passed
     round the ring over NCCL (one rank per GPU; gloo only when torch has no NCCL)."""
@@ -629,17 +652,7 @@ def run_ring(args, w, world, rank, local):
         "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: q,k,v ~ N(0,1) bf16" + (", 1% of key rows x8" if w["spike_frac"] else "")
                 + (", dO ~ N(0,1)" if train else "") + ", seeded",
-        "config": dict(config_dict(dict(w, n=n), args.step),
-                       parallelism=f"context parallel: ring over {world} device(s), one shard of {S} tokens each"
-                                   + (f", hierarchical: {args.ring_groups} groups of {world // args.ring_groups}"
-                                      if grid is not None else ""),
-                       l2=f"each rank's shard of q, k, v ({(H + 2 * Hkv) * B * S * d * 2 / 1e9:.2f} GB) "
-                          + ("larger than L2; no flush" if (H + 2 * Hkv) * B * S * d * 2 > 129e6
-                             else "smaller than L2 (129 MB): repeated steps may hit in L2"),
-                       mode=(f"multi-device ring (blocks over {args.dist_backend.upper()}"
-                             + (f", {world} ranks on {torch.cuda.device_count()} GPU(s)"
-                                if world > torch.cuda.device_count() else "") + ")")
-                       if world > 1 else "ring path on one device"),
+        "config": ring_config(w, world, args),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_b, "unit": "TFLOP/s",
                      "frac": achieved / peak_b, "traffic": None,
                      "peak_kind": f"{peak_kind} bf16 burst (MEASURED_PEAKS bf16_tflops)",

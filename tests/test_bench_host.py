@@ -80,3 +80,16 @@ def test_visible_tile_flops_exceed_the_algorithmic_count_by_the_diagonal_halves(
     assert vis - alg == pytest.approx(half_diag, rel=1e-12)
     # non-causal: every tile is visible and the two counts agree
     assert bench.visible_tile_flops(2, 8, 8192, 128, 8, False, "contiguous") == bench.fwd_flops(2, 8, 8192, 128, False)
+
+
+def test_ring_config_cuts_the_workload_into_one_shard_per_rank():
+    """Both arms of an N-rank run report this config: the workload's sequence in N shards."""
+    import argparse
+
+    from sequence_sharded_exact_gb300 import synth
+
+    args = argparse.Namespace(step="fwd", ring_groups=2, dist_backend="nccl")
+    c = bench.ring_config(synth.WORKLOADS["zigzag_gqa_128k"], 8, args)
+    assert c["n_shards"] == 8 and c["L"] == 131072 and "n8" in c["workload"]
+    assert "16384 tokens each" in c["parallelism"] and "2 groups of 4" in c["parallelism"]
+    assert "NCCL" in c["mode"]
