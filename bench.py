@@ -349,7 +349,8 @@ def main():
 
         dist = dist_mod
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        with _StdoutToStderr():
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     else:
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -558,6 +559,23 @@ class TimedOps:
         return statistics.mean(a.elapsed_time(b) for a, b in ev) if ev else None
 
 
+class _StdoutToStderr:
+    """Routes file descriptor 1 to 2 while open: the process-group setup of some backends prints
+    status lines on stdout, where the bench prints only its JSON line."""
+
+    def __enter__(self):
+        sys.stdout.flush()
+        self.saved = os.dup(1)
+        os.dup2(2, 1)
+        return self
+
+    def __exit__(self, *exc):
+        sys.stdout.flush()
+        os.dup2(self.saved, 1)
+        os.close(self.saved)
+        return False
+
+
 def ring_config(w, world, args):
     """The config of the ring mode: the workload cut into one shard per rank (the reference arm
     reports the same)."""
@@ -586,12 +604,13 @@ def run_ring(args, w, world, rank, local):
 
     torch.cuda.set_device(local % torch.cuda.device_count() if world > 1 else 0)
     dev = torch.device("cuda", torch.cuda.current_device())
-    if world > 1 and args.dist_backend == "nccl":
-        dist.init_process_group("nccl", device_id=dev)
-    elif world > 1:
-        dist.init_process_group("gloo")
-    else:
-        dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % free_port(), rank=0, world_size=1)
+    with _StdoutToStderr():
+        if world > 1 and args.dist_backend == "nccl":
+            dist.init_process_group("nccl", device_id=dev)
+        elif world > 1:
+            dist.init_process_group("gloo")
+        else:
+            dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % free_port(), rank=0, world_size=1)
     comm = ring.RingComm()
     grid = ring.RingGrid(comm, args.ring_groups) if args.ring_groups > 1 else None
     rfwd = (lambda *a, **kw: ring.ring_fwd(*a[:3], comm, *a[3:], **kw)) if grid is None else \

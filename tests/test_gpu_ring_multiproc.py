@@ -77,8 +77,9 @@ def test_pages_ring_attention_object_on_one_gpu(tmp_path):
 @pytest.mark.parametrize("step", ["fwd", "train"])
 def test_bench_ring_mode_with_two_ranks(step):
     """bench.py's multi-rank ring mode, as a launcher runs it for N > 1 (here 2 gloo ranks sharing
-    cuda:0 instead of NCCL across 2 GPUs): one JSON line from rank 0 with the whole sequence's
-    TFLOP/s, a clean status word, the roofline of the block launches and the end-to-end leg."""
+    cuda:0 instead of NCCL across 2 GPUs): one JSON line from rank 0, alone on stdout, with the whole
+    sequence's TFLOP/s, a clean status word, the roofline of the block launches and the end-to-end
+    leg."""
     import json
     import pathlib
     import subprocess
@@ -93,8 +94,9 @@ def test_bench_ring_mode_with_two_ranks(step):
            "--dist-backend", "gloo"]
     r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
-    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
-    assert len(lines) == 1, r.stdout
+    printed = [x for x in r.stdout.splitlines() if x.strip()]
+    assert len(printed) == 1, r.stdout  # the JSON line and nothing else on stdout
+    lines = [json.loads(printed[0])]
     line = lines[0]
     assert line["n_gpus"] == 2 and line["steps"] == 2 and line["scaling"] == "strong"
     assert line["device_status"] == 0 and line["value"] > 0 and line["ms_per_step"] > 0
