@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _library_built_from_current_sources():
+    """The tests run against libringattn.so as built from the sources in this tree: it is compiled
+    here if it is missing or older than a source (the binding itself never builds; it raises)."""
+    from sequence_sharded_exact_gb300 import build_lib
+
+    build_lib.build()
