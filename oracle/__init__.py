@@ -54,8 +54,9 @@ def _load():
         lib.oracle_attn_fwd.argtypes = common + [P, P]
         lib.oracle_ring_fwd.argtypes = common + [P, P, P]
         bcommon = [P, P, P, P, I, I, I, Lg, I, I, I, I]
-        lib.oracle_attn_bwd_dq_rows.argtypes = bcommon + [Lg, P, P]
-        lib.oracle_attn_bwd_dkv_rows.argtypes = bcommon + [Lg, P, P, P]
+        given = [P, P, P, P, P, I, I, I, Lg, I, I, I, I]  # q, k, v, dout, out (or NULL), ...
+        lib.oracle_attn_bwd_dq_rows.argtypes = given + [Lg, P, P]
+        lib.oracle_attn_bwd_dkv_rows.argtypes = given + [Lg, P, P, P]
         lib.oracle_attn_bwd.argtypes = bcommon + [P, P, P]
         lib.oracle_block_fwd.argtypes = [P, P, P, I, I, I, Lg, I, I, I, I, I, I, P, P]
         lib.oracle_block_bwd.argtypes = [P, P, P, P, P, P, I, I, I, Lg, I, I, I, I, I, I, P, P, P]
@@ -158,28 +159,48 @@ def attn_bwd(q, k, v, dout, n, causal, layout):
     return dq, dk, dv
 
 
-def attn_bwd_dq_rows(q, k, v, dout, n, causal, layout, rows):
-    """dQ for selected query rows (flat (b*H + h)*L + r) -> [nrows, d]."""
+def _given_out(out, shape):
+    """The output array whose rows give D, as float32 (a bf16 tensor upcasts exactly), or None."""
+    if out is None:
+        return None
+    o = _f32(out)
+    if o.shape != shape:
+        raise ValueError(f"out of shape {o.shape}, expected {shape}")
+    return o
+
+
+def attn_bwd_dq_rows(q, k, v, dout, n, causal, layout, rows, out=None):
+    """dQ for selected query rows (flat (b*H + h)*L + r) -> [nrows, d].
+
+    out: None (D = <dO, O> with the forward definition's O) or an output [B, H, L, d] whose rows give
+    D instead -- the output a backward receives as its input (the forward's stored, rounded result),
+    read as given, like the rounded q, k, v."""
     q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
     B, H, L, d = q.shape
     Hkv = k.shape[1]
+    og = _given_out(out, q.shape)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     dq = np.empty((rows.size, d), np.float64)
-    _check(_load().oracle_attn_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, H, Hkv, L, d,
+    _check(_load().oracle_attn_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                           None if og is None else _ptr(og), B, H, Hkv, L, d,
                                            int(n), int(causal), _layout(layout), rows.size,
                                            _ptr(rows), _ptr(dq)), "attn_bwd_dq_rows")
     return dq
 
 
-def attn_bwd_dkv_rows(q, k, v, dout, n, causal, layout, keys):
-    """dK, dV for selected key rows (flat (b*Hkv + g)*L + t) -> ([nkeys, d], [nkeys, d])."""
+def attn_bwd_dkv_rows(q, k, v, dout, n, causal, layout, keys, out=None):
+    """dK, dV for selected key rows (flat (b*Hkv + g)*L + t) -> ([nkeys, d], [nkeys, d]).
+
+    out: as in attn_bwd_dq_rows (D from the given output's rows, or from the forward definition)."""
     q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
     B, H, L, d = q.shape
     Hkv = k.shape[1]
+    og = _given_out(out, q.shape)
     keys = np.ascontiguousarray(keys, dtype=np.int64)
     dk = np.empty((keys.size, d), np.float64)
     dv = np.empty((keys.size, d), np.float64)
-    _check(_load().oracle_attn_bwd_dkv_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, H, Hkv, L, d,
+    _check(_load().oracle_attn_bwd_dkv_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                            None if og is None else _ptr(og), B, H, Hkv, L, d,
                                             int(n), int(causal), _layout(layout), keys.size,
                                             _ptr(keys), _ptr(dk), _ptr(dv)), "attn_bwd_dkv_rows")
     return dk, dv

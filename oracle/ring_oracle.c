@@ -282,24 +282,28 @@ int oracle_shard_tiles(long L, int n, int causal, int layout, int T, long* tiles
  * Backward (not on the pages; the derivative of the forward definition, reading above).
  * ------------------------------------------------------------------------------------------- */
 
-/* lse and D = <dO, O> of one query row, by the forward definition. */
-static void row_stats(const float* q, const float* k, const float* v, const float* dout, int H,
-                      int Hkv, long L, int d, int n, int causal, int layout, long idx,
-                      double* lse_out, double* D_out, double* o, double* scores)
+/* lse and D = <dO, O> of one query row.  lse is the forward definition's; O is the forward
+ * definition's output row, or, when out_given is not NULL, that row of out_given: the output a
+ * backward receives as its input (a stored, rounded forward result), read like the rounded q, k, v. */
+static void row_stats(const float* q, const float* k, const float* v, const float* dout,
+                      const float* out_given, int H, int Hkv, long L, int d, int n, int causal,
+                      int layout, long idx, double* lse_out, double* D_out, double* o, double* scores)
 {
     long r = idx % L;
     int h = (int)((idx / L) % H);
     int b = (int)(idx / ((long)H * L));
     *lse_out = attention_row(q, k, v, H, Hkv, L, d, n, causal, layout, b, h, r, o, scores);
     double D = 0.0;
-    for (int c = 0; c < d; ++c) D += (double)dout[idx * d + c] * o[c];
+    for (int c = 0; c < d; ++c)
+        D += (double)dout[idx * d + c] * (out_given ? (double)out_given[idx * d + c] : o[c]);
     *D_out = D;
 }
 
-/* dQ for a list of query rows (flat (b*H+h)*L + r); dq is [nrows][d]. */
+/* dQ for a list of query rows (flat (b*H+h)*L + r); dq is [nrows][d].  out: NULL, or the output
+ * [B][H][L][d] whose rows give D (see row_stats). */
 int oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, const float* dout,
-                            int B, int H, int Hkv, long L, int d, int n, int causal, int layout,
-                            long nrows, const long* rows, double* dq)
+                            const float* out, int B, int H, int Hkv, long L, int d, int n, int causal,
+                            int layout, long nrows, const long* rows, double* dq)
 {
     if (!check_args(B, H, Hkv, L, d, n, layout)) return ORACLE_BAD_ARGS;
     const double scale = 1.0 / sqrt((double)d);
@@ -319,20 +323,20 @@ int oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, cons
                 int b = (int)(idx / ((long)H * L));
                 int g = h / (H / Hkv);
                 double lse, D;
-                row_stats(q, k, v, dout, H, Hkv, L, d, n, causal, layout, idx, &lse, &D, o, scores);
+                row_stats(q, k, v, dout, out, H, Hkv, L, d, n, causal, layout, idx, &lse, &D, o, scores);
                 /* attention_row left the scaled scores (or -inf) in scores[] */
                 const float* kh = k + ((long)b * Hkv + g) * L * d;
                 const float* vh = v + ((long)b * Hkv + g) * L * d;
                 const float* dorow = dout + idx * d;
-                double* out = dq + i * d;
-                for (int c = 0; c < d; ++c) out[c] = 0.0;
+                double* dqx = dq + i * d;
+                for (int c = 0; c < d; ++c) dqx[c] = 0.0;
                 for (long t = 0; t < L; ++t) {
                     if (scores[t] == -INFINITY) continue;
                     double P = exp(scores[t] - lse);
                     double dP = 0.0;
                     for (int c = 0; c < d; ++c) dP += (double)dorow[c] * (double)vh[t * d + c];
                     double dS = P * (dP - D);
-                    for (int c = 0; c < d; ++c) out[c] += scale * dS * (double)kh[t * d + c];
+                    for (int c = 0; c < d; ++c) dqx[c] += scale * dS * (double)kh[t * d + c];
                 }
             }
         }
@@ -342,12 +346,13 @@ int oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, cons
     return status;
 }
 
-/* dK and dV for a list of key rows (flat (b*Hkv+g)*L + t); dk, dv are [nkeys][d].
+/* dK and dV for a list of key rows (flat (b*Hkv+g)*L + t); dk, dv are [nkeys][d].  out: NULL, or
+ * the output whose rows give D (see row_stats).
  * Phase 1 marks the query rows that see any listed key, phase 2 evaluates their lse and D by the
  * forward definition, phase 3 sums the contributions. */
 int oracle_attn_bwd_dkv_rows(const float* q, const float* k, const float* v, const float* dout,
-                             int B, int H, int Hkv, long L, int d, int n, int causal, int layout,
-                             long nkeys, const long* keys, double* dk, double* dv)
+                             const float* out, int B, int H, int Hkv, long L, int d, int n, int causal,
+                             int layout, long nkeys, const long* keys, double* dk, double* dv)
 {
     if (!check_args(B, H, Hkv, L, d, n, layout)) return ORACLE_BAD_ARGS;
     const int G = H / Hkv;
@@ -384,7 +389,7 @@ int oracle_attn_bwd_dkv_rows(const float* q, const float* k, const float* v, con
 #pragma omp for schedule(dynamic, 16)
             for (long idx = 0; idx < nq; ++idx)
                 if (need[idx])
-                    row_stats(q, k, v, dout, H, Hkv, L, d, n, causal, layout, idx, &lse[idx],
+                    row_stats(q, k, v, dout, out, H, Hkv, L, d, n, causal, layout, idx, &lse[idx],
                               &Dv[idx], o, scores);
         }
         free(scores);
@@ -440,10 +445,10 @@ int oracle_attn_bwd(const float* q, const float* k, const float* v, const float*
     long* rows = (long*)malloc(sizeof(long) * (nq > nk ? nq : nk));
     if (!rows) return ORACLE_NO_MEMORY;
     for (long i = 0; i < nq; ++i) rows[i] = i;
-    int st = oracle_attn_bwd_dq_rows(q, k, v, dout, B, H, Hkv, L, d, n, causal, layout, nq, rows, dq);
+    int st = oracle_attn_bwd_dq_rows(q, k, v, dout, NULL, B, H, Hkv, L, d, n, causal, layout, nq, rows, dq);
     if (st == ORACLE_OK) {
         for (long i = 0; i < nk; ++i) rows[i] = i;
-        st = oracle_attn_bwd_dkv_rows(q, k, v, dout, B, H, Hkv, L, d, n, causal, layout, nk, rows,
+        st = oracle_attn_bwd_dkv_rows(q, k, v, dout, NULL, B, H, Hkv, L, d, n, causal, layout, nk, rows,
                                       dk, dv);
     }
     free(rows);

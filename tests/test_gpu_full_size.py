@@ -132,11 +132,15 @@ def test_zigzag_gqa_128k_full_head_and_rows(capsys):
         report(capsys, name, "lse, " + what, to_np(lse.view(-1)[idx]), ref_l)
 
 
-def test_training_backward_over_the_whole_range(capsys):
-    """dQ on 4096 seeded rows; dK and dV on keys of the last kv head at natural positions 0-127, at
-    the first and last position of every chunk (the first keys of every shard), and at 64 seeded
-    random positions."""
-    name = "zigzag_gqa_64k_train"
+@pytest.mark.parametrize("name", ["zigzag_gqa_64k_train", "striped_gqa_64k_train", "zigzag_gqa_64k_train_d64"])
+def test_training_backward_over_the_whole_range(capsys, name):
+    """dQ on 4096 seeded rows against the exact gradient; then the most sensitive rows and keys --
+    dQ at positions 0-63 of every head, dK and dV on keys of the last kv head at natural positions
+    0-127, at the first and last position of every 2048-token chunk (for zigzag, the first keys of
+    every shard) and at 64 seeded random positions -- against the backward's definition applied to
+    the inputs this backward receives: D = rowsum(dO * out) over the stored bf16 out it is given,
+    as the rounded q, k, v are read.  At the first positions a gradient is a sum of a few large,
+    cancelling terms, and the rounding of out alone moves it by up to ~1.5e-2 (printed beside)."""
     w = synth.WORKLOADS[name]
     B, H, Hkv, L, d, n = w["B"], w["H"], w["Hkv"], w["L"], w["d"], w["n"]
     x = synth.make_workload(name, device=DEV, gen_device=DEV, with_dout=True)
@@ -145,6 +149,7 @@ def test_training_backward_over_the_whole_range(capsys):
     dq, dk, dv = ra.bwd(x["q"], x["k"], x["v"], out, lse, x["dout"], n, w["causal"], w["layout"])
     torch.cuda.synchronize()
     host = {t: x[t].cpu() for t in ("q", "k", "v", "dout")}
+    out_h = out.cpu()
     rng = np.random.default_rng(65536)
     rows = np.sort(rng.choice(B * H * L, size=4096, replace=False))
     ref_dq = oracle.attn_bwd_dq_rows(host["q"], host["k"], host["v"], host["dout"], n, w["causal"], w["layout"], rows)
@@ -157,11 +162,15 @@ def test_training_backward_over_the_whole_range(capsys):
     # (element-wise bound only: a relative L2 is a per-tensor statistic, estimated above)
     early = np.array([((b * H + h) * L + int(row_of[p])) for b in range(B) for h in range(H) for p in range(64)],
                      dtype=np.int64)
-    ref_e = oracle.attn_bwd_dq_rows(host["q"], host["k"], host["v"], host["dout"], n, w["causal"], w["layout"], early)
+    ref_e = oracle.attn_bwd_dq_rows(host["q"], host["k"], host["v"], host["dout"], n, w["causal"], w["layout"],
+                                    early, out=out_h)
+    exact_e = oracle.attn_bwd_dq_rows(host["q"], host["k"], host["v"], host["dout"], n, w["causal"],
+                                      w["layout"], early)
     got_e = to_np(dq.view(-1, d)[torch.from_numpy(early).to(DEV)])
     ma = float(np.abs(got_e - ref_e).max())
     with capsys.disabled():
-        print(f"\n[parity] {name} dq, positions 0-63 of every head: {ref_e.size} values, max-abs {ma:.3e}")
+        print(f"\n[parity] {name} dq, positions 0-63 of every head: {ref_e.size} values, max-abs {ma:.3e} "
+              f"(against the exact gradient: {float(np.abs(got_e - exact_e).max()):.3e})")
     assert ma <= BF16_MAX_ABS, f"dq at early positions: max-abs {ma:.3e}"
     chunk = L // (2 * n)
     positions = set(range(128))
@@ -172,9 +181,9 @@ def test_training_backward_over_the_whole_range(capsys):
     keys = np.array(sorted(((B - 1) * Hkv + g) * L + int(row_of[p]) for p in positions), dtype=np.int64)
     assert keys.size >= 64
     ref_dk, ref_dv = oracle.attn_bwd_dkv_rows(host["q"], host["k"], host["v"], host["dout"], n, w["causal"],
-                                              w["layout"], keys)
+                                              w["layout"], keys, out=out_h)
     idx = torch.from_numpy(keys).to(DEV)
-    what = f"{keys.size} keys of kv head {g} (positions 0-127, every chunk edge, 64 seeded)"
+    what = f"{keys.size} keys of kv head {g} (positions 0-127, every chunk edge, 64 seeded; D from the given out)"
     report(capsys, name, "dk, " + what, to_np(dk.view(-1, d)[idx]), ref_dk)
     report(capsys, name, "dv, " + what, to_np(dv.view(-1, d)[idx]), ref_dv)
 

@@ -327,6 +327,56 @@ def test_bwd_rows_match_full():
     np.testing.assert_allclose(dv2, dv.reshape(-1, d)[keys], rtol=0, atol=1e-13)
 
 
+def test_bwd_rows_with_the_exact_output_given_equal_the_definition():
+    """D from a given output: given the forward definition's own output (rounded to float32, the
+    oracle's input precision), the rows equal the default ones up to that rounding."""
+    B, H, Hkv, L, d, n = 1, 4, 2, 32, 8, 4
+    q, k, v, do = (rand(s, i) for i, s in enumerate(
+        [(B, H, L, d), (B, Hkv, L, d), (B, Hkv, L, d), (B, H, L, d)], start=131))
+    o, _ = oracle.attn_fwd(q, k, v, n, True, "zigzag")
+    rows = np.arange(B * H * L)
+    keys = np.arange(B * Hkv * L)
+    np.testing.assert_allclose(oracle.attn_bwd_dq_rows(q, k, v, do, n, True, "zigzag", rows, out=o),
+                               oracle.attn_bwd_dq_rows(q, k, v, do, n, True, "zigzag", rows), rtol=0, atol=1e-6)
+    dk1, dv1 = oracle.attn_bwd_dkv_rows(q, k, v, do, n, True, "zigzag", keys, out=o)
+    dk0, dv0 = oracle.attn_bwd_dkv_rows(q, k, v, do, n, True, "zigzag", keys)
+    np.testing.assert_allclose(dk1, dk0, rtol=0, atol=1e-6)
+    assert np.array_equal(dv1, dv0)  # dV does not involve D
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "striped"])
+def test_bwd_rows_given_output_enters_only_through_D(layout):
+    """Changing one element out[p, c] by delta changes D_p by delta * dO[p, c], and nothing else:
+    dV stays the same, dK_t moves by -scale P_pt D-change q_p for every key t that query p sees,
+    dQ_p by -scale D-change sum_t P_pt k_t, and every other dQ row stays the same.  P is computed
+    here from q, k and the oracle's lse with numpy."""
+    B, H, Hkv, L, d, n = 1, 2, 1, 32, 8, 2
+    q, k, v, do = (rand(s, i) for i, s in enumerate(
+        [(B, H, L, d), (B, Hkv, L, d), (B, Hkv, L, d), (B, H, L, d)], start=141))
+    o, lse = oracle.attn_fwd(q, k, v, n, True, layout)
+    o = o.astype(np.float32)
+    h, r, c, delta = 1, 21, 3, 0.25
+    o2 = o.copy()
+    o2[0, h, r, c] += delta
+    rows = np.arange(B * H * L)
+    keys = np.arange(B * Hkv * L)
+    dq1 = oracle.attn_bwd_dq_rows(q, k, v, do, n, True, layout, rows, out=o)
+    dq2 = oracle.attn_bwd_dq_rows(q, k, v, do, n, True, layout, rows, out=o2)
+    dk1, dv1 = oracle.attn_bwd_dkv_rows(q, k, v, do, n, True, layout, keys, out=o)
+    dk2, dv2 = oracle.attn_bwd_dkv_rows(q, k, v, do, n, True, layout, keys, out=o2)
+    scale = 1.0 / math.sqrt(d)
+    nat = buffer_to_natural(L, n, layout)
+    qd, kd = q.astype(np.float64), k.astype(np.float64)
+    P = np.exp(scale * kd[0, 0] @ qd[0, h, r] - lse[0, h, r]) * (nat <= nat[r])  # [L] over key rows
+    dD = delta * float(do[0, h, r, c])
+    assert np.array_equal(dv2, dv1)
+    np.testing.assert_allclose(dk2 - dk1, -scale * dD * P[:, None] * qd[0, h, r][None, :], rtol=0, atol=1e-12)
+    flat = h * L + r
+    np.testing.assert_allclose(dq2[flat] - dq1[flat], -scale * dD * (P @ kd[0, 0]), rtol=0, atol=1e-12)
+    others = np.arange(B * H * L) != flat
+    assert np.array_equal(dq2[others], dq1[others])
+
+
 def test_synth_recipe():
     """The generator is seeded, rounds to the dtype, and scales exactly round(0.01 L) key rows."""
     a = synth.make_inputs(1, 2, 1, 1000, 8, dtype=torch.bfloat16, seed=7, spike_frac=0.01)
