@@ -871,6 +871,11 @@ def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
                                        out=ot, lse=lt, stream=stream), 3, 1, stream)
     res["train_fwd_only"] = {"tflops": ff / (statistics.mean(fms) / 1e3) / 1e12,
                              "ms": statistics.mean(fms)}
+    if bwd_steps:  # the backward alone: the step's time less the forward's (both timed above)
+        bms = statistics.mean(ms) - statistics.mean(fms)
+        res["train_bwd_only"] = {"tflops": 2.5 * ff / (bms / 1e3) / 1e12, "ms": bms,
+                                 "frac": 2.5 * ff / (bms / 1e3) / 1e12 / peak_b,
+                                 "how": "forward + backward step time minus the forward's, CUDA events"}
     del xt, ot, lt, dq, dk, dv, wsb
     # head dim 64 and the striped layout: the long-context forward and the training step
     for name in ("zigzag_gqa_128k_d64", "striped_gqa_128k", "zigzag_gqa_64k_train_d64", "striped_gqa_64k_train"):
