@@ -95,6 +95,18 @@ RA_API ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void
                         int dtype, void* stream);
 
 /*
+ * ring_attn_fwd_f32out -- ring_attn_fwd with the output written in float32 whatever the inputs'
+ * dtype: the normalised output before it is rounded to dtype (ring_attn_fwd's out is this array
+ * rounded to nearest).  For a backward that takes D = rowsum(dout * out) from the unrounded output
+ * (ring_attn_bwd_f32out): with bf16 out, D carries out's rounding, which at the first positions of a
+ * causal sequence (a few large, cancelling terms per gradient) moves dq and dk by up to ~1.5e-2.
+ *   out: DEVICE float32 [B][H][L][d].  Everything else as ring_attn_fwd.
+ */
+RA_API ra_status ring_attn_fwd_f32out(const void* q, const void* k, const void* v, float* out, float* lse,
+                               int B, int H, int Hkv, int L, int d, int n_shards, int causal, int layout,
+                               int dtype, void* stream);
+
+/*
  * ring_attn_ring_step_fwd -- ring step `step` alone, for all shards at once: shard i attends to
  * the K/V of shard (i - step) mod n_shards only (one block_attention of LLM-101-CN section 6.2).
  *   o_part [B][H][L][d] float32 receives each row's attention output normalised by its own sum;
@@ -181,6 +193,16 @@ RA_API ra_status ring_attn_bwd(const void* q, const void* k, const void* v, cons
                         int grad_dtype, void* workspace, size_t workspace_bytes, int B, int H,
                         int Hkv, int L, int d, int n_shards, int causal, int layout, int dtype,
                         void* stream);
+/*
+ * ring_attn_bwd_f32out -- ring_attn_bwd with `out` in float32 (from ring_attn_fwd_f32out) while
+ * q, k, v, dout are in dtype: D = rowsum(dout * out) is taken from the unrounded output.  Same
+ * workspace, arguments and results as ring_attn_bwd otherwise.
+ */
+RA_API ra_status ring_attn_bwd_f32out(const void* q, const void* k, const void* v, const float* out,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               int grad_dtype, void* workspace, size_t workspace_bytes, int B, int H,
+                               int Hkv, int L, int d, int n_shards, int causal, int layout, int dtype,
+                               void* stream);
 RA_API size_t ring_attn_bwd_workspace_size(int B, int H, int Hkv, int L, int d, int grad_dtype);
 
 /*

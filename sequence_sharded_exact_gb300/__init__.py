@@ -11,10 +11,12 @@ from .binding import (  # noqa: F401
     device_check,
     device_status,
     fwd,
+    fwd_f32out,
     fwd_host,
     fwd_stepwise,
     fwd_tile_visits,
     bwd,
+    bwd_f32out,
     bwd_tile_visits,
     bwd_static_scratch,
     bwd_static_scratch_capacity,

@@ -35,7 +35,8 @@ EXPORTS = (
     "ring_attn_ring_step_fwd_accumulate",
     "ring_attn_fwd_host_workspace_size", "ring_attn_selftest_bounded_wait", "ring_attn_device_check",
     "ring_attn_block_fwd", "ring_attn_block_bwd", "ring_attn_bwd_preprocess", "ring_attn_f32_zero",
-    "ring_attn_f32_add", "ring_attn_f32_convert", "ring_attn_block_rope",
+    "ring_attn_f32_add", "ring_attn_f32_convert", "ring_attn_block_rope", "ring_attn_fwd_f32out",
+    "ring_attn_bwd_f32out",
 )
 
 
@@ -57,6 +58,7 @@ def library():
         lib = ctypes.CDLL(LIB_PATH)
         P, I, LL, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t
         lib.ring_attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P]
+        lib.ring_attn_fwd_f32out.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P]
         lib.ring_attn_ring_step_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
         lib.ring_attn_lse_merge.argtypes = [P, P, P, P, LL, I, P]
         lib.ring_attn_fwd_stepwise.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P]
@@ -64,6 +66,7 @@ def library():
         lib.ring_attn_fwd_stepwise_workspace_size.restype = SZ
         lib.ring_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, P, SZ, I, I, I, I, I, I, I, I,
                                       I, P]
+        lib.ring_attn_bwd_f32out.argtypes = lib.ring_attn_bwd.argtypes
         lib.ring_attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.ring_attn_bwd_workspace_size.restype = SZ
         lib.ring_attn_shard_tiles.argtypes = [I, I, I, I, I, P]
@@ -364,9 +367,9 @@ def bwd_tile_visits(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigz
     return dq, dk, dv, visits
 
 
-def _need_bwd_args(q, k, v, out, lse, dout, grad_dtype):
+def _need_bwd_args(q, k, v, out, lse, dout, grad_dtype, out_dtype=None):
     B, H, Hkv, L, d = _need_qkv(q, k, v)
-    _need(out, "out", q.device, q.shape, q.dtype)
+    _need(out, "out", q.device, q.shape, q.dtype if out_dtype is None else out_dtype)
     _need(lse, "lse", q.device, (B, H, L), torch.float32)
     _need(dout, "dout", q.device, q.shape, q.dtype)
     _dtype_code(grad_dtype)
@@ -381,8 +384,9 @@ def _need_grads(dq, dk, dv, device, dims, grad_dtype):
 
 
 def _bwd(q, k, v, out, lse, dout, n_shards, causal, layout, grad_dtype, dq, dk, dv, workspace,
-         visits, stream):
-    B, H, Hkv, L, d = _need_bwd_args(q, k, v, out, lse, dout, grad_dtype)
+         visits, stream, out_f32=False):
+    B, H, Hkv, L, d = _need_bwd_args(q, k, v, out, lse, dout, grad_dtype,
+                                     torch.float32 if out_f32 else None)
     if dq is None:
         dq = torch.empty((B, H, L, d), dtype=grad_dtype, device=q.device)
     if dk is None:
@@ -397,11 +401,37 @@ def _bwd(q, k, v, out, lse, dout, n_shards, causal, layout, grad_dtype, dq, dk, 
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
             _ptr(dv), _dtype_code(grad_dtype), _ptr(workspace), workspace.numel(), B, H, Hkv, L, d,
             int(n_shards), int(causal), _layout(layout), _dtype_code(q.dtype))
-    if visits is None:
+    if out_f32:
+        _check(library().ring_attn_bwd_f32out(*args, _stream(stream, q.device)))
+    elif visits is None:
         _check(library().ring_attn_bwd(*args, _stream(stream, q.device)))
     else:
         _check(library().ring_attn_bwd_tile_visits(*args, _ptr(visits), _stream(stream, q.device)))
     return dq, dk, dv
+
+
+def fwd_f32out(q, k, v, n_shards, causal=True, layout="zigzag", out=None, lse=None, stream=None):
+    """ring_attn_fwd_f32out: the forward with out in float32 -- the output before it is rounded to
+    q's dtype.  Returns (out [B,H,L,d] float32, lse [B,H,L] float32)."""
+    B, H, Hkv, L, d = _need_qkv(q, k, v)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    _need(out, "out", q.device, q.shape, torch.float32)
+    _need(lse, "lse", q.device, (B, H, L), torch.float32)
+    _check(library().ring_attn_fwd_f32out(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, L, d,
+                                          int(n_shards), int(causal), _layout(layout), _dtype_code(q.dtype),
+                                          _stream(stream, q.device)))
+    return out, lse
+
+
+def bwd_f32out(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigzag",
+               grad_dtype=torch.float32, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """ring_attn_bwd_f32out: the backward with out in float32 (from fwd_f32out), so that D is taken from
+    the unrounded output.  Returns (dq, dk, dv) in grad_dtype."""
+    return _bwd(q, k, v, out, lse, dout, n_shards, causal, layout, grad_dtype, dq, dk, dv,
+                workspace, None, stream, out_f32=True)
 
 
 def bwd_static_scratch(q, k, v, out, lse, dout, n_shards, causal=True, layout="zigzag",

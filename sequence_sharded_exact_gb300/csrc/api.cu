@@ -177,7 +177,7 @@ ra_status ring_attn_bwd_path(int B, int H, int Hkv, int L, int d, int n_shards, 
 namespace {
 
 ra_status fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, const Problem& p,
-                   unsigned long long* visits, void* stream)
+                   unsigned long long* visits, void* stream, int mode = kFwdFused)
 {
     ra_status st = check_problem(p);
     if (st != RA_OK) return st;
@@ -193,9 +193,9 @@ ra_status fwd_impl(const void* q, const void* k, const void* v, void* out, float
     if (tc) {
         unsigned int* sw = status_word(&e);
         if (!sw) return cuda_fail(e, "status word");
-        e = launch_fwd_tc(p, q, k, v, out, lse, kFwdFused, 0, sw, s, visits);
+        e = launch_fwd_tc(p, q, k, v, out, lse, mode, 0, sw, s, visits);
     } else {
-        e = launch_fwd_simt(p, q, k, v, out, lse, kFwdFused, 0, s);
+        e = launch_fwd_simt(p, q, k, v, out, lse, mode, 0, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "ring_attn_fwd launch");
     return RA_OK;
@@ -209,6 +209,14 @@ ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out, 
 {
     return fwd_impl(q, k, v, out, lse, Problem{B, H, Hkv, L, d, n_shards, causal, layout, dtype},
                     nullptr, stream);
+}
+
+ra_status ring_attn_fwd_f32out(const void* q, const void* k, const void* v, float* out, float* lse, int B,
+                               int H, int Hkv, int L, int d, int n_shards, int causal, int layout,
+                               int dtype, void* stream)
+{
+    return fwd_impl(q, k, v, out, lse, Problem{B, H, Hkv, L, d, n_shards, causal, layout, dtype},
+                    nullptr, stream, kFwdFusedF32);
 }
 
 ra_status ring_attn_fwd_tile_visits(const void* q, const void* k, const void* v, void* out,
@@ -338,7 +346,8 @@ namespace {
 
 ra_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
                    const void* dout, void* dq, void* dk, void* dv, int grad_dtype, void* workspace,
-                   size_t workspace_bytes, const Problem& p, unsigned long long* visits, void* stream)
+                   size_t workspace_bytes, const Problem& p, unsigned long long* visits, void* stream,
+                   int out_dtype = -1)
 {
     const int B = p.B, H = p.H, Hkv = p.Hkv, L = p.L, d = p.d, dtype = p.dtype;
     ra_status st = check_problem(p);
@@ -361,7 +370,7 @@ ra_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
     const long long rows = p.q_rows();
     char* ws = static_cast<char*>(workspace);
     float* D = reinterpret_cast<float*>(ws);
-    cudaError_t e = launch_bwd_preprocess(out, dout, dtype, rows, d, D, s);
+    cudaError_t e = launch_bwd_preprocess(out, dout, dtype, rows, d, D, s, out_dtype);
     if (e != cudaSuccess) return cuda_fail(e, "ring_attn_bwd preprocess launch");
     if (tc) {
         unsigned int* sw = status_word(&e);
@@ -391,6 +400,16 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
 {
     return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, grad_dtype, workspace, workspace_bytes,
                     Problem{B, H, Hkv, L, d, n_shards, causal, layout, dtype}, nullptr, stream);
+}
+
+ra_status ring_attn_bwd_f32out(const void* q, const void* k, const void* v, const float* out,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               int grad_dtype, void* workspace, size_t workspace_bytes, int B, int H,
+                               int Hkv, int L, int d, int n_shards, int causal, int layout, int dtype,
+                               void* stream)
+{
+    return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, grad_dtype, workspace, workspace_bytes,
+                    Problem{B, H, Hkv, L, d, n_shards, causal, layout, dtype}, nullptr, stream, RA_F32);
 }
 
 ra_status ring_attn_bwd_tile_visits(const void* q, const void* k, const void* v, const void* out,

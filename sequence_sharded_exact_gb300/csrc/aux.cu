@@ -184,6 +184,25 @@ bwd_preprocess_bf16_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfl
     }
 }
 
+// D from a float32 output and a bf16 dout (the forward's output kept before rounding): one warp per
+// row, lanes over the row's elements.
+__global__ void __launch_bounds__(256)
+bwd_preprocess_f32out_kernel(const float* __restrict__ out, const __nv_bfloat16* __restrict__ dout, long long rows,
+                             int d, float* __restrict__ D)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+         row += warps) {
+        const long long base = row * d;
+        float acc = 0.f;
+        for (int c = lane; c < d; c += 32) acc = fmaf(out[base + c], __bfloat162float(dout[base + c]), acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+        if (lane == 0) D[row] = acc;
+    }
+}
+
 __global__ void __launch_bounds__(256)
 convert_kernel(const float* __restrict__ src, void* __restrict__ dst, int dst_dtype,
                long long count, float scale)
@@ -262,10 +281,13 @@ cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part,
 }
 
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, int dtype, long long rows,
-                                  int d, float* D, cudaStream_t s)
+                                  int d, float* D, cudaStream_t s, int out_dtype)
 {
     if (rows == 0) return cudaSuccess;
-    if (dtype == 0)
+    if (out_dtype == 0 && dtype == 1)
+        bwd_preprocess_f32out_kernel<<<grid_for(rows, 8), 256, 0, s>>>(
+            static_cast<const float*>(out), static_cast<const __nv_bfloat16*>(dout), rows, d, D);
+    else if (dtype == 0)
         bwd_preprocess_kernel<float><<<grid_for(rows, 8), 256, 0, s>>>(
             static_cast<const float*>(out), static_cast<const float*>(dout), rows, d, D);
     else if (d == 128)

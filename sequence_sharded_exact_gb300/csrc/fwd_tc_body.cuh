@@ -134,8 +134,8 @@ struct KvWalk {
         geo = a.geo;
         shard = u.shard;
         p_hi = u.p_hi;
-        st = a.mode == kFwdFused ? 0 : a.step;
-        st_end = a.mode == kFwdFused ? a.geo.n : a.step + 1;
+        st = fwd_all_steps(a.mode) ? 0 : a.step;
+        st_end = fwd_all_steps(a.mode) ? a.geo.n : a.step + 1;
         c = 0;
         t = 0;
         settle();
@@ -183,8 +183,8 @@ __device__ __forceinline__ bool unit_of(const FwdArgs& a, long long item, int me
     u.p_hi = natural_position(a.geo, u.r0 + kBlock - 1);
     u.shard = u.r0 / a.geo.S;
     int nt = 0;
-    const int s0 = a.mode == kFwdFused ? 0 : a.step;
-    const int s1 = a.mode == kFwdFused ? a.geo.n : a.step + 1;
+    const int s0 = fwd_all_steps(a.mode) ? 0 : a.step;
+    const int s1 = fwd_all_steps(a.mode) ? a.geo.n : a.step + 1;
     for (int st = s0; st < s1; ++st)
         for (int c = 0; c < a.geo.cps; ++c) nt += (kv_range(a.geo, u.shard, st, c, u.p_hi).count + kTile - 1) / kTile;
     u.ntiles = nt;

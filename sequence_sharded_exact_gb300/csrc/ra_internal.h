@@ -38,7 +38,11 @@ enum FwdMode {
     kFwdFused = 0,     // all ring steps, write out (dtype) + lse
     kFwdRingStep = 1,  // one ring step, write float32 partial + lse (-inf when nothing visible)
     kFwdRingStepAcc = 2,  // one ring step folded into a running float32 output + lse, in place
+    kFwdFusedF32 = 3,  // all ring steps, write out as float32 (before any rounding to dtype) + lse
 };
+
+// Does the mode walk every ring step (the whole K/V sequence) rather than one?
+__host__ __device__ inline bool fwd_all_steps(int mode) { return mode == kFwdFused || mode == kFwdFusedF32; }
 
 // SIMT (CUDA-core) kernels: any shape, f32 or bf16 inputs.
 // blk (optional): one device's block call; the forward then runs ring step
@@ -80,7 +84,8 @@ cudaError_t launch_lse_merge(float* o_acc, float* lse_acc, const float* o_part,
 cudaError_t launch_convert(const float* src, void* dst, int dst_dtype, long long count,
                            float scale, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, int dtype, long long rows,
-                                  int d, float* D, cudaStream_t s);
+                                  int d, float* D, cudaStream_t s,
+                                  int out_dtype = -1);
 cudaError_t launch_zero(float* dst, long long count, cudaStream_t s);
 // acc[i] += part[i] for count float32 values.
 cudaError_t launch_add(float* acc, const float* part, long long count, cudaStream_t s);

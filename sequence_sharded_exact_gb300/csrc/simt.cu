@@ -84,8 +84,8 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     float m = -INFINITY, l = 0.f, o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-    const int s0 = mode == kFwdFused ? 0 : step;
-    const int s1 = mode == kFwdFused ? geo.n : step + 1;
+    const int s0 = fwd_all_steps(mode) ? 0 : step;
+    const int s1 = fwd_all_steps(mode) ? geo.n : step + 1;
     for (int st = s0; st < s1; ++st) {
         for (int c = 0; c < geo.cps; ++c) {
             const KvRange kr = kv_range(geo, i, st, c, p);

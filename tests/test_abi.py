@@ -259,3 +259,23 @@ def test_block_calls_check_their_arguments(lib):
     # an empty count enqueues nothing and needs no device
     assert lib.ring_attn_f32_zero(None, LL(0), None) == binding.RA_OK
     assert lib.ring_attn_f32_convert(None, None, LL(0), 1, None) == binding.RA_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), binding.RA_ERR_INVALID_ARG),
+    (dict(out=8), binding.RA_ERR_INVALID_ARG),
+    (dict(d=96), binding.RA_ERR_UNSUPPORTED),
+    (dict(L=1026, n=6), binding.RA_ERR_INVALID_ARG),
+])
+def test_float32_output_calls_check_their_arguments_first(lib, kw, status):
+    """ring_attn_fwd_f32out / ring_attn_bwd_f32out share the forward's and the backward's checks."""
+    a = dict(q=16, k=16, v=16, out=16, lse=16, B=1, H=2, Hkv=1, L=1024, d=128, n=4, causal=1, layout=1, dtype=1)
+    a.update(kw)
+    P = ctypes.c_void_p
+    assert lib.ring_attn_fwd_f32out(P(a["q"]), P(a["k"]), P(a["v"]), P(a["out"]), P(a["lse"]), a["B"], a["H"],
+                                    a["Hkv"], a["L"], a["d"], a["n"], a["causal"], a["layout"], a["dtype"],
+                                    None) == status
+    ws = 256
+    assert lib.ring_attn_bwd_f32out(P(a["q"]), P(a["k"]), P(a["v"]), P(a["out"]), P(a["lse"]), P(16), P(16),
+                                    P(16), P(16), 0, P(ws), ctypes.c_size_t(1 << 40), a["B"], a["H"], a["Hkv"],
+                                    a["L"], a["d"], a["n"], a["causal"], a["layout"], a["dtype"], None) == status
