@@ -1,6 +1,7 @@
 """Out-of-bounds writes: every tensor a call receives sits inside a larger buffer whose margins (64 KB
 on each side) hold a sentinel pattern; after the call the margins must be unchanged and the inputs
-untouched.  Covers the fused forward and backward on both kernel paths, the per-device block calls,
+untouched.  Covers the fused forward and backward on both kernel paths (and their float32-output
+forms), the per-device block calls,
 the ring-step and stepwise forwards, RoPE and the Ulysses all-to-all (compute-sanitizer is not used
 on this pool; this is its stand-in for writes)."""
 import pytest
@@ -66,6 +67,13 @@ def test_no_call_writes_outside_its_tensors(B, H, Hkv, L, d, n, layout, dtype):
         ws = g.new((max(256, ra.bwd_workspace_size(B, H, Hkv, L, d, gd)),), torch.uint8)
         ra.bwd(q, k, v, out, lse, do, n, True, layout, grad_dtype=gd, dq=dq, dk=dk, dv=dv, workspace=ws)
         g.check()
+    # the forward's float32 output and the backward that takes D from it
+    o32, l32 = g.new(q.shape, torch.float32), g.new((B, H, L), torch.float32)
+    ra.fwd_f32out(q, k, v, n, True, layout, out=o32, lse=l32)
+    dq3, dk3, dv3 = g.new(q.shape, torch.float32), g.new(k.shape, torch.float32), g.new(v.shape, torch.float32)
+    ws3 = g.new((max(256, ra.bwd_workspace_size(B, H, Hkv, L, d, torch.float32)),), torch.uint8)
+    ra.bwd_f32out(q, k, v, o32, l32, do, n, True, layout, dq=dq3, dk=dk3, dv=dv3, workspace=ws3)
+    g.check()
     # ring steps: a written partial, then a step folded into it; the stepwise forward
     op, lp = g.new((B, H, L, d), torch.float32), g.new((B, H, L), torch.float32)
     ra.ring_step_fwd(q, k, v, n, 0, True, layout, o_part=op, lse_part=lp)
