@@ -292,6 +292,13 @@ RA_API ra_status ring_attn_bwd_preprocess(const void* out, const void* dout, flo
                                           int dtype, void* stream);
 
 /*
+ * ring_attn_bwd_preprocess_f32out -- ring_attn_bwd_preprocess with out in float32 (the forward's
+ * output before rounding, e.g. one device's float32 running output of the ring) and dout in dtype.
+ */
+RA_API ra_status ring_attn_bwd_preprocess_f32out(const float* out, const void* dout, float* D, long long rows,
+                                          int d, int dtype, void* stream);
+
+/*
  * ring_attn_block_rope -- ring_attn_rope on one device's local buffer: x [B][H][S][d] holds shard
  * `shard`'s rows (rows [shard*S, (shard+1)*S) of the whole-sequence layout), and every row turns by
  * the angle of its natural position in the whole sequence, so that the K/V blocks a device passes

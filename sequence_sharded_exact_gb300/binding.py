@@ -36,7 +36,7 @@ EXPORTS = (
     "ring_attn_fwd_host_workspace_size", "ring_attn_selftest_bounded_wait", "ring_attn_device_check",
     "ring_attn_block_fwd", "ring_attn_block_bwd", "ring_attn_bwd_preprocess", "ring_attn_f32_zero",
     "ring_attn_f32_add", "ring_attn_f32_convert", "ring_attn_block_rope", "ring_attn_fwd_f32out",
-    "ring_attn_bwd_f32out",
+    "ring_attn_bwd_f32out", "ring_attn_bwd_preprocess_f32out",
 )
 
 
@@ -67,6 +67,7 @@ def library():
         lib.ring_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, P, SZ, I, I, I, I, I, I, I, I,
                                       I, P]
         lib.ring_attn_bwd_f32out.argtypes = lib.ring_attn_bwd.argtypes
+        lib.ring_attn_bwd_preprocess_f32out.argtypes = [P, P, P, LL, I, I, P]
         lib.ring_attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.ring_attn_bwd_workspace_size.restype = SZ
         lib.ring_attn_shard_tiles.argtypes = [I, I, I, I, I, P]
@@ -645,16 +646,19 @@ def block_bwd(q, k, v, dout, lse, D, dq_acc, dk, dv, n_shards, shard_q, shard_kv
 
 
 def bwd_preprocess(out, dout, D=None, stream=None):
-    """ring_attn_bwd_preprocess: D = rowsum(out * dout) over the last dimension, float32."""
+    """ring_attn_bwd_preprocess: D = rowsum(out * dout) over the last dimension, float32.  out may be
+    float32 while dout is bf16 (ring_attn_bwd_preprocess_f32out: the unrounded output)."""
     _need(out, "out", out.device)
-    _dtype_code(out.dtype)
-    _need(dout, "dout", out.device, out.shape, out.dtype)
+    _dtype_code(dout.dtype)
+    f32out = out.dtype == torch.float32 and dout.dtype != torch.float32
+    _need(dout, "dout", out.device, out.shape, dout.dtype if f32out else out.dtype)
     if D is None:
         D = torch.empty(out.shape[:-1], dtype=torch.float32, device=out.device)
     _need(D, "D", out.device, out.shape[:-1], torch.float32)
     d = int(out.shape[-1])
-    _check(library().ring_attn_bwd_preprocess(_ptr(out), _ptr(dout), _ptr(D), int(D.numel()), d,
-                                              _dtype_code(out.dtype), _stream(stream, out.device)))
+    call = library().ring_attn_bwd_preprocess_f32out if f32out else library().ring_attn_bwd_preprocess
+    _check(call(_ptr(out), _ptr(dout), _ptr(D), int(D.numel()), d, _dtype_code(dout.dtype),
+                _stream(stream, out.device)))
     return D
 
 

@@ -511,6 +511,21 @@ ra_status ring_attn_bwd_preprocess(const void* out, const void* dout, float* D, 
     return RA_OK;
 }
 
+ra_status ring_attn_bwd_preprocess_f32out(const float* out, const void* dout, float* D, long long rows, int d,
+                                          int dtype, void* stream)
+{
+    ra_status st = check_count(rows);
+    if (st != RA_OK) return st;
+    if (d < 1) return fail(RA_ERR_INVALID_ARG, "d must be >= 1");
+    if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (rows == 0) return RA_OK;
+    if ((st = check_ptrs({out, dout, D})) != RA_OK) return st;
+    if ((st = check_device()) != RA_OK) return st;
+    cudaError_t e = launch_bwd_preprocess(out, dout, dtype, rows, d, D, static_cast<cudaStream_t>(stream), RA_F32);
+    if (e != cudaSuccess) return cuda_fail(e, "ring_attn_bwd_preprocess_f32out launch");
+    return RA_OK;
+}
+
 ra_status ring_attn_f32_zero(float* x, long long count, void* stream)
 {
     ra_status st = check_count(count);

@@ -139,9 +139,10 @@ class LibraryOps:
         self.b.f32_add(acc, part, stream=self.stream)
 
 
-def ring_fwd(q, k, v, comm, causal=True, layout="zigzag", ops=None):
+def ring_fwd(q, k, v, comm, causal=True, layout="zigzag", ops=None, keep_f32=False):
     """Ring forward on this device (rank i of n = world size): q [B,H,S,d] and k, v [B,Hkv,S,d] are
-    shard i.  Returns (out [B,H,S,d] in q's dtype, lse [B,H,S] float32) for shard i's rows."""
+    shard i.  Returns (out [B,H,S,d] in q's dtype, lse [B,H,S] float32) for shard i's rows, and with
+    keep_f32 also the float32 running output the out was converted from (for a backward's D)."""
     ops = ops or LibraryOps()
     n, i = comm.world, comm.rank
     B, H, S, d = q.shape
@@ -159,6 +160,8 @@ def ring_fwd(q, k, v, comm, causal=True, layout="zigzag", ops=None):
         if h is not None:
             comm.wait(h)
             cur = nxt
+    if keep_f32:
+        return ops.convert(o_acc, q.dtype), lse_acc, o_acc
     return ops.convert(o_acc, q.dtype), lse_acc
 
 
@@ -171,6 +174,7 @@ def _spare_blocks(k, v, n):
 def ring_bwd(q, k, v, out, lse, dout, comm, causal=True, layout="zigzag", grad_dtype=torch.float32, ops=None):
     """Ring backward on this device: the inputs of ring_fwd plus its (out, lse) and the upstream
     gradient dout of shard i.  Returns (dq [B,H,S,d], dk, dv [B,Hkv,S,d]) of shard i in grad_dtype.
+    out may be the float32 running output ring_fwd returns with keep_f32 (D from the unrounded output).
 
     Per step r (block j = (i - r) mod n): the K/V transfer of the next block starts, this device's
     contribution to block j's dK/dV is computed into `part` (dQ is added into the local dq_acc), the
@@ -244,12 +248,12 @@ class RingGrid:
         return self.rank(self.p - a, self.q - b)
 
 
-def ring_fwd_2d(q, k, v, grid, causal=True, layout="zigzag", ops=None):
+def ring_fwd_2d(q, k, v, grid, causal=True, layout="zigzag", ops=None, keep_f32=False):
     """Ring forward over a RingGrid: for each global step a = 0..P-1 the block that arrived over the
     global ring (at a = 0 the device's own) goes round the local ring in Q local steps, while the next
     one comes from the previous group: one inter-group transfer per Q block steps, overlapped with
     them.  At (a, b) this rank holds the block of shard grid.held(a, b); over the P * Q steps it meets
-    every shard once.  Same inputs and results as ring_fwd."""
+    every shard once.  Same inputs and results as ring_fwd (keep_f32 as there)."""
     ops = ops or LibraryOps()
     comm, P, Q = grid.comm, grid.P, grid.Q
     n, i = comm.world, comm.rank
@@ -278,6 +282,8 @@ def ring_fwd_2d(q, k, v, grid, causal=True, layout="zigzag", ops=None):
         if h_g is not None:
             comm.wait(h_g)
             origin = global_spare[a % 2]
+    if keep_f32:
+        return ops.convert(o_acc, q.dtype), lse_acc, o_acc
     return ops.convert(o_acc, q.dtype), lse_acc
 
 
@@ -342,36 +348,39 @@ def ring_bwd_2d(q, k, v, out, lse, dout, grid, causal=True, layout="zigzag", gra
 # ------------------------------------------------------------------------------------------------
 class _DistributedRingAttention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, comm, groups, causal, layout, ops):
+    def forward(ctx, q, k, v, comm, groups, causal, layout, ops, f32_out):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
         if groups > 1:
-            grid = RingGrid(comm, groups)
-            out, lse = ring_fwd_2d(q, k, v, grid, causal, layout, ops=ops)
+            res = ring_fwd_2d(q, k, v, RingGrid(comm, groups), causal, layout, ops=ops, keep_f32=f32_out)
         else:
-            out, lse = ring_fwd(q, k, v, comm, causal, layout, ops=ops)
-        ctx.save_for_backward(q, k, v, out, lse)
+            res = ring_fwd(q, k, v, comm, causal, layout, ops=ops, keep_f32=f32_out)
+        out, lse = res[0], res[1]
+        ctx.save_for_backward(q, k, v, res[2] if f32_out else out, lse)
         ctx.cfg = (comm, groups, causal, layout, ops)
         return out
 
     @staticmethod
     def backward(ctx, dout):
-        q, k, v, out, lse = ctx.saved_tensors
+        q, k, v, saved, lse = ctx.saved_tensors
         comm, groups, causal, layout, ops = ctx.cfg
         dout = dout.contiguous()
         if groups > 1:
-            grads = ring_bwd_2d(q, k, v, out, lse, dout, RingGrid(comm, groups), causal, layout, q.dtype, ops=ops)
+            grads = ring_bwd_2d(q, k, v, saved, lse, dout, RingGrid(comm, groups), causal, layout, q.dtype, ops=ops)
         else:
-            grads = ring_bwd(q, k, v, out, lse, dout, comm, causal, layout, q.dtype, ops=ops)
-        return grads + (None,) * 5
+            grads = ring_bwd(q, k, v, saved, lse, dout, comm, causal, layout, q.dtype, ops=ops)
+        return grads + (None,) * 6
 
 
-def ring_attention_distributed(q, k, v, comm, causal=True, layout="zigzag", groups=1, ops=None):
+def ring_attention_distributed(q, k, v, comm, causal=True, layout="zigzag", groups=1, ops=None, f32_out=False):
     """Ring attention on this device as a differentiable operation (the pages' RingAttention module,
     LLM-101-CN section 6.2): q [B,H,S,d], k, v [B,Hkv,S,d] are this rank's shard; the forward runs
     the ring (hierarchical with groups > 1) and the backward passes the blocks round again, so that
     every rank receives the gradients of its own shard.  Every rank of the communicator must call it
-    with tensors of the same shapes."""
-    return _DistributedRingAttention.apply(q, k, v, comm, int(groups), causal, layout, ops or LibraryOps())
+    with tensors of the same shapes.  f32_out: keep the float32 running output of the forward for the
+    backward's D instead of the output rounded to q's dtype (twice the saved output's memory; closer
+    to the exact gradient where a gradient is a short sum of large, cancelling terms)."""
+    return _DistributedRingAttention.apply(q, k, v, comm, int(groups), causal, layout, ops or LibraryOps(),
+                                           bool(f32_out))
 
 
 class RingAttention(torch.nn.Module):
@@ -383,12 +392,13 @@ class RingAttention(torch.nn.Module):
     Differences from the page's listing: the running maximum starts at minus infinity instead of
     -1e4 (so that no score is ever clipped), the transfers of the next block overlap the current
     block's work, K/V may have fewer heads than Q (grouped-query attention), and ``causal``,
-    ``layout`` and ``groups`` select the causal mask, the shard layout and the hierarchical ring.
+    ``layout`` and ``groups`` select the causal mask, the shard layout and the hierarchical ring, and
+    ``f32_out`` keeps the float32 output for the backward's D.
     The defaults are the page's: no mask, contiguous shards, one flat ring.  The output is
     differentiable; the backward passes the blocks round the ring again."""
 
     def __init__(self, dim, heads, rank=None, world_size=None, causal=False, layout="contiguous",
-                 groups=1, group=None, ops=None):
+                 groups=1, group=None, ops=None, f32_out=False):
         super().__init__()
         if heads <= 0 or dim % heads:
             raise ValueError(f"dim {dim} is not a multiple of heads {heads}")
@@ -399,9 +409,10 @@ class RingAttention(torch.nn.Module):
         if world_size is not None and world_size != self.comm.world:
             raise ValueError(f"world_size {world_size} is not the group's size {self.comm.world}")
         self.rank, self.world_size = self.comm.rank, self.comm.world
-        self.causal, self.layout, self.groups, self.ops = causal, layout, int(groups), ops
+        self.causal, self.layout, self.groups, self.ops, self.f32_out = causal, layout, int(groups), ops, f32_out
 
     def forward(self, Q, K, V):
         if Q.dim() != 4 or Q.shape[1] != self.heads or Q.shape[-1] != self.head_dim:
             raise ValueError(f"Q of shape {tuple(Q.shape)} is not [bs, {self.heads}, S, {self.head_dim}]")
-        return ring_attention_distributed(Q, K, V, self.comm, self.causal, self.layout, self.groups, self.ops)
+        return ring_attention_distributed(Q, K, V, self.comm, self.causal, self.layout, self.groups, self.ops,
+                                          self.f32_out)

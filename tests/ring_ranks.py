@@ -288,12 +288,13 @@ def run_failing_rank(rank, world, port, mode, result_dir):
 
 
 def run_autograd_rank(rank, world, port, groups, result_dir, device="cpu", causal=True, layout="zigzag",
-                      module=False):
+                      module=False, f32_out=False):
     """ring_attention_distributed under autograd: the output and the gradients that backward() leaves
     on this rank's q, k, v equal its shard of the oracle's whole sequence.  CPU ranks use the oracle's
     block ops (float64, 1e-10); GPU ranks (sharing cuda:0) the library's kernels (bf16 inputs and
     gradients: the bf16 bounds, stored-bf16 for the gradients).  With ``module`` the call goes
-    through the pages' per-rank object, RingAttention(dim, heads, rank, world_size)."""
+    through the pages' per-rank object, RingAttention(dim, heads, rank, world_size); with ``f32_out``
+    the forward's float32 running output is kept for the backward's D."""
     os.environ.setdefault("GLOO_SOCKET_IFNAME", "lo")
     try:
         dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
@@ -317,7 +318,8 @@ def run_autograd_rank(rank, world, port, groups, result_dir, device="cpu", causa
             q, k, v = (shard(x[t], rank, world).cuda().requires_grad_(True) for t in ("q", "k", "v"))
             do, ops = shard(x["dout"], rank, world).cuda(), None
         if module:
-            att = ring.RingAttention(H * d, H, rank, world, causal=causal, layout=layout, groups=groups, ops=ops)
+            att = ring.RingAttention(H * d, H, rank, world, causal=causal, layout=layout, groups=groups, ops=ops,
+                                     f32_out=f32_out)
             out = att(q, k, v)
             for bad in (dict(rank=(rank + 1) % world, world_size=world), dict(rank=rank, world_size=world + 1)):
                 try:
@@ -331,7 +333,8 @@ def run_autograd_rank(rank, world, port, groups, result_dir, device="cpu", causa
             except ValueError:
                 pass
         else:
-            out = ring.ring_attention_distributed(q, k, v, comm, causal, layout, groups=groups, ops=ops)
+            out = ring.ring_attention_distributed(q, k, v, comm, causal, layout, groups=groups, ops=ops,
+                                                  f32_out=f32_out)
         (out.float() * do.float()).sum().backward()
         for got, ref, name in ((out.detach(), ref_o[:, :, sl], "out"), (q.grad, rq[:, :, sl], "dq"),
                                (k.grad, rk[:, :, sl], "dk"), (v.grad, rv[:, :, sl], "dv")):

@@ -127,3 +127,19 @@ def test_eight_ranks_at_16k_flat_and_hierarchical(tmp_path):
                     os.remove(f)
         ok, errs = launch(8, [case], "cuda", str(tmp_path), timeout=900, groups=groups)
         assert ok, f"groups={groups}:\n" + "\n".join(errs)
+
+
+def test_distributed_ring_attention_keeping_the_float32_output_on_one_gpu(tmp_path):
+    """ring_attention_distributed(..., f32_out=True) with the library's kernels, 4 ranks sharing
+    cuda:0: the backward's D from each rank's float32 running output (the mixed-precision
+    preprocess); forward and gradients against the oracle."""
+    import os
+    import torch.multiprocessing as mp
+
+    from ring_ranks import free_port, run_autograd_rank
+
+    mp.start_processes(run_autograd_rank, args=(4, free_port(), 1, str(tmp_path), "cuda", True, "zigzag", False, True),
+                       nprocs=4, join=True, start_method="spawn")
+    errs = [open(tmp_path / f"rank{r}.err").read() for r in range(4) if os.path.exists(tmp_path / f"rank{r}.err")]
+    assert not errs, "\n".join(errs)
+    assert all(os.path.exists(tmp_path / f"rank{r}.ok") for r in range(4))

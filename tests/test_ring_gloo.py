@@ -65,3 +65,18 @@ def test_pages_ring_attention_object(world, groups, causal, layout, tmp_path):
     errs = [open(tmp_path / f"rank{r}.err").read() for r in range(world) if os.path.exists(tmp_path / f"rank{r}.err")]
     assert not errs, "\n".join(errs)
     assert all(os.path.exists(tmp_path / f"rank{r}.ok") for r in range(world))
+
+
+def test_distributed_ring_attention_keeping_the_float32_output(tmp_path):
+    """ring_attention_distributed(..., f32_out=True): the backward takes D from the forward's running
+    output (the plumbing of the float32 output through the autograd function), 3 gloo CPU ranks."""
+    import os
+    import torch.multiprocessing as mp
+
+    from ring_ranks import free_port, run_autograd_rank
+
+    mp.start_processes(run_autograd_rank, args=(3, free_port(), 1, str(tmp_path), "cpu", True, "zigzag", False, True),
+                       nprocs=3, join=True, start_method="spawn")
+    errs = [open(tmp_path / f"rank{r}.err").read() for r in range(3) if os.path.exists(tmp_path / f"rank{r}.err")]
+    assert not errs, "\n".join(errs)
+    assert all(os.path.exists(tmp_path / f"rank{r}.ok") for r in range(3))
