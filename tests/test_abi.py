@@ -256,6 +256,10 @@ def test_block_calls_check_their_arguments(lib):
     assert lib.ring_attn_f32_add(ok16, P(8), LL(4), None) == binding.RA_ERR_INVALID_ARG
     assert lib.ring_attn_f32_convert(ok16, ok16, LL(4), 7, None) == binding.RA_ERR_INVALID_ARG
     assert lib.ring_attn_bwd_preprocess(ok16, ok16, ok16, LL(4), 0, 1, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_bwd_preprocess_f32out(ok16, ok16, ok16, LL(-1), 128, 1, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_bwd_preprocess_f32out(ok16, ok16, ok16, LL(4), 128, 9, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_bwd_preprocess_f32out(ok16, P(8), ok16, LL(4), 128, 1, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_bwd_preprocess_f32out(None, None, None, LL(0), 128, 1, None) == binding.RA_OK
     # an empty count enqueues nothing and needs no device
     assert lib.ring_attn_f32_zero(None, LL(0), None) == binding.RA_OK
     assert lib.ring_attn_f32_convert(None, None, LL(0), 1, None) == binding.RA_OK
