@@ -132,3 +132,16 @@ def test_bwd_preprocess_row_sums(rows, d, dtype):
     got = D[:rows].double().cpu().numpy()
     assert np.allclose(got, ref, rtol=1e-5, atol=1e-5 * np.sqrt(d))
     assert torch.isnan(D[rows:]).all()
+
+
+@pytest.mark.parametrize("rows,d", [(13, 128), (1000, 64), (37, 96)])
+def test_bwd_preprocess_with_a_float32_output(rows, d):
+    """D = rowsum(out * dout) with out in float32 and dout in bf16 (the unrounded output), against
+    float64 sums of the same values."""
+    g = torch.Generator().manual_seed(rows * 7 + d)
+    o = torch.randn(rows, d, generator=g)
+    do = torch.randn(rows, d, generator=g).to(torch.bfloat16)
+    D = ra.bwd_preprocess(o.to(DEV), do.to(DEV))
+    torch.cuda.synchronize()
+    ref = (o.double() * do.double()).sum(-1).numpy()
+    assert np.allclose(D.double().cpu().numpy(), ref, rtol=1e-5, atol=1e-5 * np.sqrt(d))
