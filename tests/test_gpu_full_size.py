@@ -342,3 +342,26 @@ def test_float32_output_backward_at_the_first_positions_against_the_exact_gradie
     idx = torch.from_numpy(keys).to(DEV)
     report(capsys, name, "float32-output backward, dk, keys 0-127 (exact gradient)", to_np(dk.view(-1, d)[idx]), ref_dk)
     report(capsys, name, "float32-output backward, dv, keys 0-127 (exact gradient)", to_np(dv.view(-1, d)[idx]), ref_dv)
+
+
+def test_training_backward_with_bf16_gradients_at_full_size():
+    """The bf16-gradient path at the training size (dQ summed in the float32 workspace, then
+    converted; dK, dV rounded in the kernel's epilogue) gives the float32-gradient path's values
+    rounded to bf16: dK and dV bit for bit; dQ, whose float32 sums add in arrival order in both runs,
+    within one bf16 step plus a floor of 2^-16 of the tensor's largest element for elements whose
+    terms cancel (the order of the additions moves their float32 sum by more than their own bf16
+    step), and within 2^-8 in relative L2."""
+    name = "zigzag_gqa_64k_train"
+    w = synth.WORKLOADS[name]
+    n = w["n"]
+    x = synth.make_workload(name, device=DEV, gen_device=DEV, with_dout=True)
+    out, lse = ra.fwd(x["q"], x["k"], x["v"], n, w["causal"], w["layout"])
+    f = ra.bwd(x["q"], x["k"], x["v"], out, lse, x["dout"], n, w["causal"], w["layout"])
+    h = ra.bwd(x["q"], x["k"], x["v"], out, lse, x["dout"], n, w["causal"], w["layout"], grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert all(t.dtype == torch.bfloat16 for t in h)
+    assert torch.equal(h[1], f[1].to(torch.bfloat16)) and torch.equal(h[2], f[2].to(torch.bfloat16))
+    diff = (h[0].float() - f[0]).abs()
+    bound = f[0].abs() * 2.0 ** -7 + f[0].abs().max() * 2.0 ** -16
+    assert bool((diff <= bound).all()), f"dq: worst excess {(diff - bound).max().item():.3e}"
+    assert (diff.norm() / f[0].norm()).item() <= 2.0 ** -8
