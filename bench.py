@@ -876,6 +876,19 @@ def secondary(ra, w, x, out, lse, stream, dev, peak_b, hbm, args):
         res["train_bwd_only"] = {"tflops": 2.5 * ff / (bms / 1e3) / 1e12, "ms": bms,
                                  "frac": 2.5 * ff / (bms / 1e3) / 1e12 / peak_b,
                                  "how": "forward + backward step time minus the forward's, CUDA events"}
+    if bwd_steps:  # the same step keeping the forward's float32 output for the backward's D
+        o32 = torch.empty(xt["q"].shape, dtype=torch.float32, device=dev)
+
+        def train_step_f32out():
+            ra.fwd_f32out(xt["q"], xt["k"], xt["v"], nt, t["causal"], t["layout"], out=o32, lse=lt, stream=stream)
+            ra.bwd_f32out(xt["q"], xt["k"], xt["v"], o32, lt, xt["dout"], nt, t["causal"], t["layout"],
+                          dq=dq, dk=dk, dv=dv, workspace=wsb, stream=stream)
+
+        ms32 = time_launches(train_step_f32out, bwd_steps, 1, stream)
+        res["train_fwd_bwd_f32out"] = {"tflops": 3.5 * ff / (statistics.mean(ms32) / 1e3) / 1e12,
+                                       "ms": statistics.mean(ms32),
+                                       "what": "ring_attn_fwd_f32out + ring_attn_bwd_f32out (D from the float32 output)"}
+        del o32
     del xt, ot, lt, dq, dk, dv, wsb
     # head dim 64 and the striped layout: the long-context forward and the training step
     for name in ("zigzag_gqa_128k_d64", "striped_gqa_128k", "zigzag_gqa_64k_train_d64", "striped_gqa_64k_train"):

@@ -203,6 +203,53 @@ bwd_preprocess_f32out_kernel(const float* __restrict__ out, const __nv_bfloat16*
     }
 }
 
+// The same for kD = 64 or 128: kD / 4 lanes per row, each 16 bytes of out and 8 of dout, four row
+// groups per warp iteration with all their loads issued before any is used.
+template <int kD>
+__global__ void __launch_bounds__(256)
+bwd_preprocess_f32out_vec_kernel(const float* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
+                                 long long rows, float* __restrict__ D)
+{
+    constexpr int kLanesPerRow = kD / 4;
+    constexpr int kRowsPerLoad = 32 / kLanesPerRow;
+    constexpr int kGroups = 4;
+    constexpr int kRowsPerIter = kRowsPerLoad * kGroups;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / kLanesPerRow;
+    const int c = (lane % kLanesPerRow) * 4;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    const long long w0 = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (long long r0 = w0 * kRowsPerIter; r0 < rows; r0 += warps * kRowsPerIter) {
+        float4 xo[kGroups];
+        uint2 xd[kGroups];
+#pragma unroll
+        for (int k = 0; k < kGroups; ++k) {
+            const long long row = r0 + k * kRowsPerLoad + sub;
+            if (row < rows) {
+                xo[k] = *reinterpret_cast<const float4*>(out + row * kD + c);
+                xd[k] = *reinterpret_cast<const uint2*>(dout + row * kD + c);
+            } else {
+                xo[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                xd[k] = make_uint2(0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kGroups; ++k) {
+            const __nv_bfloat162* pd = reinterpret_cast<const __nv_bfloat162*>(&xd[k]);
+            const float2 d0 = __bfloat1622float2(pd[0]);
+            const float2 d1 = __bfloat1622float2(pd[1]);
+            float acc = fmaf(xo[k].x, d0.x, 0.f);
+            acc = fmaf(xo[k].y, d0.y, acc);
+            acc = fmaf(xo[k].z, d1.x, acc);
+            acc = fmaf(xo[k].w, d1.y, acc);
+#pragma unroll
+            for (int o = kLanesPerRow / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+            const long long row = r0 + k * kRowsPerLoad + sub;
+            if (lane % kLanesPerRow == 0 && row < rows) D[row] = acc;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(256)
 convert_kernel(const float* __restrict__ src, void* __restrict__ dst, int dst_dtype,
                long long count, float scale)
@@ -284,7 +331,13 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, int dtype, 
                                   int d, float* D, cudaStream_t s, int out_dtype)
 {
     if (rows == 0) return cudaSuccess;
-    if (out_dtype == 0 && dtype == 1)
+    if (out_dtype == 0 && dtype == 1 && d == 128)
+        bwd_preprocess_f32out_vec_kernel<128><<<grid_for((rows + 3) / 4, 8), 256, 0, s>>>(
+            static_cast<const float*>(out), static_cast<const __nv_bfloat16*>(dout), rows, D);
+    else if (out_dtype == 0 && dtype == 1 && d == 64)
+        bwd_preprocess_f32out_vec_kernel<64><<<grid_for((rows + 7) / 8, 8), 256, 0, s>>>(
+            static_cast<const float*>(out), static_cast<const __nv_bfloat16*>(dout), rows, D);
+    else if (out_dtype == 0 && dtype == 1)
         bwd_preprocess_f32out_kernel<<<grid_for(rows, 8), 256, 0, s>>>(
             static_cast<const float*>(out), static_cast<const __nv_bfloat16*>(dout), rows, d, D);
     else if (dtype == 0)
